@@ -1,0 +1,456 @@
+"""Benchmark: one step = the whole memory-bound hot path on one GPU.
+
+A step runs, on synthetic data already resident in HBM:
+  * the fused AdamW update over the Llama-7B parameter table (291 tensors,
+    6,738,415,616 params; bf16 grads, fp32 master/m/v, bf16 working copy);
+  * the softmax backward of an attention block at B=8, H=12, S=1024
+    (98,304 x 1,024, causal), once in fp32 and once in bf16;
+  * the LayerNorm backward at B=8, S=2048, D=4096 (bf16 I/O, fp32 dgamma/dbeta).
+Every input is larger than the 129 MB L2, so nothing stays cached between
+launches.  `value` is the algorithmic HBM bytes of a step (30 B/param for
+AdamW, 12 or 6 B/element for softmax, 6 B/element + stats for LayerNorm)
+divided by the device time of the step, summed over ranks for N > 1 (each rank
+runs an independent replica: weak scaling).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With --impl reference the CPU oracle is timed on the host instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("AdamW step Gparams/s + GB/s as % of GB300 HBM peak; softmax/LN bwd GB/s")
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+LOSS_SCALE = 65536.0
+
+# Workload (sizes of the full configurations).
+SM_ROWS, SM_COLS = 8 * 12 * 1024, 1024
+LN_ROWS, LN_D = 8 * 2048, 4096
+FALLBACK_HBM_GBS = 6800.0
+
+
+def adamw_bytes(n_params: int) -> int:
+    # read grad 2 + theta 4 + m 4 + v 4; write theta 4 + m 4 + v 4 + copy 2 + grad 2
+    return 30 * n_params
+
+
+def softmax_bytes(rows: int, cols: int, esize: int) -> int:
+    return 3 * esize * rows * cols              # read P, dY; write dX
+
+
+def layernorm_bytes(rows: int, D: int, esize: int) -> int:
+    # read x, dY; write dX; + mean/inv_std per row; + gamma, dgamma, dbeta per column
+    return 3 * esize * rows * D + 8 * rows + 12 * D
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_over_ranks(values, op="max"):
+    """Max (or sum) of a list of floats over all ranks; identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return t.cpu().tolist()
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows
+                                    if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ----------------------------------------------------------------------------- our arm
+class HotPath:
+    """Device buffers and the C-ABI calls of one step."""
+
+    def __init__(self, device):
+        import torch
+        import ln_backward_gb300 as tb
+        from ln_backward_gb300 import synth
+        self.tb, self.torch = tb, torch
+        self.dev = device
+        self.st = synth.make_adamw_state(synth.llama7b_shapes(), seed=0, device=device,
+                                         grad_std=1e-4, loss_scale=LOSS_SCALE)
+        k = len(self.st.sizes)
+        self.plan = tb.tb_adamw_plan_create(*[[self.st.tensor(a, i) for i in range(k)]
+                                              for a in ("theta", "m", "v", "grad", "copy")])
+        self.P32, self.dY32 = synth.softmax_inputs(SM_ROWS, SM_COLS, torch.float32, seed=1,
+                                                   device=device, causal_period=1024)
+        self.P16, self.dY16 = synth.softmax_inputs(SM_ROWS, SM_COLS, torch.bfloat16, seed=2,
+                                                   device=device, causal_period=1024)
+        self.dX32 = torch.empty_like(self.P32)
+        self.dX16 = torch.empty_like(self.P16)
+        (self.x, self.ldY, self.mean, self.rstd,
+         self.gamma) = synth.layernorm_inputs(LN_ROWS, LN_D, torch.bfloat16, seed=3, device=device,
+                                              eps=1e-5, dy_std=1e-2)
+        self.ldX = torch.empty_like(self.x)
+        self.dg = torch.empty(LN_D, device=device)
+        self.db = torch.empty(LN_D, device=device)
+        ws = tb.tb_layernorm_bwd_workspace_size(LN_ROWS, LN_D, torch.bfloat16)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.t = 0
+        self.n_params = self.st.n_params
+        self.bytes = {
+            "adamw": adamw_bytes(self.n_params),
+            "softmax_f32": softmax_bytes(SM_ROWS, SM_COLS, 4),
+            "softmax_bf16": softmax_bytes(SM_ROWS, SM_COLS, 2),
+            "layernorm_bf16": layernorm_bytes(LN_ROWS, LN_D, 2),
+        }
+        self.launches_per_step = 1 + 1 + 1 + 2
+
+    def step(self, events=None):
+        tb = self.tb
+        self.t += 1
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        rec(0)
+        tb.tb_adamw_step(self.plan, self.t, inv_loss_scale=1.0 / LOSS_SCALE, **HP)
+        rec(1)
+        tb.tb_softmax_bwd(self.dY32, self.P32, self.dX32)
+        rec(2)
+        tb.tb_softmax_bwd(self.dY16, self.P16, self.dX16)
+        rec(3)
+        tb.tb_layernorm_bwd(self.ldY, self.x, self.mean, self.rstd, self.gamma, self.ldX,
+                            self.dg, self.db, self.ws)
+        rec(4)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hp_path = HotPath(dev)
+    names = ["adamw", "softmax_f32", "softmax_bf16", "layernorm_bf16"]
+    K, W = args.steps, args.warmup
+
+    for _ in range(W):
+        hp_path.step()
+    torch.cuda.synchronize()
+    if hp_path.tb.tb_device_error(reset=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    start.record()
+    for k in range(K):
+        hp_path.step(evs[k])
+    end.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i, n in enumerate(names)}
+    mean_ms = {n: statistics.fmean(v) for n, v in per.items()}
+    red = reduce_over_ranks([total_ms] + [mean_ms[n] for n in names], "max")
+    total_ms, mean_ms = red[0], dict(zip(names, red[1:]))
+
+    step_bytes = sum(hp_path.bytes.values())
+    value = world * step_bytes * K / (total_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    kernels = {}
+    for n in names:
+        gbs = hp_path.bytes[n] / (mean_ms[n] / 1e3) / 1e9
+        kernels[n] = {"ms": round(mean_ms[n], 4), "GB_s": round(gbs, 1),
+                      "frac_of_peak": round(gbs / peak, 4), "bytes": hp_path.bytes[n]}
+    kernels["adamw"]["gparams_s"] = round(hp_path.n_params / (mean_ms["adamw"] / 1e3) / 1e9, 2)
+    ad_gbs = kernels["adamw"]["GB_s"]
+
+    e2e = run_e2e(hp_path, K) if not args.no_e2e else None
+    if e2e is not None:
+        e2e_ms = reduce_over_ranks([e2e.pop("ms")], "max")[0]
+        e2e["value"] = round(world * step_bytes * K / (e2e_ms / 1e3) / 1e9, 1)
+
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(seconds_budget=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s",
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {
+                "workload": ("Llama-7B-shaped fused AdamW (291 tensors, 6,738,415,616 params, bf16 "
+                             "grads x65536, fp32 master/m/v, bf16 copy) + softmax bwd 98,304x1,024 "
+                             "causal fp32 and bf16 + LayerNorm bwd 16,384x4,096 bf16"),
+                "bytes_per_step": step_bytes,
+                "adamw_gparams_per_s": kernels["adamw"]["gparams_s"],
+                "l2": "no flush: every launch streams far more than the 129 MB L2",
+                "parallelism": f"replicas x{world}",
+                "wall_s_timed_region": round(wall, 3),
+            },
+            "kernels": kernels,
+            "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": round(ad_gbs / peak, 4), "traffic": ADAMW_TRAFFIC_PER_LAUNCH,
+                         "kernel": "adamw_multi_tensor_kernel", "peak_source": peak_kind},
+            "clocks": clk,
+            "gpu_launches": hp_path.launches_per_step * K,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, from
+# ncu; None until a capture of the current kernel exists.
+ADAMW_TRAFFIC_PER_LAUNCH = None
+
+
+def run_e2e(hp_path, K):
+    """Same step through the public API, starting from pinned host buffers: per step the
+    inputs go host->device, the kernels run, the results come back device->host."""
+    import torch
+    st = hp_path.st
+    pin = dict(pin_memory=True)
+    h_grad = torch.empty_like(st.grad, device="cpu", **pin)
+    h_grad.copy_(st.grad)
+    h_copy = torch.empty_like(st.copy, device="cpu", **pin)
+    ins = [hp_path.P32, hp_path.dY32, hp_path.P16, hp_path.dY16, hp_path.x, hp_path.ldY,
+           hp_path.mean, hp_path.rstd]
+    h_ins = []
+    for t in ins:
+        h = torch.empty_like(t, device="cpu", **pin)
+        h.copy_(t)
+        h_ins.append(h)
+    outs = [hp_path.dX32, hp_path.dX16, hp_path.ldX, hp_path.dg, hp_path.db]
+    h_outs = [torch.empty_like(t, device="cpu", **pin) for t in outs]
+    h2d = h_grad.numel() * 2 + sum(h.numel() * h.element_size() for h in h_ins)
+    d2h = h_copy.numel() * 2 + sum(h.numel() * h.element_size() for h in h_outs)
+
+    def one():
+        st.grad.copy_(h_grad, non_blocking=True)
+        for d, h in zip(ins, h_ins):
+            d.copy_(h, non_blocking=True)
+        hp_path.step()
+        h_copy.copy_(st.copy, non_blocking=True)
+        for h, d in zip(h_outs, outs):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(K):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    barrier()
+    return {"ms": s.elapsed_time(e), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "note": "algorithmic HBM bytes per step / step time including pinned H2D of grads "
+                    "and activations and D2H of the bf16 copy and all backward outputs"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_rates(adamw_n, sm_rows, ln_rows, reps=1):
+    """Seconds per unit of the CPU oracle on bounded samples (inputs prepared outside)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(0)
+    th = rng.standard_normal(adamw_n) * 0.02
+    m = np.zeros(adamw_n)
+    v = np.zeros(adamw_n)
+    g = oracle.encode16(rng.standard_normal(adamw_n) * 1e-4 * LOSS_SCALE, "bf16")
+    oracle.adamw_step_f64(th[:4096], m[:4096], v[:4096], g[:4096], "bf16", 1 / LOSS_SCALE, 1, **HP)
+    P = rng.random((sm_rows, SM_COLS))
+    P /= P.sum(axis=1, keepdims=True)
+    dY = rng.standard_normal((sm_rows, SM_COLS))
+    x = rng.standard_normal((ln_rows, LN_D))
+    ldY = rng.standard_normal((ln_rows, LN_D)) * 1e-2
+    mu = x.mean(axis=1)
+    rs = 1.0 / np.sqrt(x.var(axis=1) + 1e-5)
+    gam = np.ones(LN_D)
+    oracle.softmax_bwd_f64(dY[:8], P[:8])
+    oracle.layernorm_bwd_f64(ldY[:8], x[:8], mu[:8], rs[:8], gam)
+    t_a = t_s = t_l = 0.0
+    for r in range(reps):
+        t0 = time.perf_counter()
+        oracle.adamw_step_f64(th, m, v, g, "bf16", 1 / LOSS_SCALE, r + 1, **HP)
+        t1 = time.perf_counter()
+        oracle.softmax_bwd_f64(dY, P)
+        t2 = time.perf_counter()
+        oracle.layernorm_bwd_f64(ldY, x, mu, rs, gam)
+        t3 = time.perf_counter()
+        t_a += t1 - t0
+        t_s += t2 - t1
+        t_l += t3 - t2
+    return (t_a / (reps * adamw_n), t_s / (reps * sm_rows * SM_COLS),
+            t_l / (reps * ln_rows * LN_D), t_a + t_s + t_l)
+
+
+def _full_step_equivalent(per_param, per_sm, per_ln):
+    """GB/s of the full workload at the oracle's per-unit speeds (single thread)."""
+    n = 6_738_415_616
+    t = (n * per_param + 2 * SM_ROWS * SM_COLS * per_sm + LN_ROWS * LN_D * per_ln)
+    b = (adamw_bytes(n) + softmax_bytes(SM_ROWS, SM_COLS, 4) + softmax_bytes(SM_ROWS, SM_COLS, 2)
+         + layernorm_bytes(LN_ROWS, LN_D, 2))
+    return b / t / 1e9, t
+
+
+def cpu_baseline(seconds_budget=15.0):
+    adamw_n = 1 << 26
+    per_p, per_s, per_l, spent = _oracle_rates(adamw_n, 8192, 4096, reps=1)
+    reps = max(1, min(4, int(seconds_budget / max(spent, 1e-3))))
+    if reps > 1:
+        per_p, per_s, per_l, spent2 = _oracle_rates(adamw_n, 8192, 4096, reps=reps - 1)
+        spent += spent2
+    gbs, t_full = _full_step_equivalent(per_p, per_s, per_l)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"float64 C oracle, single thread, on a 2^26-param AdamW slice, "
+                       f"8192x1024 softmax rows and 4096x4096 LayerNorm rows ({spent:.1f} s of "
+                       f"CPU work); per-unit times scaled to the full step "
+                       f"({t_full:.0f} s per step)"),
+            "adamw_ns_per_param": round(per_p * 1e9, 2)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    adamw_n, sm_rows, ln_rows = 1 << 22, 2048, 1024
+    for _ in range(args.warmup):
+        _oracle_rates(adamw_n, sm_rows, ln_rows)
+    per = [0.0, 0.0, 0.0]
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        p, s, l, _spent = _oracle_rates(adamw_n, sm_rows, ln_rows)
+        per = [per[0] + p, per[1] + s, per[2] + l]
+    wall = time.perf_counter() - t0
+    per = [x / args.steps for x in per]
+    gbs, t_full = _full_step_equivalent(*per)
+    line = {
+        "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_full * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": ("Llama-7B-shaped fused AdamW + softmax bwd 98,304x1,024 fp32 and "
+                                "bf16 + LayerNorm bwd 16,384x4,096 bf16 (per-unit oracle times "
+                                "on bounded samples, scaled to the full step)")},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": (f"each step: 2^22-param AdamW slice, {sm_rows}x1024 softmax, "
+                                    f"{ln_rows}x4096 LayerNorm; {wall:.1f} s wall for the timed steps")},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 1:
+        ap.error("--warmup must be >= 1 (timed numbers use the default of 3)")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

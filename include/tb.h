@@ -1,0 +1,223 @@
+/*
+ * tb.h -- C ABI of the GB300 (sm_103a) memory-bound training-step library.
+ *
+ * The library implements the memory-bound half of an LLM training step as
+ * hand-written CUDA kernels:
+ *   - a fused, multi-tensor, mixed-precision AdamW update;
+ *   - the row-wise softmax backward;
+ *   - the LayerNorm backward (dX, dgamma, dbeta).
+ *
+ * Sources (web pages on the subject; cited by page title and section):
+ *   [GPU-Opt-P2]  "GPU 优化实战 Part 2：用 CUDA/ROCm 实现 LLM 反向传播与训练循环"
+ *   [Mastering]   "Mastering LLM Training with CUDA and ROCm: The Backpropagation
+ *                  and Optimization Workflow"
+ *
+ * Conventions for every entry point
+ *   - Buffers are device-accessible memory owned by the caller, row-major and
+ *     contiguous.  The library keeps no pointer after a call returns, except the
+ *     AdamW plan's copy of the tensor table (see tb_adamw_plan_create).
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Work is enqueued on it and the call returns without waiting: a
+ *     fault inside a kernel surfaces at the caller's next synchronisation.
+ *   - Argument errors are reported synchronously, before anything is enqueued,
+ *     as a tb_status.  A failed launch reports TB_ERR_CUDA.
+ *   - fp32 pointers must be 4-byte aligned and 16-bit pointers 2-byte aligned
+ *     (TB_ERR_MISALIGNED otherwise).  Any larger alignment is optional: 16-byte
+ *     aligned buffers take the vectorised path, others a scalar one.
+ *   - The calls are not thread-safe against tb_adamw_plan_destroy of the plan
+ *     they use; otherwise they may be called from several host threads.
+ */
+#ifndef TB_H_
+#define TB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tb_status {
+    TB_OK = 0,
+    TB_ERR_INVALID_VALUE = 1,     /* null pointer, negative size, step < 1, ... */
+    TB_ERR_UNSUPPORTED_DTYPE = 2, /* dtype not accepted by this entry point     */
+    TB_ERR_MISALIGNED = 3,        /* pointer not aligned to its element size    */
+    TB_ERR_ALIAS = 4,             /* an output overlaps an input or another output */
+    TB_ERR_WORKSPACE = 5,         /* workspace missing or smaller than required */
+    TB_ERR_OOM = 6,               /* the library's own small allocation failed  */
+    TB_ERR_CUDA = 7,              /* a CUDA runtime call or launch failed        */
+    TB_ERR_DEVICE = 8,            /* plan used with another device current       */
+    TB_ERR_TIMEOUT = 9            /* a kernel's bounded wait gave up (see tb_device_error) */
+} tb_status;
+
+typedef enum tb_dtype {
+    TB_F32 = 0,   /* IEEE binary32 */
+    TB_F16 = 1,   /* IEEE binary16 */
+    TB_BF16 = 2   /* bfloat16 */
+} tb_dtype;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* tb_status_string(tb_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int tb_version(void);
+
+/*
+ * tb_device_error -- read (and optionally clear) the device-side error word of
+ * the current device.  Kernels that wait on an mbarrier for their own bulk
+ * copies give up after about one second; they then set this word to a nonzero
+ * code, drain what they issued and return early (their outputs are then
+ * undefined).  This call synchronises the current device.
+ *   code   out: 0 when no kernel gave up since the last reset
+ *   reset  nonzero: clear the word after reading it
+ * Returns TB_OK, TB_ERR_INVALID_VALUE (code == NULL) or TB_ERR_CUDA.
+ */
+tb_status tb_device_error(int* code, int reset);
+
+/* ======================================================================== */
+/* Fused mixed-precision AdamW (multi-tensor)                               */
+/* ======================================================================== */
+/*
+ * One pass over every element of every tensor computes, per element
+ * ([Mastering] §"AdamW Algorithm" update rule; [GPU-Opt-P2] §"AdamW 优化器——
+ * 融合内核" and §"混合精度训练（FP16 / BF16）"):
+ *     g      = float(grad) * inv_loss_scale            (unscale)
+ *     m      = beta1*m + (1-beta1)*g
+ *     v      = beta2*v + (1-beta2)*g*g
+ *     m_hat  = m / (1 - beta1^t),  v_hat = v / (1 - beta2^t)
+ *     param  = param - lr*(m_hat/(sqrt(v_hat)+eps) + weight_decay*param_t)
+ *     copy   = round-to-nearest-even(param) in copy_dtype
+ *     grad   = +0
+ * with decoupled weight decay taken on the pre-update parameter param_t.
+ * The bias corrections and (1-beta) are formed once per call on the host.
+ */
+typedef struct tb_tensor_desc {
+    float* param;   /* fp32 master weights [n], read and written in place        */
+    float* m;       /* fp32 first moment   [n], read and written in place        */
+    float* v;       /* fp32 second moment  [n], read and written in place        */
+    void* grad;     /* loss-scaled gradient [n] in grad_dtype, read then zeroed  */
+    void* copy;     /* working copy [n] in copy_dtype, written                   */
+    int64_t n;      /* element count (>= 0; 0 skips the tensor)                  */
+} tb_tensor_desc;
+
+typedef struct tb_adamw_hparams {
+    float lr;            /* learning rate eta                         */
+    float beta1;         /* first-moment decay, in [0, 1)             */
+    float beta2;         /* second-moment decay, in [0, 1)            */
+    float eps;           /* added to sqrt(v_hat), >= 0                */
+    float weight_decay;  /* decoupled decay lambda, >= 0              */
+} tb_adamw_hparams;
+
+typedef struct tb_adamw_plan tb_adamw_plan;   /* opaque */
+
+/*
+ * tb_adamw_plan_create -- validate a table of parameter tensors and copy it to
+ * the current device once, so that every later step is a single launch.
+ *   tensors     host array of n_tensors descriptors (read during the call only)
+ *   n_tensors   >= 1
+ *   grad_dtype  TB_F16 or TB_BF16
+ *   copy_dtype  TB_BF16 or TB_F16
+ *   out         receives the plan; the caller owns it and frees it with
+ *               tb_adamw_plan_destroy.  The plan owns a device copy of the table
+ *               (64 bytes per tensor) and remembers the current device.
+ * Errors: TB_ERR_INVALID_VALUE (null pointer with n > 0, n < 0, n_tensors < 1,
+ * out == NULL), TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_MISALIGNED, TB_ERR_ALIAS (any
+ * two of the 5*n_tensors buffers overlap), TB_ERR_OOM, TB_ERR_CUDA.
+ */
+tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
+                               tb_dtype grad_dtype, tb_dtype copy_dtype,
+                               tb_adamw_plan** out);
+
+/*
+ * tb_adamw_step -- enqueue one fused AdamW step over every tensor of the plan.
+ *   step            global step t >= 1 (the first update is t = 1)
+ *   hp              hyperparameters (read during the call only)
+ *   inv_loss_scale  1/loss_scale (exact for a power-of-two scale); > 0
+ *   stream          cudaStream_t or NULL
+ * Errors: TB_ERR_INVALID_VALUE (plan/hp NULL, step < 1, beta outside [0,1),
+ * eps, lr or weight_decay negative or not finite, inv_loss_scale <= 0),
+ * TB_ERR_DEVICE (another device is current), TB_ERR_CUDA.
+ */
+tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
+                        const tb_adamw_hparams* hp, float inv_loss_scale,
+                        void* stream);
+
+/* Free a plan (NULL is accepted).  Synchronises nothing: the caller must not
+ * destroy a plan while a step that uses it may still be running. */
+tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan);
+
+/* ======================================================================== */
+/* Softmax backward                                                          */
+/* ======================================================================== */
+/*
+ * tb_softmax_bwd -- for every row r of a [rows, cols] matrix
+ *     dX[r,i] = P[r,i] * (dY[r,i] - sum_j P[r,j]*dY[r,j])
+ * ([GPU-Opt-P2] §2.1 "Softmax 反向内核"), P being the forward softmax output.
+ * The dot product is accumulated in fp32 whatever the I/O dtype.
+ *   dY, P   inputs [rows, cols] in dtype
+ *   dX      output [rows, cols] in dtype; must not overlap dY or P
+ *   rows, cols  >= 0 (either 0: nothing is enqueued)
+ *   dtype   TB_F32, TB_BF16 or TB_F16
+ * Each element of dY and P is read from HBM once when a row fits on chip
+ * (cols <= 8192 fp32 / 16384 16-bit, 16-byte aligned rows); longer or
+ * unaligned rows are read twice.
+ * Errors: TB_ERR_INVALID_VALUE, TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_MISALIGNED,
+ * TB_ERR_ALIAS, TB_ERR_CUDA.
+ */
+tb_status tb_softmax_bwd(const void* dY, const void* P, void* dX,
+                         int64_t rows, int64_t cols, tb_dtype dtype, void* stream);
+
+/* ======================================================================== */
+/* LayerNorm backward                                                        */
+/* ======================================================================== */
+/*
+ * Forward being y = gamma * xhat + beta with xhat = (x - mean) * inv_std over
+ * the D features of each row, the backward computes ([GPU-Opt-P2] §2.2
+ * "LayerNorm 反向"; [Mastering] §"Layer Normalization Backpropagation"):
+ *     dxhat   = dY * gamma
+ *     dX      = inv_std * (dxhat - mean_D(dxhat) - xhat * mean_D(dxhat*xhat))
+ *     dgamma  = sum over rows of dY * xhat     (per column)
+ *     dbeta   = sum over rows of dY            (per column)
+ * dgamma and dbeta are OVERWRITTEN (not accumulated).  They are reduced in two
+ * stages -- per-CTA partial sums into the workspace, then a second kernel that
+ * adds them in a fixed order -- so results are bitwise reproducible run to run
+ * on the same device model.
+ */
+
+/*
+ * tb_layernorm_bwd_workspace_size -- bytes of workspace tb_layernorm_bwd needs
+ * for this shape on the current device (it depends on the SM count).
+ * Errors: TB_ERR_INVALID_VALUE (bytes NULL, rows or D negative),
+ * TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_CUDA.
+ */
+tb_status tb_layernorm_bwd_workspace_size(int64_t rows, int64_t D, tb_dtype io_dtype,
+                                          size_t* bytes);
+
+/*
+ * tb_layernorm_bwd
+ *   dY, x      inputs [rows, D] in io_dtype (TB_F32, TB_BF16 or TB_F16)
+ *   mean       fp32 [rows], the forward's saved row means
+ *   inv_std    fp32 [rows], the forward's saved 1/sqrt(var + eps)
+ *   gamma      fp32 [D]
+ *   dX         output [rows, D] in io_dtype
+ *   dgamma     output fp32 [D]
+ *   dbeta      output fp32 [D]
+ *   workspace  device scratch of at least tb_layernorm_bwd_workspace_size()
+ *              bytes, 16-byte aligned; contents on entry are ignored
+ *   stream     cudaStream_t or NULL
+ * rows == 0 writes zeros to dgamma and dbeta; D == 0 enqueues nothing.
+ * Outputs must not overlap any input, each other or the workspace.
+ * Errors: TB_ERR_INVALID_VALUE, TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_MISALIGNED,
+ * TB_ERR_ALIAS, TB_ERR_WORKSPACE, TB_ERR_CUDA.
+ */
+tb_status tb_layernorm_bwd(const void* dY, const void* x, const float* mean,
+                           const float* inv_std, const float* gamma,
+                           void* dX, float* dgamma, float* dbeta,
+                           int64_t rows, int64_t D, tb_dtype io_dtype,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* TB_H_ */

@@ -1,0 +1,213 @@
+"""ctypes binding over libtb.so -- argument marshalling only.
+
+Every function here carries the name of the C entry point it calls, turns
+torch tensors into (pointer, size, dtype) arguments, passes torch's current
+CUDA stream unless one is given, and raises ``TbError`` on a non-OK status.
+No arithmetic of the kernels happens in Python, and there is no fallback:
+if libtb.so is missing, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtb.so")
+
+TB_F32, TB_F16, TB_BF16 = 0, 1, 2
+_DTYPE = {torch.float32: TB_F32, torch.float16: TB_F16, torch.bfloat16: TB_BF16}
+
+STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_VALUE", 2: "TB_ERR_UNSUPPORTED_DTYPE",
+          3: "TB_ERR_MISALIGNED", 4: "TB_ERR_ALIAS", 5: "TB_ERR_WORKSPACE", 6: "TB_ERR_OOM",
+          7: "TB_ERR_CUDA", 8: "TB_ERR_DEVICE", 9: "TB_ERR_TIMEOUT"}
+
+# Every symbol include/tb.h declares.
+EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_create",
+           "tb_adamw_step", "tb_adamw_plan_destroy", "tb_softmax_bwd",
+           "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd")
+
+
+class TbError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class tb_tensor_desc(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("grad", ctypes.c_void_p), ("copy", ctypes.c_void_p), ("n", ctypes.c_int64)]
+
+
+class tb_adamw_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
+
+
+def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run `python -c 'import __graft_entry__ as g; "
+                          "g.build()'` (needs nvcc) -- there is no CPU fallback")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.tb_status_string.argtypes = [i32]
+    lib.tb_status_string.restype = ctypes.c_char_p
+    lib.tb_version.argtypes = []
+    lib.tb_version.restype = i32
+    lib.tb_device_error.argtypes = [ctypes.POINTER(i32), i32]
+    lib.tb_device_error.restype = i32
+    lib.tb_adamw_plan_create.argtypes = [ctypes.POINTER(tb_tensor_desc), i32, i32, i32,
+                                         ctypes.POINTER(vp)]
+    lib.tb_adamw_plan_create.restype = i32
+    lib.tb_adamw_step.argtypes = [vp, i64, ctypes.POINTER(tb_adamw_hparams), f32, vp]
+    lib.tb_adamw_step.restype = i32
+    lib.tb_adamw_plan_destroy.argtypes = [vp]
+    lib.tb_adamw_plan_destroy.restype = i32
+    lib.tb_softmax_bwd.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+    lib.tb_softmax_bwd.restype = i32
+    lib.tb_layernorm_bwd_workspace_size.argtypes = [i64, i64, i32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.tb_layernorm_bwd_workspace_size.restype = i32
+    lib.tb_layernorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, vp,
+                                     ctypes.c_size_t, vp]
+    lib.tb_layernorm_bwd.restype = i32
+    return lib
+
+
+lib = _load_library()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise TbError(fn, code)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libtb must be contiguous")
+    return t.data_ptr() if t.numel() > 0 else (t.data_ptr() or None)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DTYPE[t.dtype]
+    except KeyError:
+        raise TbError("dtype", 2) from None
+
+
+# ----------------------------------------------------------------------------- misc
+def tb_status_string(code: int) -> str:
+    return lib.tb_status_string(int(code)).decode()
+
+
+def tb_version() -> int:
+    return lib.tb_version()
+
+
+def tb_device_error(reset: bool = True) -> int:
+    """Device-side error word of the current device (0: no kernel gave up)."""
+    code = ctypes.c_int(0)
+    _check("tb_device_error", lib.tb_device_error(ctypes.byref(code), int(reset)))
+    return code.value
+
+
+# ----------------------------------------------------------------------------- AdamW
+class AdamWPlan:
+    """Owns a ``tb_adamw_plan*``; keeps the tensors it points at alive."""
+
+    def __init__(self, handle: int, tensors):
+        self.handle = handle
+        self._keep = tensors
+
+    def close(self) -> None:
+        if self.handle:
+            _check("tb_adamw_plan_destroy", lib.tb_adamw_plan_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tb_adamw_plan_create(params: Sequence[torch.Tensor], ms: Sequence[torch.Tensor],
+                         vs: Sequence[torch.Tensor], grads: Sequence[torch.Tensor],
+                         copies: Sequence[torch.Tensor]) -> AdamWPlan:
+    n = len(params)
+    if not (len(ms) == len(vs) == len(grads) == len(copies) == n):
+        raise ValueError("params, m, v, grads and copies must have one entry per tensor")
+    descs = (tb_tensor_desc * max(n, 1))()
+    for i in range(n):
+        descs[i] = tb_tensor_desc(_ptr(params[i]), _ptr(ms[i]), _ptr(vs[i]), _ptr(grads[i]),
+                                  _ptr(copies[i]), params[i].numel())
+    gdt = _dtype(grads[0]) if n else TB_BF16
+    cdt = _dtype(copies[0]) if n else TB_BF16
+    handle = ctypes.c_void_p(None)
+    _check("tb_adamw_plan_create",
+           lib.tb_adamw_plan_create(descs, n, gdt, cdt, ctypes.byref(handle)))
+    return AdamWPlan(handle.value, (list(params), list(ms), list(vs), list(grads), list(copies)))
+
+
+def tb_adamw_step(plan: AdamWPlan, step: int, lr: float, beta1: float, beta2: float, eps: float,
+                  weight_decay: float, inv_loss_scale: float, stream=None) -> None:
+    hp = tb_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+    _check("tb_adamw_step", lib.tb_adamw_step(plan.handle, int(step), ctypes.byref(hp),
+                                              float(inv_loss_scale), _stream(stream)))
+
+
+def tb_adamw_plan_destroy(plan: AdamWPlan) -> None:
+    plan.close()
+
+
+# ----------------------------------------------------------------------------- softmax bwd
+def tb_softmax_bwd(dY: torch.Tensor, P: torch.Tensor, dX: torch.Tensor, stream=None) -> None:
+    """dX = P * (dY - rowsum(P*dY)) over the last dimension of [rows, cols] tensors."""
+    if not (dY.shape == P.shape == dX.shape) or dY.dim() != 2:
+        raise ValueError("dY, P and dX must be [rows, cols] tensors of one shape")
+    if not (dY.dtype == P.dtype == dX.dtype):
+        raise ValueError("dY, P and dX must share a dtype")
+    rows, cols = dY.shape
+    _check("tb_softmax_bwd", lib.tb_softmax_bwd(_ptr(dY), _ptr(P), _ptr(dX), rows, cols,
+                                                _dtype(dY), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- LayerNorm bwd
+def tb_layernorm_bwd_workspace_size(rows: int, D: int, dtype: torch.dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check("tb_layernorm_bwd_workspace_size",
+           lib.tb_layernorm_bwd_workspace_size(int(rows), int(D), _DTYPE[dtype], ctypes.byref(out)))
+    return out.value
+
+
+def tb_layernorm_bwd(dY: torch.Tensor, x: torch.Tensor, mean: torch.Tensor, inv_std: torch.Tensor,
+                     gamma: torch.Tensor, dX: torch.Tensor, dgamma: torch.Tensor,
+                     dbeta: torch.Tensor, workspace: Optional[torch.Tensor], stream=None) -> None:
+    if x.dim() != 2 or dY.shape != x.shape or dX.shape != x.shape:
+        raise ValueError("x, dY and dX must be [rows, D] tensors of one shape")
+    if not (dY.dtype == x.dtype == dX.dtype):
+        raise ValueError("x, dY and dX must share a dtype")
+    for t in (mean, inv_std, gamma, dgamma, dbeta):
+        if t.dtype != torch.float32:
+            raise ValueError("mean, inv_std, gamma, dgamma and dbeta are fp32")
+    rows, D = x.shape
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("tb_layernorm_bwd",
+           lib.tb_layernorm_bwd(_ptr(dY), _ptr(x), _ptr(mean), _ptr(inv_std), _ptr(gamma),
+                                _ptr(dX), _ptr(dgamma), _ptr(dbeta), rows, D, _dtype(x), ws_ptr,
+                                ws_bytes, _stream(stream)))

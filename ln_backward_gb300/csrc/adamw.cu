@@ -1,0 +1,333 @@
+// adamw.cu -- fused, multi-tensor, mixed-precision AdamW step.
+//
+// Per element ("Mastering LLM Training with CUDA and ROCm", section "AdamW
+// Algorithm"; "GPU 优化实战 Part 2", sections "AdamW 优化器——融合内核" and
+// "混合精度训练（FP16 / BF16）"):
+//   g = float(grad) * inv_loss_scale
+//   m = b1*m + (1-b1)*g ;  v = b2*v + (1-b2)*g^2
+//   param = param - lr*( (m/bc1) / (sqrt(v/bc2) + eps) + wd*param )
+//   copy = rne(param) ;  grad = 0
+//
+// Design (GB300): one launch covers every tensor of the model.  The host plan
+// holds a device table of tensors and a prefix sum of their "units" (8
+// elements = one 16-byte vector of the 16-bit gradient and two of each fp32
+// stream).  The flat unit space is cut into one contiguous range per CTA (grid
+// = SM count x resident CTAs); each CTA finds its first tensor by binary search
+// and walks forward.  Every thread moves 2 units per iteration with 128-bit
+// evict-first loads and stores: 14 B read and 16 B written per element, one
+// HBM pass.  Tensors whose five pointers are not all 16-byte aligned, and the
+// last partial unit of a tensor, take a scalar path.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <new>
+#include <vector>
+
+#include "tb_common.cuh"
+
+namespace tb {
+namespace {
+
+constexpr int kUnit = 8;        // elements per unit
+constexpr int kThreads = 256;   // threads per CTA
+constexpr int kUnroll = 2;      // units in flight per thread
+constexpr uint64_t kPlanMagic = 0x7462616461707731ull;
+
+struct alignas(16) TensorEntry {
+    float* p;
+    float* m;
+    float* v;
+    void* g;
+    void* c;
+    int64_t n;
+    int64_t unit_begin;   // prefix sum of ceil(n/8) over the preceding tensors
+    int32_t vec_ok;       // all five pointers 16-byte aligned
+    int32_t pad;
+};
+static_assert(sizeof(TensorEntry) == 64, "table entry is one 64-byte line");
+
+// Per-step scalars, hoisted on the host.
+struct Scalars {
+    float lr, beta1, beta2, eps, wd;
+    float omb1, omb2;   // 1 - beta, formed in fp32
+    float bc1, bc2;     // 1 - beta^t, formed in double and rounded
+    float inv_s;        // 1 / loss_scale
+};
+
+__device__ __forceinline__ void adamw_update(float& th, float& m, float& v, float g_scaled,
+                                             const Scalars& s) {
+    const float g = g_scaled * s.inv_s;
+    m = s.beta1 * m + s.omb1 * g;
+    v = s.beta2 * v + s.omb2 * (g * g);
+    const float m_hat = m / s.bc1;
+    const float v_hat = v / s.bc2;
+    const float u = m_hat / (sqrtf(v_hat) + s.eps);
+    th = th - s.lr * (u + s.wd * th);
+}
+
+template <class G, class C>
+__device__ __forceinline__ void scalar_element(const TensorEntry& t, int64_t i, const Scalars& s) {
+    using GT = typename G::T;
+    using CT = typename C::T;
+    float th = t.p[i], m = t.m[i], v = t.v[i];
+    GT* gp = static_cast<GT*>(t.g);
+    adamw_update(th, m, v, G::to_f32(gp[i]), s);
+    t.p[i] = th;
+    t.m[i] = m;
+    t.v[i] = v;
+    static_cast<CT*>(t.c)[i] = C::from_f32(th);
+    gp[i] = G::from_f32(0.0f);
+}
+
+// Units [a, e) of one tensor (local unit indices).
+template <class G, class C>
+__device__ __forceinline__ void process_segment(const TensorEntry& t, int64_t a, int64_t e,
+                                                const Scalars& s) {
+    using GT = typename G::T;
+    using CT = typename C::T;
+    const int64_t n = t.n;
+    const int64_t full = n / kUnit;   // units holding 8 valid elements
+    if (t.vec_ok) {
+        const int64_t fe = e < full ? e : full;
+        for (int64_t base = a + threadIdx.x; base < fe; base += (int64_t)kThreads * kUnroll) {
+            float th[kUnroll][8], mm[kUnroll][8], vv[kUnroll][8], gg[kUnroll][8];
+            bool act[kUnroll];
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j) {
+                const int64_t uu = base + (int64_t)j * kThreads;
+                act[j] = uu < fe;
+                if (act[j]) {
+                    const int64_t i0 = uu * kUnit;
+                    float4 a0 = ld_stream_f4(t.p + i0), a1 = ld_stream_f4(t.p + i0 + 4);
+                    float4 b0 = ld_stream_f4(t.m + i0), b1 = ld_stream_f4(t.m + i0 + 4);
+                    float4 c0 = ld_stream_f4(t.v + i0), c1 = ld_stream_f4(t.v + i0 + 4);
+                    uint4 gr = ld_stream_u4(static_cast<const GT*>(t.g) + i0);
+                    th[j][0] = a0.x; th[j][1] = a0.y; th[j][2] = a0.z; th[j][3] = a0.w;
+                    th[j][4] = a1.x; th[j][5] = a1.y; th[j][6] = a1.z; th[j][7] = a1.w;
+                    mm[j][0] = b0.x; mm[j][1] = b0.y; mm[j][2] = b0.z; mm[j][3] = b0.w;
+                    mm[j][4] = b1.x; mm[j][5] = b1.y; mm[j][6] = b1.z; mm[j][7] = b1.w;
+                    vv[j][0] = c0.x; vv[j][1] = c0.y; vv[j][2] = c0.z; vv[j][3] = c0.w;
+                    vv[j][4] = c1.x; vv[j][5] = c1.y; vv[j][6] = c1.z; vv[j][7] = c1.w;
+                    unpack8<G>(gr, gg[j]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j) {
+                if (!act[j]) continue;
+                const int64_t i0 = (base + (int64_t)j * kThreads) * kUnit;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) adamw_update(th[j][q], mm[j][q], vv[j][q], gg[j][q], s);
+                st_stream_f4(t.p + i0, make_float4(th[j][0], th[j][1], th[j][2], th[j][3]));
+                st_stream_f4(t.p + i0 + 4, make_float4(th[j][4], th[j][5], th[j][6], th[j][7]));
+                st_stream_f4(t.m + i0, make_float4(mm[j][0], mm[j][1], mm[j][2], mm[j][3]));
+                st_stream_f4(t.m + i0 + 4, make_float4(mm[j][4], mm[j][5], mm[j][6], mm[j][7]));
+                st_stream_f4(t.v + i0, make_float4(vv[j][0], vv[j][1], vv[j][2], vv[j][3]));
+                st_stream_f4(t.v + i0 + 4, make_float4(vv[j][4], vv[j][5], vv[j][6], vv[j][7]));
+                st_stream_u4(static_cast<CT*>(t.c) + i0, pack8<C>(th[j]));
+                st_stream_u4(static_cast<GT*>(t.g) + i0, make_uint4(0u, 0u, 0u, 0u));
+            }
+        }
+        // The tensor's last, partial unit (fewer than 8 elements).
+        if (full >= a && full < e) {
+            for (int64_t i = full * kUnit + threadIdx.x; i < n; i += kThreads)
+                scalar_element<G, C>(t, i, s);
+        }
+    } else {
+        const int64_t hi = e * kUnit < n ? e * kUnit : n;
+        for (int64_t i = a * kUnit + threadIdx.x; i < hi; i += kThreads)
+            scalar_element<G, C>(t, i, s);
+    }
+}
+
+template <class G, class C>
+__global__ void __launch_bounds__(kThreads, 2)
+adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
+                          int64_t units_per_cta, Scalars s) {
+    const int64_t u_lo = (int64_t)blockIdx.x * units_per_cta;
+    if (u_lo >= total_units) return;
+    const int64_t u_hi = u_lo + units_per_cta < total_units ? u_lo + units_per_cta : total_units;
+    // Last tensor whose first unit is <= u_lo.
+    int lo = 0, hi = ntab - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab[mid].unit_begin <= u_lo) lo = mid; else hi = mid - 1;
+    }
+    int k = lo;
+    int64_t u = u_lo;
+    while (u < u_hi && k < ntab) {
+        const TensorEntry t = tab[k];
+        const int64_t t_end = (k + 1 < ntab) ? tab[k + 1].unit_begin : total_units;
+        const int64_t seg_hi = u_hi < t_end ? u_hi : t_end;
+        if (seg_hi > u) process_segment<G, C>(t, u - t.unit_begin, seg_hi - t.unit_begin, s);
+        u = seg_hi > u ? seg_hi : u;
+        ++k;
+    }
+}
+
+template <class G, class C>
+const void* kernel_for() {
+    return reinterpret_cast<const void*>(&adamw_multi_tensor_kernel<G, C>);
+}
+
+const void* select_kernel(tb_dtype g, tb_dtype c) {
+    if (g == TB_BF16 && c == TB_BF16) return kernel_for<BF16, BF16>();
+    if (g == TB_BF16 && c == TB_F16) return kernel_for<BF16, F16>();
+    if (g == TB_F16 && c == TB_BF16) return kernel_for<F16, BF16>();
+    return kernel_for<F16, F16>();
+}
+
+}  // namespace
+}  // namespace tb
+
+struct tb_adamw_plan {
+    uint64_t magic;
+    int device;
+    int n_tensors;
+    tb_dtype grad_dtype;
+    tb_dtype copy_dtype;
+    tb::TensorEntry* d_table;
+    int64_t total_units;
+    int grid;
+};
+
+extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
+                                          tb_dtype grad_dtype, tb_dtype copy_dtype,
+                                          tb_adamw_plan** out) {
+    using namespace tb;
+    if (!out || !tensors || n_tensors < 1) return TB_ERR_INVALID_VALUE;
+    *out = nullptr;
+    if (grad_dtype != TB_BF16 && grad_dtype != TB_F16) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (copy_dtype != TB_BF16 && copy_dtype != TB_F16) return TB_ERR_UNSUPPORTED_DTYPE;
+
+    std::vector<TensorEntry> tab(n_tensors);
+    std::vector<Range> ranges;
+    ranges.reserve(5 * (size_t)n_tensors);
+    int64_t units = 0;
+    for (int i = 0; i < n_tensors; ++i) {
+        const tb_tensor_desc& d = tensors[i];
+        if (d.n < 0) return TB_ERR_INVALID_VALUE;
+        if (d.n > 0 && (!d.param || !d.m || !d.v || !d.grad || !d.copy)) return TB_ERR_INVALID_VALUE;
+        if (d.n > 0 && (!aligned_to(d.param, 4) || !aligned_to(d.m, 4) || !aligned_to(d.v, 4) ||
+                        !aligned_to(d.grad, 2) || !aligned_to(d.copy, 2)))
+            return TB_ERR_MISALIGNED;
+        if (d.n > INT64_MAX / 8 - units * 8) return TB_ERR_INVALID_VALUE;
+        TensorEntry& t = tab[i];
+        t.p = d.param;
+        t.m = d.m;
+        t.v = d.v;
+        t.g = d.grad;
+        t.c = d.copy;
+        t.n = d.n;
+        t.unit_begin = units;
+        t.vec_ok = aligned_to(d.param, 16) && aligned_to(d.m, 16) && aligned_to(d.v, 16) &&
+                   aligned_to(d.grad, 16) && aligned_to(d.copy, 16);
+        t.pad = 0;
+        units += (d.n + kUnit - 1) / kUnit;
+        ranges.push_back(range_of(d.param, d.n, 4));
+        ranges.push_back(range_of(d.m, d.n, 4));
+        ranges.push_back(range_of(d.v, d.n, 4));
+        ranges.push_back(range_of(d.grad, d.n, 2));
+        ranges.push_back(range_of(d.copy, d.n, 2));
+    }
+    // No two buffers may overlap: sort by start, compare with the furthest end so far.
+    ranges.erase(std::remove_if(ranges.begin(), ranges.end(),
+                                [](const Range& r) { return r.lo == r.hi; }),
+                 ranges.end());
+    std::sort(ranges.begin(), ranges.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+    uintptr_t reach = 0;
+    for (size_t i = 0; i < ranges.size(); ++i) {
+        if (i > 0 && ranges[i].lo < reach) return TB_ERR_ALIAS;
+        reach = std::max(reach, ranges[i].hi);
+    }
+
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_kernel(grad_dtype, copy_dtype),
+                                                      kThreads, 0) != cudaSuccess)
+        return TB_ERR_CUDA;
+    per_sm = std::max(per_sm, 1);
+
+    tb_adamw_plan* plan = new (std::nothrow) tb_adamw_plan;
+    if (!plan) return TB_ERR_OOM;
+    plan->magic = kPlanMagic;
+    plan->device = dev;
+    plan->n_tensors = n_tensors;
+    plan->grad_dtype = grad_dtype;
+    plan->copy_dtype = copy_dtype;
+    plan->total_units = units;
+    plan->grid = info.sm_count * per_sm;
+    plan->d_table = nullptr;
+    const size_t bytes = sizeof(TensorEntry) * (size_t)n_tensors;
+    cudaError_t e = cudaMalloc(&plan->d_table, bytes);
+    if (e != cudaSuccess) {
+        delete plan;
+        cudaGetLastError();
+        return e == cudaErrorMemoryAllocation ? TB_ERR_OOM : TB_ERR_CUDA;
+    }
+    if (cudaMemcpy(plan->d_table, tab.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(plan->d_table);
+        delete plan;
+        return TB_ERR_CUDA;
+    }
+    *out = plan;
+    return TB_OK;
+}
+
+extern "C" tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
+                                   const tb_adamw_hparams* hp, float inv_loss_scale,
+                                   void* stream) {
+    using namespace tb;
+    if (!plan || !hp || plan->magic != kPlanMagic) return TB_ERR_INVALID_VALUE;
+    if (step < 1) return TB_ERR_INVALID_VALUE;
+    const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
+    if (!std::isfinite(lr) || lr < 0.f) return TB_ERR_INVALID_VALUE;
+    if (!(b1 >= 0.f && b1 < 1.f) || !(b2 >= 0.f && b2 < 1.f)) return TB_ERR_INVALID_VALUE;
+    if (!std::isfinite(eps) || eps < 0.f) return TB_ERR_INVALID_VALUE;
+    if (!std::isfinite(wd) || wd < 0.f) return TB_ERR_INVALID_VALUE;
+    if (!std::isfinite(inv_loss_scale) || !(inv_loss_scale > 0.f)) return TB_ERR_INVALID_VALUE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TB_ERR_CUDA;
+    if (dev != plan->device) return TB_ERR_DEVICE;
+    if (plan->total_units == 0) return TB_OK;
+
+    Scalars s;
+    s.lr = lr;
+    s.beta1 = b1;
+    s.beta2 = b2;
+    s.eps = eps;
+    s.wd = wd;
+    s.omb1 = 1.0f - b1;
+    s.omb2 = 1.0f - b2;
+    s.bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(b1), static_cast<double>(step)));
+    s.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(b2), static_cast<double>(step)));
+    s.inv_s = inv_loss_scale;
+
+    const int64_t grid = std::min<int64_t>(plan->grid, plan->total_units);
+    const int64_t per_cta = (plan->total_units + grid - 1) / grid;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const tb::TensorEntry* tab = plan->d_table;
+    const int nt = plan->n_tensors;
+    const int64_t tu = plan->total_units;
+    const tb_dtype g = plan->grad_dtype, c = plan->copy_dtype;
+    if (g == TB_BF16 && c == TB_BF16)
+        adamw_multi_tensor_kernel<BF16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+    else if (g == TB_BF16 && c == TB_F16)
+        adamw_multi_tensor_kernel<BF16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+    else if (g == TB_F16 && c == TB_BF16)
+        adamw_multi_tensor_kernel<F16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+    else
+        adamw_multi_tensor_kernel<F16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+    return launch_status();
+}
+
+extern "C" tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan) {
+    if (!plan) return TB_OK;
+    if (plan->magic != tb::kPlanMagic) return TB_ERR_INVALID_VALUE;
+    plan->magic = 0;
+    tb_status st = TB_OK;
+    if (plan->d_table && cudaFree(plan->d_table) != cudaSuccess) st = TB_ERR_CUDA;
+    delete plan;
+    return st;
+}

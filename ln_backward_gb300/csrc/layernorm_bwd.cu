@@ -1,0 +1,600 @@
+// layernorm_bwd.cu -- LayerNorm backward from the saved mean / inv_std.
+//
+//   xhat = (x - mean) * inv_std,  dxhat = dY * gamma
+//   dX   = inv_std * (dxhat - mean_D(dxhat) - xhat * mean_D(dxhat * xhat))
+//   dgamma_j = sum_rows dY*xhat,  dbeta_j = sum_rows dY
+// ("GPU 优化实战 Part 2：用 CUDA/ROCm 实现 LLM 反向传播与训练循环", section 2.2
+// "LayerNorm 反向": saved mean/inv_std, gamma/beta gradients by reduction, dX
+// from the normalised values; the reduction runs over rows, per feature.)
+//
+// Design (GB300):
+//  * Kernel 1 (rows): persistent CTAs, each owning a contiguous block of rows.
+//    One elected thread streams the x and dY rows into a ring of shared-memory
+//    stages with 1-D bulk async copies (cp.async.bulk, completion counted on an
+//    mbarrier), several rows ahead, so HBM stays busy without holding the rows
+//    in registers.  Each thread owns a fixed set of 16-byte column vectors:
+//    it keeps gamma and its dgamma/dbeta partial sums for those columns in
+//    registers across all rows of the CTA.  Phase 1 reads the staged row and
+//    forms the two row sums (dxhat, dxhat*xhat) with a warp butterfly plus one
+//    shared-memory exchange and one barrier per row; phase 2 re-reads the
+//    staged row (shared memory, not HBM), writes dX and accumulates the column
+//    partials.  A stage is refilled one row later, once every thread is past
+//    it.  At the end each CTA stores its column partials to the workspace.
+//  * Kernel 2 (columns): adds the per-CTA partials in a fixed order -> dgamma,
+//    dbeta, bitwise reproducible run to run.
+//  * Rows whose byte length is not a multiple of 16, unaligned buffers, or D
+//    beyond the register budget use a plain-load fallback of the same
+//    structure (two passes over the row, partials kept in the workspace).
+//
+// Every mbarrier wait is bounded (about one second of %globaltimer); on expiry
+// the CTA sets the device error word, waits (bounded) for the copies it issued
+// and returns.
+#include <algorithm>
+
+#include "tb_common.cuh"
+
+namespace tb {
+namespace {
+
+constexpr int kRowThreads = 256;               // max threads of the row kernels
+constexpr int kMaxWarps = kRowThreads / 32;
+constexpr int kMaxStages = 4;
+constexpr int kMaxElemsPerThread = 32;
+constexpr int kRingBudget = 96 * 1024;         // bytes of ring per CTA we aim for
+constexpr int kBarRegion = 128;                // bytes reserved for the mbarriers
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with this parity to complete; false after ~1 s.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared; completion is counted on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Read one 16-byte vector from shared memory as fp32 values.
+template <class Fmt>
+__device__ __forceinline__ void lds_vec(const void* p, float (&f)[Vec<Fmt>::kElems]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const typename Fmt::T* h = reinterpret_cast<const typename Fmt::T*>(&u);
+#pragma unroll
+    for (int e = 0; e < Vec<Fmt>::kElems; ++e) f[e] = Fmt::to_f32(h[e]);
+}
+
+// ------------------------------------------------------------------ row kernel (bulk-copy ring)
+// Columns per thread NV*E up to 16 fit two CTAs per SM; 32 need the full budget.
+template <class Fmt, int NV>
+__global__ void __launch_bounds__(kRowThreads, (NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
+ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
+                        const float* __restrict__ mean, const float* __restrict__ inv_std,
+                        const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
+                        float* __restrict__ partials, int64_t rows, int D, int stages,
+                        int64_t rows_per_cta, int* err) {
+    using T = typename Fmt::T;
+    constexpr int E = Vec<Fmt>::kElems;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[2][2][kMaxWarps];
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int nvec = D / E;
+    const uint32_t row_bytes = (uint32_t)D * (uint32_t)sizeof(T);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    unsigned char* ring = smem + kBarRegion;   // stage s: [x row | dY row]
+
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = r0 + rows_per_cta < rows ? r0 + rows_per_cta : rows;
+    const int64_t nrows = r1 > r0 ? r1 - r0 : 0;
+
+    uint64_t pol = 0;
+    int64_t issued = 0;   // meaningful in thread 0 only
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+        mbar_init_fence();
+        pol = evict_first_policy();
+        for (; issued < nrows && issued < stages; ++issued) {
+            const int s = (int)issued;
+            const uint32_t bar = smem_addr(&bars[s]);
+            unsigned char* st = ring + (size_t)s * 2 * row_bytes;
+            mbar_arrive_expect_tx(bar, 2 * row_bytes);
+            bulk_g2s(smem_addr(st), x + (r0 + issued) * D, row_bytes, bar, pol);
+            bulk_g2s(smem_addr(st + row_bytes), dY + (r0 + issued) * D, row_bytes, bar, pol);
+        }
+    }
+
+    float g[NV][E], acc_g[NV][E], acc_b[NV][E];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int vi = tid + k * nthreads;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            g[k][e] = vi < nvec ? gamma[vi * E + e] : 0.f;
+            acc_g[k][e] = 0.f;
+            acc_b[k][e] = 0.f;
+        }
+    }
+    __syncthreads();   // barriers initialised before anyone waits on them
+
+    const float inv_D = 1.0f / (float)D;
+    int64_t fail_at = -1;
+    for (int64_t i = 0; i < nrows; ++i) {
+        const int s = (int)(i % stages);
+        const uint32_t parity = (uint32_t)((i / stages) & 1);
+        const int64_t r = r0 + i;
+        const float mu = mean[r], rs = inv_std[r];
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity);
+        const unsigned char* st = ring + (size_t)s * 2 * row_bytes;
+
+        // Phase 1: the two row sums, from the staged row.
+        float sa = 0.f, sb = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int vi = tid + k * nthreads;
+                if (vi < nvec) {
+                    float xv[E], dy[E];
+                    lds_vec<Fmt>(st + (size_t)vi * 16, xv);
+                    lds_vec<Fmt>(st + row_bytes + (size_t)vi * 16, dy);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float xh = (xv[e] - mu) * rs;
+                        const float dxh = dy[e] * g[k][e];
+                        sa += dxh;
+                        sb += dxh * xh;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, o);
+            sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        }
+        const int buf = (int)(i & 1);
+        if (lane == 0) {
+            red[buf][0][wid] = sa;
+            red[buf][1][wid] = sb;
+        }
+        // Past this barrier every thread has finished row i-1 entirely, so its
+        // stage can be refilled; row i's stage is still read below.
+        if (__syncthreads_or(!ok)) {
+            fail_at = i;
+            break;
+        }
+        if (tid == 0 && i >= 1 && issued < nrows) {
+            const int sp = (int)((i - 1) % stages);
+            const uint32_t bar = smem_addr(&bars[sp]);
+            unsigned char* dst = ring + (size_t)sp * 2 * row_bytes;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, 2 * row_bytes);
+            bulk_g2s(smem_addr(dst), x + (r0 + issued) * D, row_bytes, bar, pol);
+            bulk_g2s(smem_addr(dst + row_bytes), dY + (r0 + issued) * D, row_bytes, bar, pol);
+            ++issued;
+        }
+        float a = 0.f, b = 0.f;
+        for (int w = 0; w < nwarps; ++w) {
+            a += red[buf][0][w];
+            b += red[buf][1][w];
+        }
+        const float mean_a = a * inv_D, mean_b = b * inv_D;
+
+        // Phase 2: dX and the column partials, re-reading the staged row.
+        T* dxr = dX + r * D;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int vi = tid + k * nthreads;
+            if (vi < nvec) {
+                float xv[E], dy[E], out[E];
+                lds_vec<Fmt>(st + (size_t)vi * 16, xv);
+                lds_vec<Fmt>(st + row_bytes + (size_t)vi * 16, dy);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float xh = (xv[e] - mu) * rs;
+                    const float dxh = dy[e] * g[k][e];
+                    out[e] = rs * (dxh - mean_a - xh * mean_b);
+                    acc_g[k][e] += dy[e] * xh;
+                    acc_b[k][e] += dy[e];
+                }
+                store_vec<Fmt>(dxr + (size_t)vi * E, out);
+            }
+        }
+    }
+
+    if (fail_at >= 0) {
+        // Rows [fail_at, issued) still have copies in flight (at most one per
+        // stage): wait for them, bounded, before the CTA's shared memory is freed.
+        if (tid == 0) {
+            atomicExch(err, (int)TB_ERR_TIMEOUT);
+            for (int64_t q = fail_at; q < issued; ++q)
+                mbar_wait_bounded(smem_addr(&bars[q % stages]), (uint32_t)((q / stages) & 1));
+        }
+        __syncthreads();
+        return;
+    }
+
+    float* pg = partials + (size_t)blockIdx.x * 2 * D;
+    float* pb = pg + D;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int vi = tid + k * nthreads;
+        if (vi < nvec) {
+#pragma unroll
+            for (int e = 0; e < E; e += 4) {
+                *reinterpret_cast<float4*>(pg + vi * E + e) =
+                    make_float4(acc_g[k][e], acc_g[k][e + 1], acc_g[k][e + 2], acc_g[k][e + 3]);
+                *reinterpret_cast<float4*>(pb + vi * E + e) =
+                    make_float4(acc_b[k][e], acc_b[k][e + 1], acc_b[k][e + 2], acc_b[k][e + 3]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ row kernel (plain loads)
+template <class Fmt>
+__global__ void __launch_bounds__(kRowThreads)
+ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
+                         const float* __restrict__ mean, const float* __restrict__ inv_std,
+                         const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
+                         float* __restrict__ partials, int64_t rows, int64_t D, int64_t rows_per_cta) {
+    __shared__ float red[2][2][kMaxWarps];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    float* pg = partials + (size_t)blockIdx.x * 2 * D;
+    float* pb = pg + D;
+    for (int64_t j = tid; j < D; j += blockDim.x) { pg[j] = 0.f; pb[j] = 0.f; }
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = r0 + rows_per_cta < rows ? r0 + rows_per_cta : rows;
+    const float inv_D = 1.0f / (float)D;
+    int buf = 0;
+    for (int64_t r = r0; r < r1; ++r, buf ^= 1) {
+        const float mu = mean[r], rs = inv_std[r];
+        const int64_t off = r * D;
+        float sa = 0.f, sb = 0.f;
+        for (int64_t j = tid; j < D; j += blockDim.x) {
+            const float xh = (Fmt::to_f32(x[off + j]) - mu) * rs;
+            const float dxh = Fmt::to_f32(dY[off + j]) * gamma[j];
+            sa += dxh;
+            sb += dxh * xh;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, o);
+            sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        }
+        if (lane == 0) {
+            red[buf][0][wid] = sa;
+            red[buf][1][wid] = sb;
+        }
+        __syncthreads();
+        float a = 0.f, b = 0.f;
+        for (int w = 0; w < nwarps; ++w) {
+            a += red[buf][0][w];
+            b += red[buf][1][w];
+        }
+        const float mean_a = a * inv_D, mean_b = b * inv_D;
+        for (int64_t j = tid; j < D; j += blockDim.x) {
+            const float dyv = Fmt::to_f32(dY[off + j]);
+            const float xh = (Fmt::to_f32(x[off + j]) - mu) * rs;
+            const float dxh = dyv * gamma[j];
+            dX[off + j] = Fmt::from_f32(rs * (dxh - mean_a - xh * mean_b));
+            pg[j] += dyv * xh;   // column j belongs to this thread only
+            pb[j] += dyv;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ column reduction
+// partials: [G][2][D] fp32 viewed as [G][2D]; out column c < D -> dgamma, else dbeta.
+// Warp w of the CTA sums rows w, w+8, ... in ascending order; the 8 warp sums are
+// then added in warp order.  The order never depends on timing.
+constexpr int kColThreads = 256;
+
+__global__ void __launch_bounds__(kColThreads)
+ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t D,
+                     float* __restrict__ dgamma, float* __restrict__ dbeta) {
+    __shared__ float sm[kColThreads / 32][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    constexpr int kGroups = kColThreads / 32;
+    const int64_t W = 2 * D;
+    const int64_t c = (int64_t)blockIdx.x * 32 + lane;
+    float acc = 0.f;
+    if (c < W) {
+        int b = w;
+        // four independent loads in flight, added in the fixed ascending order
+        for (; b + 3 * kGroups < G; b += 4 * kGroups) {
+            const float v0 = partials[(int64_t)b * W + c];
+            const float v1 = partials[(int64_t)(b + kGroups) * W + c];
+            const float v2 = partials[(int64_t)(b + 2 * kGroups) * W + c];
+            const float v3 = partials[(int64_t)(b + 3 * kGroups) * W + c];
+            acc += v0;
+            acc += v1;
+            acc += v2;
+            acc += v3;
+        }
+        for (; b < G; b += kGroups) acc += partials[(int64_t)b * W + c];
+    }
+    sm[w][lane] = acc;
+    __syncthreads();
+    if (w == 0 && c < W) {
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < kGroups; ++q) t += sm[q][lane];
+        if (c < D) dgamma[c] = t; else dbeta[c - D] = t;
+    }
+}
+
+// ------------------------------------------------------------------ launch planning
+enum class Path { kRing, kPlain };
+
+struct LnPlan {
+    Path path;
+    int threads;
+    int nv;          // vectors per thread (ring path)
+    int stages;      // ring stages
+    size_t smem;     // dynamic shared memory (ring path)
+    int grid;        // CTAs of the row kernel == partial rows in the workspace
+    int64_t rows_per_cta;
+};
+
+template <class Fmt, int NV>
+const void* ring_kernel_ptr() {
+    return reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, NV>);
+}
+
+// Largest NV instantiated: kMaxElemsPerThread columns per thread.
+template <class Fmt>
+constexpr int max_nv() { return kMaxElemsPerThread / Vec<Fmt>::kElems; }
+
+template <class Fmt>
+const void* ring_kernel_for(int nv) {
+    switch (nv) {
+        case 1: return ring_kernel_ptr<Fmt, 1>();
+        case 2: return ring_kernel_ptr<Fmt, 2>();
+        case 4: return ring_kernel_ptr<Fmt, 4>();
+        default: return ring_kernel_ptr<Fmt, max_nv<Fmt>()>();
+    }
+}
+
+const void* ring_kernel(tb_dtype dt, int nv) {
+    switch (dt) {
+        case TB_F32: return ring_kernel_for<F32>(nv);
+        case TB_BF16: return ring_kernel_for<BF16>(nv);
+        default: return ring_kernel_for<F16>(nv);
+    }
+}
+
+const void* plain_kernel(tb_dtype dt) {
+    switch (dt) {
+        case TB_F32: return reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<F32>);
+        case TB_BF16: return reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<BF16>);
+        default: return reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<F16>);
+    }
+}
+
+// `aligned`: every row buffer 16-byte aligned (the caller checks pointers).
+bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceInfo& info,
+               LnPlan* p) {
+    const int64_t es = (int64_t)dtype_size(dt);
+    const int64_t E = 16 / es;
+    const int64_t row_bytes = D * es;
+    const int64_t nvec = D / E;
+    p->path = Path::kPlain;
+    // Ring path: at most kMaxElemsPerThread columns per thread (gamma and the two
+    // partial sums live in registers), i.e. D <= 8192.
+    if (aligned && row_bytes % 16 == 0 && D <= (int64_t)kMaxElemsPerThread * kRowThreads) {
+        int threads = (int)std::min<int64_t>(kRowThreads, (nvec + 31) / 32 * 32);
+        int nv = (int)((nvec + threads - 1) / threads);
+        nv = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : 8;
+        const int64_t stage_bytes = 2 * row_bytes;
+        int stages = (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
+        size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
+        if ((int64_t)smem <= info.max_smem_optin) {
+            const void* k = ring_kernel(dt, nv);
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+                return false;
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) != cudaSuccess)
+                return false;
+            p->path = Path::kRing;
+            p->threads = threads;
+            p->nv = nv;
+            p->stages = stages;
+            p->smem = smem;
+            p->grid = info.sm_count * std::max(per_sm, 1);
+        }
+    }
+    if (p->path == Path::kPlain) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plain_kernel(dt), kRowThreads, 0) !=
+            cudaSuccess)
+            return false;
+        p->threads = kRowThreads;
+        p->nv = 0;
+        p->stages = 0;
+        p->smem = 0;
+        p->grid = info.sm_count * std::min(std::max(per_sm, 1), 2);
+    }
+    p->grid = (int)std::min<int64_t>(p->grid, rows);
+    p->rows_per_cta = p->grid > 0 ? (rows + p->grid - 1) / p->grid : 0;
+    return true;
+}
+
+size_t workspace_bytes_for(const LnPlan& p, int64_t D) {
+    return (size_t)p.grid * 2 * (size_t)D * sizeof(float);
+}
+
+template <class Fmt>
+void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* mean,
+                 const float* inv_std, const float* gamma, void* dX, float* ws, int64_t rows,
+                 int64_t D, int* err, cudaStream_t st) {
+    using T = typename Fmt::T;
+    const T* dy = static_cast<const T*>(dY);
+    const T* xx = static_cast<const T*>(x);
+    T* dx = static_cast<T*>(dX);
+    if (p.path == Path::kRing) {
+        const int Di = (int)D;
+        switch (p.nv) {
+            case 1:
+                ln_bwd_rows_ring_kernel<Fmt, 1><<<p.grid, p.threads, p.smem, st>>>(
+                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
+                break;
+            case 2:
+                ln_bwd_rows_ring_kernel<Fmt, 2><<<p.grid, p.threads, p.smem, st>>>(
+                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
+                break;
+            case 4:
+                ln_bwd_rows_ring_kernel<Fmt, 4><<<p.grid, p.threads, p.smem, st>>>(
+                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
+                break;
+            default:
+                ln_bwd_rows_ring_kernel<Fmt, max_nv<Fmt>()><<<p.grid, p.threads, p.smem, st>>>(
+                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
+                break;
+        }
+    } else {
+        ln_bwd_rows_plain_kernel<Fmt><<<p.grid, p.threads, 0, st>>>(dy, xx, mean, inv_std, gamma, dx,
+                                                                   ws, rows, D, p.rows_per_cta);
+    }
+}
+
+}  // namespace
+}  // namespace tb
+
+extern "C" tb_status tb_layernorm_bwd_workspace_size(int64_t rows, int64_t D, tb_dtype io_dtype,
+                                                     size_t* bytes) {
+    using namespace tb;
+    if (!bytes || rows < 0 || D < 0) return TB_ERR_INVALID_VALUE;
+    if (!dtype_valid(io_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
+    *bytes = 0;
+    if (rows == 0 || D == 0) return TB_OK;
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    LnPlan p;
+    // Size for the aligned layout; the fallback path never uses more CTAs.
+    if (!make_plan(rows, D, io_dtype, true, info, &p)) return TB_ERR_CUDA;
+    LnPlan q;
+    if (!make_plan(rows, D, io_dtype, false, info, &q)) return TB_ERR_CUDA;
+    *bytes = std::max(workspace_bytes_for(p, D), workspace_bytes_for(q, D));
+    return TB_OK;
+}
+
+extern "C" tb_status tb_layernorm_bwd(const void* dY, const void* x, const float* mean,
+                                      const float* inv_std, const float* gamma, void* dX,
+                                      float* dgamma, float* dbeta, int64_t rows, int64_t D,
+                                      tb_dtype io_dtype, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    using namespace tb;
+    if (rows < 0 || D < 0) return TB_ERR_INVALID_VALUE;
+    if (!dtype_valid(io_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (D == 0) return TB_OK;
+    if (D > (int64_t)1 << 30) return TB_ERR_INVALID_VALUE;
+    if (!dgamma || !dbeta || !gamma) return TB_ERR_INVALID_VALUE;
+    if (rows > 0 && (!dY || !x || !mean || !inv_std || !dX)) return TB_ERR_INVALID_VALUE;
+    if (rows > 0 && D > INT64_MAX / rows / 4) return TB_ERR_INVALID_VALUE;
+    const size_t es = dtype_size(io_dtype);
+    if (!aligned_to(dgamma, 4) || !aligned_to(dbeta, 4) || !aligned_to(gamma, 4)) return TB_ERR_MISALIGNED;
+    if (rows > 0 && (!aligned_to(dY, es) || !aligned_to(x, es) || !aligned_to(dX, es) ||
+                     !aligned_to(mean, 4) || !aligned_to(inv_std, 4)))
+        return TB_ERR_MISALIGNED;
+    const int64_t n = rows * D;
+    const Range r_dx = range_of(dX, n, es), r_dg = range_of(dgamma, D, 4), r_db = range_of(dbeta, D, 4);
+    const Range r_ws = range_of(workspace, (int64_t)workspace_bytes, 1);
+    const Range ins[5] = {range_of(dY, n, es), range_of(x, n, es), range_of(mean, rows, 4),
+                          range_of(inv_std, rows, 4), range_of(gamma, D, 4)};
+    const Range outs[4] = {r_dx, r_dg, r_db, r_ws};
+    for (const Range& o : outs)
+        for (const Range& in : ins)
+            if (overlap(o, in)) return TB_ERR_ALIAS;
+    for (int a = 0; a < 4; ++a)
+        for (int b = a + 1; b < 4; ++b)
+            if (overlap(outs[a], outs[b])) return TB_ERR_ALIAS;
+
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t W = 2 * D;
+    const unsigned col_grid = (unsigned)((W + 31) / 32);
+    if (rows == 0) {
+        ln_bwd_colsum_kernel<<<col_grid, kColThreads, 0, st>>>(nullptr, 0, D, dgamma, dbeta);
+        return launch_status();
+    }
+    const bool aligned = aligned_to(dY, 16) && aligned_to(x, 16) && aligned_to(dX, 16) &&
+                         aligned_to(gamma, 16) && aligned_to(workspace, 16);
+    LnPlan p;
+    if (!make_plan(rows, D, io_dtype, aligned, info, &p)) return TB_ERR_CUDA;
+    if (!workspace || workspace_bytes < workspace_bytes_for(p, D)) return TB_ERR_WORKSPACE;
+    if (!aligned_to(workspace, 4)) return TB_ERR_MISALIGNED;
+    int* err = device_error_word();
+    if (!err) return TB_ERR_CUDA;
+    float* ws = static_cast<float*>(workspace);
+    switch (io_dtype) {
+        case TB_F32: launch_rows<F32>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
+        case TB_BF16: launch_rows<BF16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
+        default: launch_rows<F16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
+    ln_bwd_colsum_kernel<<<col_grid, kColThreads, 0, st>>>(ws, p.grid, D, dgamma, dbeta);
+    return launch_status();
+}

@@ -1,0 +1,254 @@
+// softmax_bwd.cu -- row-wise softmax backward.
+//
+//   dX[r,i] = P[r,i] * (dY[r,i] - sum_j P[r,j] dY[r,j])
+// ("GPU 优化实战 Part 2：用 CUDA/ROCm 实现 LLM 反向传播与训练循环", section 2.1
+// "Softmax 反向内核").  The page's kernel gives one thread a whole row and walks
+// it twice with a stride of `cols` between neighbouring threads; here a row is
+// spread over the lanes of a group (4..32 lanes) or over a whole CTA so that
+// every access is a coalesced 16-byte vector, the row is staged once in
+// registers, the dot product is a butterfly of __shfl_xor_sync (plus shared
+// memory across warps in the CTA path), and dX is written from the registers:
+// each input element crosses HBM exactly once.
+//
+// Paths, chosen on the host:
+//   group : rows of <= 256 vectors (1024 fp32 / 2048 16-bit), G lanes per row
+//   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row
+//   twopass: anything longer or not 16-byte aligned; reads the row twice
+#include <algorithm>
+
+#include "tb_common.cuh"
+
+namespace tb {
+namespace {
+
+// Value e of a 16-byte vector held as raw bits.
+template <class Fmt>
+__device__ __forceinline__ float vec_elem(const uint4& u, int e) {
+    const typename Fmt::T* h = reinterpret_cast<const typename Fmt::T*>(&u);
+    return Fmt::to_f32(h[e]);
+}
+
+template <class Fmt>
+__device__ __forceinline__ uint4 vec_from(const float (&f)[Vec<Fmt>::kElems]) {
+    uint4 u;
+    typename Fmt::T* h = reinterpret_cast<typename Fmt::T*>(&u);
+#pragma unroll
+    for (int e = 0; e < Vec<Fmt>::kElems; ++e) h[e] = Fmt::from_f32(f[e]);
+    return u;
+}
+
+// ------------------------------------------------------------------ group path
+// G lanes per row (G divides 32), VPL vectors per lane; 256 threads per CTA.
+template <class Fmt, int G, int VPL>
+__global__ void __launch_bounds__(256)
+softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
+                         uint4* __restrict__ dX, int64_t rows, int nv) {
+    constexpr int E = Vec<Fmt>::kElems;
+    constexpr int kRowsPerWarp = 32 / G;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / G;        // row slot inside the warp
+    const int gl = lane % G;         // lane inside the group
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t r0 = warp * kRowsPerWarp; r0 < rows; r0 += nwarps * kRowsPerWarp) {
+        const int64_t row = r0 + sub;
+        const bool live = row < rows;
+        const int64_t off = row * (int64_t)nv;
+        uint4 p[VPL], d[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int vi = gl + k * G;
+            if (live && vi < nv) {
+                p[k] = __ldcs(P + off + vi);
+                d[k] = __ldcs(dY + off + vi);
+            } else {
+                p[k] = make_uint4(0u, 0u, 0u, 0u);
+                d[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k)
+#pragma unroll
+            for (int e = 0; e < E; ++e) dot += vec_elem<Fmt>(p[k], e) * vec_elem<Fmt>(d[k], e);
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o, G);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int vi = gl + k * G;
+            if (live && vi < nv) {
+                float out[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    out[e] = vec_elem<Fmt>(p[k], e) * (vec_elem<Fmt>(d[k], e) - dot);
+                __stcs(dX + off + vi, vec_from<Fmt>(out));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ CTA path
+constexpr int kCtaThreads = 512;
+
+template <class Fmt, int VPL>
+__global__ void __launch_bounds__(kCtaThreads)
+softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
+                       uint4* __restrict__ dX, int64_t rows, int nv) {
+    constexpr int E = Vec<Fmt>::kElems;
+    constexpr int kWarps = kCtaThreads / 32;
+    __shared__ float red[2][kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
+        const int64_t off = row * (int64_t)nv;
+        uint4 p[VPL], d[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int vi = tid + k * kCtaThreads;
+            if (vi < nv) {
+                p[k] = __ldcs(P + off + vi);
+                d[k] = __ldcs(dY + off + vi);
+            } else {
+                p[k] = make_uint4(0u, 0u, 0u, 0u);
+                d[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k)
+#pragma unroll
+            for (int e = 0; e < E; ++e) dot += vec_elem<Fmt>(p[k], e) * vec_elem<Fmt>(d[k], e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) red[parity][wid] = dot;
+        __syncthreads();   // one barrier per row: the other buffer is reused two rows later
+        dot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) dot += red[parity][w];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int vi = tid + k * kCtaThreads;
+            if (vi < nv) {
+                float out[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    out[e] = vec_elem<Fmt>(p[k], e) * (vec_elem<Fmt>(d[k], e) - dot);
+                __stcs(dX + off + vi, vec_from<Fmt>(out));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ two-pass path
+constexpr int kTwoPassThreads = 256;
+
+template <class Fmt>
+__global__ void __launch_bounds__(kTwoPassThreads)
+softmax_bwd_twopass_kernel(const typename Fmt::T* __restrict__ dY,
+                           const typename Fmt::T* __restrict__ P,
+                           typename Fmt::T* __restrict__ dX, int64_t rows, int64_t cols) {
+    constexpr int kWarps = kTwoPassThreads / 32;
+    __shared__ float red[2][kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
+        const int64_t off = row * cols;
+        float dot = 0.f;
+        for (int64_t j = tid; j < cols; j += kTwoPassThreads)
+            dot += Fmt::to_f32(P[off + j]) * Fmt::to_f32(dY[off + j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) red[parity][wid] = dot;
+        __syncthreads();
+        dot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) dot += red[parity][w];
+        for (int64_t j = tid; j < cols; j += kTwoPassThreads) {
+            const float p = Fmt::to_f32(P[off + j]);
+            dX[off + j] = Fmt::from_f32(p * (Fmt::to_f32(dY[off + j]) - dot));
+        }
+    }
+}
+
+// ------------------------------------------------------------------ dispatch
+template <class Fmt, int G, int VPL>
+tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, int nv,
+                       int sms, cudaStream_t st) {
+    constexpr int kRowsPerCta = 256 / G;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, reinterpret_cast<const void*>(&softmax_bwd_group_kernel<Fmt, G, VPL>), 256, 0);
+    const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1)));
+    softmax_bwd_group_kernel<Fmt, G, VPL><<<(unsigned)grid, 256, 0, st>>>(
+        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv);
+    return launch_status();
+}
+
+template <class Fmt, int VPL>
+tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int nv, int sms,
+                     cudaStream_t st) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, VPL>), kCtaThreads, 0);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * std::max(per_sm, 1)));
+    softmax_bwd_cta_kernel<Fmt, VPL><<<(unsigned)grid, kCtaThreads, 0, st>>>(
+        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv);
+    return launch_status();
+}
+
+template <class Fmt>
+tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_t cols,
+                   bool aligned, int sms, cudaStream_t st) {
+    constexpr int E = Vec<Fmt>::kElems;
+    if (aligned && cols % E == 0 && cols / E <= 2048) {
+        const int nv = (int)(cols / E);
+        if (nv <= 4) return launch_group<Fmt, 4, 1>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 8) return launch_group<Fmt, 8, 1>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 16) return launch_group<Fmt, 16, 1>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 32) return launch_group<Fmt, 32, 1>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 64) return launch_group<Fmt, 32, 2>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 128) return launch_group<Fmt, 32, 4>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 256) return launch_group<Fmt, 32, 8>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 512) return launch_cta<Fmt, 1>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 1024) return launch_cta<Fmt, 2>(dY, P, dX, rows, nv, sms, st);
+        return launch_cta<Fmt, 4>(dY, P, dX, rows, nv, sms, st);
+    }
+    using T = typename Fmt::T;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, reinterpret_cast<const void*>(&softmax_bwd_twopass_kernel<Fmt>), kTwoPassThreads, 0);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * std::max(per_sm, 1)));
+    softmax_bwd_twopass_kernel<Fmt><<<(unsigned)grid, kTwoPassThreads, 0, st>>>(
+        static_cast<const T*>(dY), static_cast<const T*>(P), static_cast<T*>(dX), rows, cols);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace tb
+
+extern "C" tb_status tb_softmax_bwd(const void* dY, const void* P, void* dX, int64_t rows,
+                                    int64_t cols, tb_dtype dtype, void* stream) {
+    using namespace tb;
+    if (rows < 0 || cols < 0) return TB_ERR_INVALID_VALUE;
+    if (!dtype_valid(dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (rows == 0 || cols == 0) return TB_OK;
+    if (!dY || !P || !dX) return TB_ERR_INVALID_VALUE;
+    if (cols > INT64_MAX / rows / 4) return TB_ERR_INVALID_VALUE;
+    const size_t es = dtype_size(dtype);
+    if (!aligned_to(dY, es) || !aligned_to(P, es) || !aligned_to(dX, es)) return TB_ERR_MISALIGNED;
+    const int64_t n = rows * cols;
+    const Range out = range_of(dX, n, es);
+    if (overlap(out, range_of(dY, n, es)) || overlap(out, range_of(P, n, es))) return TB_ERR_ALIAS;
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    const bool aligned = aligned_to(dY, 16) && aligned_to(P, 16) && aligned_to(dX, 16) &&
+                         (cols * (int64_t)es) % 16 == 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+        case TB_F32: return dispatch<F32>(dY, P, dX, rows, cols, aligned, info.sm_count, st);
+        case TB_BF16: return dispatch<BF16>(dY, P, dX, rows, cols, aligned, info.sm_count, st);
+        default: return dispatch<F16>(dY, P, dX, rows, cols, aligned, info.sm_count, st);
+    }
+}

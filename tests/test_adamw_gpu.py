@@ -1,0 +1,236 @@
+"""GPU parity of the fused multi-tensor AdamW step against the CPU oracle.
+
+Targets: fp32 theta/m/v within 1e-5 floored relative error of the float64
+oracle after the stated number of steps, the 16-bit working copy within one
+16-bit ulp of the oracle's theta rounded to nearest even, and the gradient
+zeroed bit-exactly after every step.  Sizes: the tiny flat tensor (every
+element compared), ragged / misaligned tables, the GPT-2-small table for 100
+steps and the Llama-7B table for 20 steps (sampled windows replayed by the
+oracle), plus determinism, resume and NaN-confinement checks.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tolerance import floored_rel, to_bits
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+KIND = {torch.bfloat16: "bf16", torch.float16: "f16"}
+
+
+@pytest.fixture(scope="module")
+def tb():
+    import ln_backward_gb300
+    return ln_backward_gb300
+
+
+@pytest.fixture(scope="module")
+def synth():
+    from ln_backward_gb300 import synth
+    return synth
+
+
+def _plan(tb, st):
+    k = len(st.sizes)
+    return tb.tb_adamw_plan_create([st.tensor("theta", i) for i in range(k)],
+                                   [st.tensor("m", i) for i in range(k)],
+                                   [st.tensor("v", i) for i in range(k)],
+                                   [st.tensor("grad", i) for i in range(k)],
+                                   [st.tensor("copy", i) for i in range(k)])
+
+
+def _windows(st, edge=2048, n_random=0, rlen=32768, seed=0):
+    """Arena indices to compare: each tensor's first and last `edge` elements,
+    plus random windows inside the larger tensors."""
+    rng = np.random.default_rng(seed)
+    parts = []
+    for off, n in zip(st.offsets, st.sizes):
+        if n == 0:
+            continue
+        parts.append(np.arange(off, off + min(n, edge)))
+        if n > edge:
+            parts.append(np.arange(off + max(edge, n - edge), off + n))
+    big = [(o, n) for o, n in zip(st.offsets, st.sizes) if n > 4 * rlen]
+    for _ in range(n_random if big else 0):
+        o, n = big[rng.integers(len(big))]
+        s = int(rng.integers(0, n - rlen))
+        parts.append(np.arange(o + s, o + s + rlen))
+    return np.unique(np.concatenate(parts))
+
+
+def _all_live(st):
+    return np.concatenate([np.arange(o, o + n) for o, n in zip(st.offsets, st.sizes) if n > 0])
+
+
+def _run(tb, synth, st, steps, idx, first_step=1):
+    """Runs `steps` GPU steps and the oracle on arena indices `idx`; returns errors."""
+    dev = st.theta.device
+    gkind, ckind = KIND[st.grad.dtype], KIND[st.copy.dtype]
+    inv = 1.0 / st.loss_scale
+    plan = _plan(tb, st)
+    it = torch.from_numpy(idx).to(dev)
+    th = st.theta.index_select(0, it).double().cpu().numpy()
+    m = st.m.index_select(0, it).double().cpu().numpy()
+    v = st.v.index_select(0, it).double().cpu().numpy()
+    for t in range(first_step, first_step + steps):
+        if t != 1:
+            synth.fill_grads(st, t)
+        gb = to_bits(st.grad.index_select(0, it))
+        tb.tb_adamw_step(plan, t, inv_loss_scale=inv, **HP)
+        cb, _ = oracle.adamw_step_f64(th, m, v, gb, gkind, inv, t, copy_kind=ckind, **HP)
+        torch.cuda.synchronize()
+        gz = to_bits(st.grad.index_select(0, it))
+        assert np.all(gz == 0), f"gradient not zeroed at step {t}"
+    plan.close()
+    got_th = st.theta.index_select(0, it).double().cpu().numpy()
+    got_m = st.m.index_select(0, it).double().cpu().numpy()
+    got_v = st.v.index_select(0, it).double().cpu().numpy()
+    got_c = to_bits(st.copy.index_select(0, it)).astype(np.int64)
+    cdist = np.abs(got_c - cb.astype(np.int64))
+    return dict(theta=floored_rel(got_th, th), m=floored_rel(got_m, m), v=floored_rel(got_v, v),
+                copy_ulps=int(cdist.max()))
+
+
+def _assert_within_targets(err):
+    assert err["theta"] <= 1e-5, err
+    assert err["m"] <= 1e-5, err
+    assert err["v"] <= 1e-5, err
+    assert err["copy_ulps"] <= 1, err
+
+
+# ----------------------------------------------------------------------------- tiny config
+def test_tiny_flat_tensor_10_steps(tb, synth):
+    """1,048,576 params, fp16 grads = N(0,1e-3)*1024, bf16 copy, 10 steps, every element."""
+    st = synth.make_adamw_state([("w", (1 << 20,))], seed=0, device="cuda",
+                                grad_dtype=torch.float16, copy_dtype=torch.bfloat16,
+                                grad_std=1e-3, loss_scale=1024.0)
+    err = _run(tb, synth, st, 10, _all_live(st))
+    _assert_within_targets(err)
+
+
+def test_tiny_flat_tensor_fp16_copy(tb, synth):
+    st = synth.make_adamw_state([("w", (1 << 20,))], seed=1, device="cuda",
+                                grad_dtype=torch.float16, copy_dtype=torch.float16,
+                                grad_std=1e-3, loss_scale=1024.0)
+    _assert_within_targets(_run(tb, synth, st, 3, _all_live(st)))
+
+
+@pytest.mark.parametrize("align", [1, 3, 128])
+def test_ragged_and_misaligned_tables(tb, synth, align):
+    """Tensor sizes around the 8-element unit, empty tensors, and arenas packed
+    with no alignment (most tensors then take the scalar path)."""
+    sizes = [1, 7, 8, 9, 0, 15, 16, 17, 1000, 8191, 8193, 0, 65541, 3, 300_007]
+    shapes = [(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    st = synth.make_adamw_state(shapes, seed=2, device="cuda", grad_std=1e-3,
+                                loss_scale=65536.0, align=align)
+    _assert_within_targets(_run(tb, synth, st, 4, _all_live(st)))
+
+
+def test_bf16_grads_bf16_copy_many_small_tensors(tb, synth):
+    shapes = [(f"t{i}", (int(n),)) for i, n in enumerate(np.random.default_rng(3).integers(1, 5000, 700))]
+    st = synth.make_adamw_state(shapes, seed=3, device="cuda", grad_std=1e-3, loss_scale=65536.0)
+    _assert_within_targets(_run(tb, synth, st, 3, _all_live(st)))
+
+
+# ----------------------------------------------------------------------------- full-size configs
+def test_gpt2_small_table_100_steps(tb, synth):
+    """148 tensors, 124,439,808 params, bf16 grads * 65536, steps 1..100."""
+    shapes = synth.gpt2_small_shapes()
+    st = synth.make_adamw_state(shapes, seed=0, device="cuda", grad_std=1e-3, loss_scale=65536.0)
+    assert len(st.sizes) == 148 and st.n_params == 124_439_808
+    idx = _windows(st, edge=2048, n_random=24)
+    _assert_within_targets(_run(tb, synth, st, 100, idx))
+
+
+def test_llama7b_table_20_steps(tb, synth):
+    """291 tensors, 6,738,415,616 params (~108 GB of state), bf16 grads * 65536 with
+    sigma 1e-4, steps 1..20, in the launch configuration the benchmark times."""
+    shapes = synth.llama7b_shapes()
+    st = synth.make_adamw_state(shapes, seed=0, device="cuda", grad_std=1e-4, loss_scale=65536.0)
+    assert len(st.sizes) == 291 and st.n_params == 6_738_415_616
+    idx = _windows(st, edge=1024, n_random=32, rlen=65536)
+    err = _run(tb, synth, st, 20, idx)
+    del st
+    torch.cuda.empty_cache()
+    _assert_within_targets(err)
+
+
+# ----------------------------------------------------------------------------- properties
+def _clone_state(st):
+    import copy
+    c = copy.copy(st)
+    for k in ("theta", "m", "v", "grad", "copy"):
+        setattr(c, k, getattr(st, k).clone())
+    return c
+
+
+def test_deterministic_bitwise(tb, synth):
+    st = synth.make_adamw_state(synth.gpt2_small_shapes()[:20], seed=4, device="cuda")
+    st2 = _clone_state(st)
+    for s in (st, st2):
+        p = _plan(tb, s)
+        for t in (1, 2, 3):
+            synth.fill_grads(s, t)
+            tb.tb_adamw_step(p, t, inv_loss_scale=1 / 65536.0, **HP)
+        p.close()
+    torch.cuda.synchronize()
+    for k in ("theta", "m", "v", "copy", "grad"):
+        assert torch.equal(getattr(st, k), getattr(st2, k)), k
+
+
+def test_resume_is_bitwise(tb, synth):
+    """10 steps straight == 5 steps, state copied to fresh buffers, 5 more steps."""
+    shapes = [("a", (3001,)), ("b", (64, 64))]
+    a = synth.make_adamw_state(shapes, seed=5, device="cuda")
+    b = _clone_state(a)
+    pa = _plan(tb, a)
+    for t in range(1, 11):
+        synth.fill_grads(a, t)
+        tb.tb_adamw_step(pa, t, inv_loss_scale=1 / 65536.0, **HP)
+    pb = _plan(tb, b)
+    for t in range(1, 6):
+        synth.fill_grads(b, t)
+        tb.tb_adamw_step(pb, t, inv_loss_scale=1 / 65536.0, **HP)
+    pb.close()
+    c = _clone_state(b)          # "checkpoint": copy theta/m/v out, resume from the copy
+    del b
+    pc = _plan(tb, c)
+    for t in range(6, 11):
+        synth.fill_grads(c, t)
+        tb.tb_adamw_step(pc, t, inv_loss_scale=1 / 65536.0, **HP)
+    torch.cuda.synchronize()
+    for k in ("theta", "m", "v", "copy"):
+        assert torch.equal(getattr(a, k), getattr(c, k)), k
+
+
+def test_nan_gradient_stays_confined(tb, synth):
+    shapes = [("a", (4096,))]
+    a = synth.make_adamw_state(shapes, seed=6, device="cuda")
+    b = _clone_state(a)
+    a.grad[123] = float("nan")
+    for s in (a, b):
+        p = _plan(tb, s)
+        tb.tb_adamw_step(p, 1, inv_loss_scale=1 / 65536.0, **HP)
+        p.close()
+    torch.cuda.synchronize()
+    assert torch.isnan(a.theta[123]) and torch.isnan(a.m[123]) and torch.isnan(a.v[123])
+    keep = torch.ones(a.theta.numel(), dtype=torch.bool, device="cuda")
+    keep[123] = False
+    for k in ("theta", "m", "v", "copy"):
+        assert torch.equal(getattr(a, k)[keep], getattr(b, k)[keep]), k
+
+
+def test_step_argument_errors(tb, synth):
+    st = synth.make_adamw_state([("a", (64,))], seed=7, device="cuda")
+    p = _plan(tb, st)
+    with pytest.raises(tb.TbError):
+        tb.tb_adamw_step(p, 0, inv_loss_scale=1.0, **HP)
+    with pytest.raises(tb.TbError):
+        tb.tb_adamw_step(p, 1, inv_loss_scale=1.0, lr=1e-3, beta1=1.0, beta2=0.999, eps=1e-8,
+                         weight_decay=0.0)
+    with pytest.raises(tb.TbError):
+        tb.tb_adamw_step(p, 1, inv_loss_scale=-1.0, **HP)
+    p.close()

@@ -1,0 +1,147 @@
+"""GPU parity of the LayerNorm backward against the CPU oracle.
+
+Targets: fp32 dX within 1e-4 floored relative error; 16-bit dX within one
+16-bit ulp of the oracle's exact result rounded to nearest even (or within the
+fp32 arithmetic's own error bound for outputs that cancel -- see
+tests/tolerance.py); dgamma and dbeta within 1e-3 floored relative error.
+Covers the tiny config (1024 x 256 fp32), the full config (16,384 x 4,096 bf16,
+every element), a sweep of D across the ring and plain paths with ragged row
+counts, unaligned buffers, zero rows, bitwise determinism and the workspace
+check.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tolerance import floored_rel, lowp_check, to_bits
+
+pytestmark = pytest.mark.gpu
+
+KIND = {torch.bfloat16: "bf16", torch.float16: "f16"}
+
+
+@pytest.fixture(scope="module")
+def tb():
+    import ln_backward_gb300
+    return ln_backward_gb300
+
+
+@pytest.fixture(scope="module")
+def synth():
+    from ln_backward_gb300 import synth
+    return synth
+
+
+def run(tb, x, dY, mean, rstd, gamma, ws_bytes=None):
+    rows, D = x.shape
+    dX = torch.full_like(x, float("nan"))
+    dg = torch.full((D,), float("nan"), device=x.device)
+    db = torch.full((D,), float("nan"), device=x.device)
+    need = tb.tb_layernorm_bwd_workspace_size(rows, D, x.dtype)
+    ws = torch.empty(max(need if ws_bytes is None else ws_bytes, 1), dtype=torch.uint8,
+                     device=x.device)
+    tb.tb_layernorm_bwd(dY, x, mean, rstd, gamma, dX, dg, db, ws)
+    return dX, dg, db
+
+
+def _dx_err_bound(x, dY, mean, rstd, gamma):
+    """Bound on |dX_fp32 - dX_exact|: xhat and dxhat carry a few fp32 roundings,
+    the two row sums at most D/32 + 64 rounded additions each."""
+    D = x.shape[1]
+    xh = (x - mean[:, None]) * rstd[:, None]
+    dxh = dY * gamma[None, :]
+    sa = np.sum(np.abs(dxh), axis=1, keepdims=True) / D
+    sb = np.sum(np.abs(dxh * xh), axis=1, keepdims=True) / D
+    mb = np.abs(np.sum(dxh * xh, axis=1, keepdims=True)) / D
+    ma = np.abs(np.sum(dxh, axis=1, keepdims=True)) / D
+    k = D / 32 + 64
+    u = 2.0 ** -24
+    return rstd[:, None] * (4 * u * (np.abs(dxh) + ma + np.abs(xh) * mb) +
+                            k * u * (sa + np.abs(xh) * sb))
+
+
+def check(tb, x, dY, mean, rstd, gamma, dX, dg, db):
+    xn, dYn = x.double().cpu().numpy(), dY.double().cpu().numpy()
+    mn, rn, gn = (t.double().cpu().numpy() for t in (mean, rstd, gamma))
+    rdx, rdg, rdb = oracle.layernorm_bwd_f64(dYn, xn, mn, rn, gn)
+    assert floored_rel(dg.double().cpu().numpy(), rdg) <= 1e-3
+    assert floored_rel(db.double().cpu().numpy(), rdb) <= 1e-3
+    if dX.dtype == torch.float32:
+        e = floored_rel(dX.double().cpu().numpy(), rdx)
+        assert e <= 1e-4, f"dX floored relative error {e}"
+    else:
+        ok, n_err, dmax = lowp_check(to_bits(dX), rdx, KIND[dX.dtype],
+                                     _dx_err_bound(xn, dYn, mn, rn, gn))
+        assert ok.all(), f"{(~ok).sum()} dX elements off (max ulp distance {dmax})"
+
+
+def test_tiny_config_fp32(tb, synth):
+    args = synth.layernorm_inputs(1024, 256, torch.float32, seed=0, device="cuda", eps=1e-5)
+    check(tb, *args, *run(tb, *args))
+
+
+def test_full_config_bf16(tb, synth):
+    """B=8, S=2048, D=4096: 16,384 rows, bf16 x ~ N(0,1), dY ~ N(0,1e-2)."""
+    x, dY, mean, rstd, gamma = synth.layernorm_inputs(16384, 4096, torch.bfloat16, seed=0,
+                                                      device="cuda", eps=1e-5, dy_std=1e-2)
+    dX, dg, db = run(tb, x, dY, mean, rstd, gamma)
+    torch.cuda.synchronize()
+    check(tb, x, dY, mean, rstd, gamma, dX, dg, db)
+
+
+DS = [1, 2, 3, 4, 8, 17, 64, 100, 256, 768, 1000, 1024, 2048, 4096, 4104, 6144, 8192, 8200, 12288]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
+                         ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", DS)
+def test_feature_dim_sweep(tb, synth, D, dtype):
+    for rows in (1, 7, 300):
+        args = synth.layernorm_inputs(rows, D, dtype, seed=D + rows, device="cuda")
+        check(tb, *args, *run(tb, *args))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_unaligned_buffers_take_plain_path(tb, synth, dtype):
+    rows, D = 33, 1024
+    x0, dY0, mean, rstd, gamma = synth.layernorm_inputs(rows, D, dtype, seed=5, device="cuda")
+    bx = torch.empty(rows * D + 1, dtype=dtype, device="cuda")
+    by = torch.empty(rows * D + 1, dtype=dtype, device="cuda")
+    x = bx[1:].view(rows, D)
+    dY = by[1:].view(rows, D)
+    x.copy_(x0)
+    dY.copy_(dY0)
+    check(tb, x, dY, mean, rstd, gamma, *run(tb, x, dY, mean, rstd, gamma))
+
+
+def test_zero_rows_write_zero_parameter_gradients(tb):
+    D = 96
+    x = torch.empty(0, D, device="cuda")
+    mean = torch.empty(0, device="cuda")
+    gamma = torch.ones(D, device="cuda")
+    dX, dg, db = run(tb, x, x.clone(), mean, mean.clone(), gamma)
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0) and torch.all(db == 0)
+
+
+def test_deterministic_bitwise(tb, synth):
+    args = synth.layernorm_inputs(16384, 4096, torch.bfloat16, seed=6, device="cuda", dy_std=1e-2)
+    a = run(tb, *args)
+    b = run(tb, *args)
+    torch.cuda.synchronize()
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
+
+
+def test_workspace_too_small_is_rejected(tb, synth):
+    args = synth.layernorm_inputs(512, 1024, torch.bfloat16, seed=7, device="cuda")
+    need = tb.tb_layernorm_bwd_workspace_size(512, 1024, torch.bfloat16)
+    assert need > 0
+    with pytest.raises(tb.TbError) as ei:
+        run(tb, *args, ws_bytes=need - 16)
+    assert ei.value.code == 5
+
+
+def test_no_kernel_gave_up_waiting(tb):
+    assert tb.tb_device_error(reset=True) == 0

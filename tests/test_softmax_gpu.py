@@ -1,0 +1,130 @@
+"""GPU parity of the softmax backward against the CPU oracle.
+
+Targets: fp32 dX within 1e-5 absolute of the float64 oracle; 16-bit dX within
+one 16-bit ulp of the oracle's exact result rounded to nearest even (or, for
+outputs that cancel far below their terms, within the fp32 arithmetic's own
+error bound -- see tests/tolerance.py).  Covers the tiny config (1024 x 128
+fp32, every element), the attention config (98,304 x 1,024 causal, fp32 and
+bf16, every element), a sweep of row lengths across every kernel path with a
+ragged row count, unaligned buffers (two-pass path) and empty inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tolerance import lowp_check, to_bits
+
+pytestmark = pytest.mark.gpu
+
+KIND = {torch.bfloat16: "bf16", torch.float16: "f16"}
+
+
+@pytest.fixture(scope="module")
+def tb():
+    import ln_backward_gb300
+    return ln_backward_gb300
+
+
+@pytest.fixture(scope="module")
+def synth():
+    from ln_backward_gb300 import synth
+    return synth
+
+
+def _err_bound(P, dY):
+    """Bound on |dX_fp32 - dX_exact| for the kernel's fp32 arithmetic: the dot
+    product (at most cols/32 + 16 rounded additions on any path, each below
+    2^-24 of sum|P*dY|), the subtraction and the final multiply."""
+    cols = P.shape[1]
+    S = np.sum(np.abs(P * dY), axis=1, keepdims=True)
+    dot = np.sum(P * dY, axis=1, keepdims=True)
+    k = cols / 32 + 64
+    return np.abs(P) * (k * 2.0 ** -24 * S + 2.0 ** -22 * (np.abs(dY) + np.abs(dot)))
+
+
+def check(dX, P, dY):
+    """Compares the GPU result with the float64 oracle on the same inputs."""
+    Pn = P.double().cpu().numpy()
+    dYn = dY.double().cpu().numpy()
+    ref = oracle.softmax_bwd_f64(dYn, Pn)
+    if dX.dtype == torch.float32:
+        err = np.max(np.abs(dX.double().cpu().numpy() - ref)) if ref.size else 0.0
+        assert err <= 1e-5, f"max abs error {err}"
+    else:
+        ok, n_err, dmax = lowp_check(to_bits(dX), ref, KIND[dX.dtype], _err_bound(Pn, dYn))
+        assert ok.all(), f"{(~ok).sum()} elements off (max ulp distance {dmax})"
+
+
+def test_tiny_config_fp32(tb, synth):
+    P, dY = synth.softmax_inputs(1024, 128, torch.float32, seed=0, device="cuda")
+    dX = torch.empty_like(P)
+    tb.tb_softmax_bwd(dY, P, dX)
+    check(dX, P, dY)
+
+
+COLS = [1, 2, 3, 4, 5, 8, 16, 31, 33, 64, 127, 128, 255, 256, 1000, 1023, 1024, 1025, 2048,
+        2049, 4096, 8192, 8200, 16384, 16392, 20000]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
+                         ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("cols", COLS)
+def test_row_length_sweep(tb, synth, cols, dtype):
+    P, dY = synth.softmax_inputs(37, cols, dtype, seed=cols, device="cuda")
+    dX = torch.full_like(P, float("nan"))
+    tb.tb_softmax_bwd(dY, P, dX)
+    check(dX, P, dY)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_unaligned_buffers_take_two_pass_path(tb, synth, dtype):
+    rows, cols = 19, 1024
+    P0, dY0 = synth.softmax_inputs(rows, cols, dtype, seed=9, device="cuda")
+    bufP = torch.empty(rows * cols + 1, dtype=dtype, device="cuda")
+    bufY = torch.empty(rows * cols + 1, dtype=dtype, device="cuda")
+    bufX = torch.empty(rows * cols + 1, dtype=dtype, device="cuda")
+    P = bufP[1:].view(rows, cols)
+    dY = bufY[1:].view(rows, cols)
+    dX = bufX[1:].view(rows, cols)
+    P.copy_(P0)
+    dY.copy_(dY0)
+    tb.tb_softmax_bwd(dY, P, dX)
+    check(dX, P, dY)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_attention_config_full_size(tb, synth, dtype):
+    """B=8, H=12, S=1024: 98,304 rows x 1,024 causal columns; every element compared."""
+    rows, cols = 8 * 12 * 1024, 1024
+    P, dY = synth.softmax_inputs(rows, cols, dtype, seed=2, device="cuda", causal_period=1024)
+    # the causal structure: row r sees columns j <= r mod 1024, masked entries exactly 0
+    assert torch.all(P[5, 6:] == 0) and torch.all(P[5, :6] > 0)
+    dX = torch.empty_like(P)
+    tb.tb_softmax_bwd(dY, P, dX)
+    torch.cuda.synchronize()
+    for r0 in range(0, rows, 16384):
+        check(dX[r0:r0 + 16384], P[r0:r0 + 16384], dY[r0:r0 + 16384])
+    # masked positions give exactly zero
+    assert torch.all(dX[5, 6:] == 0)
+
+
+def test_empty_inputs_are_noops(tb):
+    for shape in ((0, 16), (16, 0), (0, 0)):
+        P = torch.empty(shape, device="cuda")
+        tb.tb_softmax_bwd(P, P.clone(), P.clone())
+
+
+def test_aliasing_rejected(tb, synth):
+    P, dY = synth.softmax_inputs(8, 64, torch.float32, seed=3, device="cuda")
+    with pytest.raises(tb.TbError):
+        tb.tb_softmax_bwd(dY, P, dY)
+
+
+def test_deterministic(tb, synth):
+    P, dY = synth.softmax_inputs(4096, 1024, torch.bfloat16, seed=4, device="cuda")
+    a, b = torch.empty_like(P), torch.empty_like(P)
+    tb.tb_softmax_bwd(dY, P, a)
+    tb.tb_softmax_bwd(dY, P, b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
