@@ -18,8 +18,8 @@ F32, F16, BF16 = 0, 1, 2
 
 @pytest.fixture(scope="module")
 def tb():
-    from ln_backward_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import ln_backward_gb300
     return ln_backward_gb300
 

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from tolerance import floored_rel, lowp_check, to_bits
+from tolerance import floored_rel, lowp_check, to_bits, within_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -61,15 +61,23 @@ def _dx_err_bound(x, dY, mean, rstd, gamma):
                             k * u * (sa + np.abs(xh) * sb))
 
 
-def check(tb, x, dY, mean, rstd, gamma, dX, dg, db):
+def check(tb, x, dY, mean, rstd, gamma, dX, dg, db, strict_fp32=True):
+    """strict_fp32: the fp32 dX target (1e-4 floored relative).  Without it, fp32
+    dX may instead sit within the derived fp32 error bound -- needed for D <= 2,
+    where the exact dX is proportional to eps and cancels far below its terms."""
     xn, dYn = x.double().cpu().numpy(), dY.double().cpu().numpy()
     mn, rn, gn = (t.double().cpu().numpy() for t in (mean, rstd, gamma))
     rdx, rdg, rdb = oracle.layernorm_bwd_f64(dYn, xn, mn, rn, gn)
     assert floored_rel(dg.double().cpu().numpy(), rdg) <= 1e-3
     assert floored_rel(db.double().cpu().numpy(), rdb) <= 1e-3
     if dX.dtype == torch.float32:
-        e = floored_rel(dX.double().cpu().numpy(), rdx)
-        assert e <= 1e-4, f"dX floored relative error {e}"
+        got = dX.double().cpu().numpy()
+        e = floored_rel(got, rdx)
+        if not strict_fp32 and e > 1e-4:
+            ok = within_bound(got, rdx, _dx_err_bound(xn, dYn, mn, rn, gn))
+            assert ok.all(), f"dX: {(~ok).sum()} elements beyond the fp32 error bound"
+        else:
+            assert e <= 1e-4, f"dX floored relative error {e}"
     else:
         ok, n_err, dmax = lowp_check(to_bits(dX), rdx, KIND[dX.dtype],
                                      _dx_err_bound(xn, dYn, mn, rn, gn))
@@ -99,7 +107,7 @@ DS = [1, 2, 3, 4, 8, 17, 64, 100, 256, 768, 1000, 1024, 2048, 4096, 4104, 6144, 
 def test_feature_dim_sweep(tb, synth, D, dtype):
     for rows in (1, 7, 300):
         args = synth.layernorm_inputs(rows, D, dtype, seed=D + rows, device="cuda")
-        check(tb, *args, *run(tb, *args))
+        check(tb, *args, *run(tb, *args), strict_fp32=D > 2)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])

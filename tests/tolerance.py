@@ -51,14 +51,16 @@ def ulp16(x: np.ndarray, kind: str) -> np.ndarray:
 
 def lowp_check(got_bits, ref, kind: str, err=None):
     """Returns (ok_mask, n_needing_err_bound, max_ulp_distance)."""
+    ref = np.asarray(ref, np.float64)
+    if err is not None:
+        err = np.broadcast_to(np.asarray(err, np.float64), ref.shape).ravel()
     got_bits = np.asarray(got_bits).view(np.uint16).ravel()
-    ref = np.asarray(ref, np.float64).ravel()
+    ref = ref.ravel()
     ref_bits = oracle.encode16(ref, kind)
     dist = np.abs(_ordered(got_bits) - _ordered(ref_bits))
     ok = dist <= 1
     n_err = 0
     if err is not None:
-        err = np.broadcast_to(np.asarray(err, np.float64), ref.shape).ravel()
         got = oracle.decode16(got_bits, kind)
         ok2 = np.abs(got - ref) <= err + 0.5 * ulp16(np.abs(ref) + err, kind)
         n_err = int(np.sum(ok2 & ~ok))
@@ -70,3 +72,10 @@ def to_bits(t) -> np.ndarray:
     """uint16 view of a 16-bit torch tensor, on the host."""
     import torch
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def within_bound(got, ref, err) -> np.ndarray:
+    """|got - ref| <= err elementwise (fp32 outputs with a derived error bound)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return np.abs(got - ref) <= np.broadcast_to(np.asarray(err, np.float64), ref.shape)
