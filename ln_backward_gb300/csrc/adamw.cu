@@ -11,12 +11,13 @@
 // Design (GB300): one launch covers every tensor of the model.  The host plan
 // holds a device table of tensors and a prefix sum of their "units" (8
 // elements = one 16-byte vector of the 16-bit gradient and two of each fp32
-// stream).  The flat unit space is cut into one contiguous range per CTA (grid
-// = SM count x resident CTAs); each CTA finds its first tensor by binary search
-// and walks forward.  Every thread moves 2 units per iteration with 128-bit
-// evict-first loads and stores: 14 B read and 16 B written per element, one
-// HBM pass.  Tensors whose five pointers are not all 16-byte aligned, and the
-// last partial unit of a tensor, take a scalar path.
+// stream).  The flat unit space is cut into tiles of 512 units dealt
+// round-robin to a persistent grid (SM count x resident CTAs), so all CTAs
+// stream through the same region of HBM at once; each CTA follows its tensor
+// with a forward scan of the table.  Every thread moves 2 units per tile with
+// 128-bit evict-first loads and stores: 14 B read and 16 B written per element,
+// one HBM pass.  Tensors whose five pointers are not all 16-byte aligned, and
+// the last partial unit of a tensor, take a scalar path.
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
@@ -31,6 +32,7 @@ namespace {
 constexpr int kUnit = 8;        // elements per unit
 constexpr int kThreads = 256;   // threads per CTA
 constexpr int kUnroll = 2;      // units in flight per thread
+constexpr int64_t kTileUnits = (int64_t)kThreads * kUnroll;   // 4096 elements
 constexpr uint64_t kPlanMagic = 0x7462616461707731ull;
 
 struct alignas(16) TensorEntry {
@@ -139,28 +141,44 @@ __device__ __forceinline__ void process_segment(const TensorEntry& t, int64_t a,
     }
 }
 
+// Index of the tensor holding unit u, searching forward from k (tiles of a CTA
+// visit the unit space in increasing order): a few linear steps, then binary search.
+__device__ __forceinline__ int tensor_of(const TensorEntry* __restrict__ tab, int ntab, int k,
+                                         int64_t u) {
+#pragma unroll 1
+    for (int step = 0; step < 4; ++step) {
+        if (k + 1 >= ntab || tab[k + 1].unit_begin > u) return k;
+        ++k;
+    }
+    int lo = k, hi = ntab - 1;   // last index with unit_begin <= u
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab[mid].unit_begin <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Tiles of kTileUnits consecutive units are dealt round-robin to the CTAs, so at
+// any moment all CTAs stream through one window of about grid*kTileUnits units.
 template <class G, class C>
 __global__ void __launch_bounds__(kThreads, 2)
 adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
-                          int64_t units_per_cta, Scalars s) {
-    const int64_t u_lo = (int64_t)blockIdx.x * units_per_cta;
-    if (u_lo >= total_units) return;
-    const int64_t u_hi = u_lo + units_per_cta < total_units ? u_lo + units_per_cta : total_units;
-    // Last tensor whose first unit is <= u_lo.
-    int lo = 0, hi = ntab - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tab[mid].unit_begin <= u_lo) lo = mid; else hi = mid - 1;
-    }
-    int k = lo;
-    int64_t u = u_lo;
-    while (u < u_hi && k < ntab) {
-        const TensorEntry t = tab[k];
-        const int64_t t_end = (k + 1 < ntab) ? tab[k + 1].unit_begin : total_units;
-        const int64_t seg_hi = u_hi < t_end ? u_hi : t_end;
-        if (seg_hi > u) process_segment<G, C>(t, u - t.unit_begin, seg_hi - t.unit_begin, s);
-        u = seg_hi > u ? seg_hi : u;
-        ++k;
+                          int64_t n_tiles, Scalars s) {
+    int k = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t u_lo = tile * kTileUnits;
+        const int64_t u_hi = u_lo + kTileUnits < total_units ? u_lo + kTileUnits : total_units;
+        k = tensor_of(tab, ntab, k, u_lo);
+        int kk = k;
+        int64_t u = u_lo;
+        while (u < u_hi && kk < ntab) {
+            const TensorEntry t = tab[kk];
+            const int64_t t_end = (kk + 1 < ntab) ? tab[kk + 1].unit_begin : total_units;
+            const int64_t seg_hi = u_hi < t_end ? u_hi : t_end;
+            if (seg_hi > u) process_segment<G, C>(t, u - t.unit_begin, seg_hi - t.unit_begin, s);
+            u = seg_hi > u ? seg_hi : u;
+            ++kk;
+        }
     }
 }
 
@@ -304,21 +322,21 @@ extern "C" tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
     s.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(b2), static_cast<double>(step)));
     s.inv_s = inv_loss_scale;
 
-    const int64_t grid = std::min<int64_t>(plan->grid, plan->total_units);
-    const int64_t per_cta = (plan->total_units + grid - 1) / grid;
+    const int64_t n_tiles = (plan->total_units + kTileUnits - 1) / kTileUnits;
+    const int64_t grid = std::min<int64_t>(plan->grid, n_tiles);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const tb::TensorEntry* tab = plan->d_table;
     const int nt = plan->n_tensors;
     const int64_t tu = plan->total_units;
     const tb_dtype g = plan->grad_dtype, c = plan->copy_dtype;
     if (g == TB_BF16 && c == TB_BF16)
-        adamw_multi_tensor_kernel<BF16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+        adamw_multi_tensor_kernel<BF16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
     else if (g == TB_BF16 && c == TB_F16)
-        adamw_multi_tensor_kernel<BF16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+        adamw_multi_tensor_kernel<BF16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
     else if (g == TB_F16 && c == TB_BF16)
-        adamw_multi_tensor_kernel<F16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+        adamw_multi_tensor_kernel<F16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
     else
-        adamw_multi_tensor_kernel<F16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, per_cta, s);
+        adamw_multi_tensor_kernel<F16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
     return launch_status();
 }
 

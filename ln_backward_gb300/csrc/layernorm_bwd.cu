@@ -41,6 +41,7 @@ constexpr int kMaxWarps = kRowThreads / 32;
 constexpr int kMaxStages = 4;
 constexpr int kMaxElemsPerThread = 32;
 constexpr int kRingBudget = 96 * 1024;         // bytes of ring per CTA we aim for
+constexpr int kStageTargetBytes = 32 * 1024;   // x + dY bytes per ring stage we aim for
 constexpr int kBarRegion = 128;                // bytes reserved for the mbarriers
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
@@ -107,6 +108,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Programmatic dependent launch: the primary grid allows its dependent to be
+// scheduled; the dependent waits until the primary has completed and flushed.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -120,9 +130,69 @@ __device__ __forceinline__ void lds_vec(const void* p, float (&f)[Vec<Fmt>::kEle
     for (int e = 0; e < Vec<Fmt>::kElems; ++e) f[e] = Fmt::to_f32(h[e]);
 }
 
+// One 16-byte shared-memory vector as E/2 fp32 pairs (packed f32x2 math below).
+// bf16 widens exactly with a shift / mask; fp16 with the half2 conversion.
+template <class Fmt>
+struct Pairs {
+    static constexpr int kN = Vec<Fmt>::kElems / 2;
+};
+
+template <class Fmt>
+__device__ __forceinline__ void lds_pairs(const void* p, float2 (&f)[Pairs<Fmt>::kN]);
+template <>
+__device__ __forceinline__ void lds_pairs<F32>(const void* p, float2 (&f)[2]) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    f[0] = make_float2(u.x, u.y);
+    f[1] = make_float2(u.z, u.w);
+}
+template <>
+__device__ __forceinline__ void lds_pairs<BF16>(const void* p, float2 (&f)[4]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ void lds_pairs<F16>(const void* p, float2 (&f)[4]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+}
+
+// Store E/2 fp32 pairs as one 16-byte global vector (round to nearest even).
+template <class Fmt>
+__device__ __forceinline__ void stg_pairs(void* p, const float2 (&f)[Pairs<Fmt>::kN]);
+template <>
+__device__ __forceinline__ void stg_pairs<F32>(void* p, const float2 (&f)[2]) {
+    st_stream_f4(static_cast<float*>(p), make_float4(f[0].x, f[0].y, f[1].x, f[1].y));
+}
+template <>
+__device__ __forceinline__ void stg_pairs<BF16>(void* p, const float2 (&f)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f[i].x, f[i].y);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    st_stream_u4(p, make_uint4(w[0], w[1], w[2], w[3]));
+}
+template <>
+__device__ __forceinline__ void stg_pairs<F16>(void* p, const float2 (&f)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(f[i].x, f[i].y);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    st_stream_u4(p, make_uint4(w[0], w[1], w[2], w[3]));
+}
+
 // ------------------------------------------------------------------ row kernel (bulk-copy ring)
+// A ring stage holds a group of R consecutive rows: [R rows of x | R rows of dY].
 // Columns per thread NV*E up to 16 fit two CTAs per SM; 32 need the full budget.
-template <class Fmt, int NV>
+template <class Fmt, int NV, int R>
 __global__ void __launch_bounds__(kRowThreads, (NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
 ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
                         const float* __restrict__ mean, const float* __restrict__ inv_std,
@@ -132,135 +202,179 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
     using T = typename Fmt::T;
     constexpr int E = Vec<Fmt>::kElems;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[2][2][kMaxWarps];
+    __shared__ float red[2][R][2][kMaxWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nthreads = blockDim.x, nwarps = nthreads >> 5;
     const int nvec = D / E;
     const uint32_t row_bytes = (uint32_t)D * (uint32_t)sizeof(T);
+    const uint32_t grp_bytes = (uint32_t)R * row_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    unsigned char* ring = smem + kBarRegion;   // stage s: [x row | dY row]
+    unsigned char* ring = smem + kBarRegion;   // stage s at ring + s * 2 * grp_bytes
 
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = r0 + rows_per_cta < rows ? r0 + rows_per_cta : rows;
     const int64_t nrows = r1 > r0 ? r1 - r0 : 0;
+    const int64_t ngroups = (nrows + R - 1) / R;
 
     uint64_t pol = 0;
-    int64_t issued = 0;   // meaningful in thread 0 only
+    int64_t issued = 0;   // groups issued so far (thread 0 only)
+    auto issue = [&](int64_t grp, int s) {
+        const int64_t first = r0 + grp * R;
+        const int64_t nr = nrows - grp * R < R ? nrows - grp * R : R;
+        const uint32_t bytes = (uint32_t)nr * row_bytes;
+        const uint32_t bar = smem_addr(&bars[s]);
+        unsigned char* st = ring + (size_t)s * 2 * grp_bytes;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_g2s(smem_addr(st), x + first * D, bytes, bar, pol);
+        bulk_g2s(smem_addr(st + grp_bytes), dY + first * D, bytes, bar, pol);
+    };
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&bars[s]), 1);
         mbar_init_fence();
         pol = evict_first_policy();
-        for (; issued < nrows && issued < stages; ++issued) {
-            const int s = (int)issued;
-            const uint32_t bar = smem_addr(&bars[s]);
-            unsigned char* st = ring + (size_t)s * 2 * row_bytes;
-            mbar_arrive_expect_tx(bar, 2 * row_bytes);
-            bulk_g2s(smem_addr(st), x + (r0 + issued) * D, row_bytes, bar, pol);
-            bulk_g2s(smem_addr(st + row_bytes), dY + (r0 + issued) * D, row_bytes, bar, pol);
-        }
+        for (; issued < ngroups && issued < stages; ++issued) issue(issued, (int)issued);
     }
 
-    float g[NV][E], acc_g[NV][E], acc_b[NV][E];
+    constexpr int NP = Pairs<Fmt>::kN;
+    float2 g[NV][NP], acc_g[NV][NP], acc_b[NV][NP];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         const int vi = tid + k * nthreads;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            g[k][e] = vi < nvec ? gamma[vi * E + e] : 0.f;
-            acc_g[k][e] = 0.f;
-            acc_b[k][e] = 0.f;
+        for (int q = 0; q < NP; ++q) {
+            g[k][q] = vi < nvec ? make_float2(gamma[vi * E + 2 * q], gamma[vi * E + 2 * q + 1])
+                                : make_float2(0.f, 0.f);
+            acc_g[k][q] = make_float2(0.f, 0.f);
+            acc_b[k][q] = make_float2(0.f, 0.f);
         }
+    }
+    float mu[R], rs[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        mu[i] = i < nrows ? mean[r0 + i] : 0.f;
+        rs[i] = i < nrows ? inv_std[r0 + i] : 0.f;
     }
     __syncthreads();   // barriers initialised before anyone waits on them
 
     const float inv_D = 1.0f / (float)D;
     int64_t fail_at = -1;
-    for (int64_t i = 0; i < nrows; ++i) {
-        const int s = (int)(i % stages);
-        const uint32_t parity = (uint32_t)((i / stages) & 1);
-        const int64_t r = r0 + i;
-        const float mu = mean[r], rs = inv_std[r];
+    for (int64_t grp = 0; grp < ngroups; ++grp) {
+        const int s = (int)(grp % stages);
+        const uint32_t parity = (uint32_t)((grp / stages) & 1);
+        const int64_t first = r0 + grp * R;
+        const int nr = (int)(nrows - grp * R < R ? nrows - grp * R : R);
+        // Prefetch the next group's statistics while this one is processed.
+        float mu_n[R], rs_n[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int64_t rn = first + R + i;
+            const bool has = rn < r1;
+            mu_n[i] = has ? mean[rn] : 0.f;
+            rs_n[i] = has ? inv_std[rn] : 0.f;
+        }
         const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity);
-        const unsigned char* st = ring + (size_t)s * 2 * row_bytes;
+        const unsigned char* st = ring + (size_t)s * 2 * grp_bytes;
 
-        // Phase 1: the two row sums, from the staged row.
-        float sa = 0.f, sb = 0.f;
-        if (ok) {
+        // Phase 1: the two sums of every row of the group, from the staged rows.
+        float sa[R], sb[R];
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int vi = tid + k * nthreads;
-                if (vi < nvec) {
-                    float xv[E], dy[E];
-                    lds_vec<Fmt>(st + (size_t)vi * 16, xv);
-                    lds_vec<Fmt>(st + row_bytes + (size_t)vi * 16, dy);
+        for (int i = 0; i < R; ++i) {
+            float2 sa2 = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+            if (ok && i < nr) {
+                const float2 nmu = make_float2(-mu[i], -mu[i]), rs2 = make_float2(rs[i], rs[i]);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float xh = (xv[e] - mu) * rs;
-                        const float dxh = dy[e] * g[k][e];
-                        sa += dxh;
-                        sb += dxh * xh;
+                for (int k = 0; k < NV; ++k) {
+                    const int vi = tid + k * nthreads;
+                    if (vi < nvec) {
+                        float2 xv[NP], dy[NP];
+                        lds_pairs<Fmt>(st + (size_t)i * row_bytes + (size_t)vi * 16, xv);
+                        lds_pairs<Fmt>(st + grp_bytes + (size_t)i * row_bytes + (size_t)vi * 16, dy);
+#pragma unroll
+                        for (int q = 0; q < NP; ++q) {
+                            const float2 xh = __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
+                            const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
+                            sa2 = __fadd2_rn(sa2, dxh);
+                            sb2 = __ffma2_rn(dxh, xh, sb2);
+                        }
+                    }
+                }
+            }
+            sa[i] = sa2.x + sa2.y;
+            sb[i] = sb2.x + sb2.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                sa[i] += __shfl_xor_sync(0xffffffffu, sa[i], o);
+                sb[i] += __shfl_xor_sync(0xffffffffu, sb[i], o);
+            }
+        }
+        const int buf = (int)(grp & 1);
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                red[buf][i][0][wid] = sa[i];
+                red[buf][i][1][wid] = sb[i];
+            }
+        }
+        // Past this barrier every thread has finished the previous group entirely,
+        // so its stage can be refilled; this group's stage is still read below.
+        if (__syncthreads_or(!ok)) {
+            fail_at = grp;
+            break;
+        }
+        if (tid == 0 && grp >= 1 && issued < ngroups) {
+            fence_proxy_async_smem();
+            issue(issued, (int)((grp - 1) % stages));
+            ++issued;
+        }
+
+        // Phase 2: dX and the column partials, re-reading the staged rows.
+        //   dX = rs*dxhat - rs*mean_a - rs*mean_b*xhat  (two packed FMAs per pair)
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            if (i < nr) {
+                float a = 0.f, b = 0.f;
+                for (int w = 0; w < nwarps; ++w) {
+                    a += red[buf][i][0][w];
+                    b += red[buf][i][1][w];
+                }
+                const float mean_a = a * inv_D, mean_b = b * inv_D;
+                const float2 nmu = make_float2(-mu[i], -mu[i]), rs2 = make_float2(rs[i], rs[i]);
+                const float c0 = -(rs[i] * mean_a), c1 = -(rs[i] * mean_b);
+                const float2 nc0 = make_float2(c0, c0), nc1 = make_float2(c1, c1);
+                T* dxr = dX + (first + i) * D;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const int vi = tid + k * nthreads;
+                    if (vi < nvec) {
+                        float2 xv[NP], dy[NP], out[NP];
+                        lds_pairs<Fmt>(st + (size_t)i * row_bytes + (size_t)vi * 16, xv);
+                        lds_pairs<Fmt>(st + grp_bytes + (size_t)i * row_bytes + (size_t)vi * 16, dy);
+#pragma unroll
+                        for (int q = 0; q < NP; ++q) {
+                            const float2 xh = __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
+                            const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
+                            out[q] = __ffma2_rn(dxh, rs2, __ffma2_rn(xh, nc1, nc0));
+                            acc_g[k][q] = __ffma2_rn(dy[q], xh, acc_g[k][q]);
+                            acc_b[k][q] = __fadd2_rn(acc_b[k][q], dy[q]);
+                        }
+                        stg_pairs<Fmt>(dxr + (size_t)vi * E, out);
                     }
                 }
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            sa += __shfl_xor_sync(0xffffffffu, sa, o);
-            sb += __shfl_xor_sync(0xffffffffu, sb, o);
-        }
-        const int buf = (int)(i & 1);
-        if (lane == 0) {
-            red[buf][0][wid] = sa;
-            red[buf][1][wid] = sb;
-        }
-        // Past this barrier every thread has finished row i-1 entirely, so its
-        // stage can be refilled; row i's stage is still read below.
-        if (__syncthreads_or(!ok)) {
-            fail_at = i;
-            break;
-        }
-        if (tid == 0 && i >= 1 && issued < nrows) {
-            const int sp = (int)((i - 1) % stages);
-            const uint32_t bar = smem_addr(&bars[sp]);
-            unsigned char* dst = ring + (size_t)sp * 2 * row_bytes;
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, 2 * row_bytes);
-            bulk_g2s(smem_addr(dst), x + (r0 + issued) * D, row_bytes, bar, pol);
-            bulk_g2s(smem_addr(dst + row_bytes), dY + (r0 + issued) * D, row_bytes, bar, pol);
-            ++issued;
-        }
-        float a = 0.f, b = 0.f;
-        for (int w = 0; w < nwarps; ++w) {
-            a += red[buf][0][w];
-            b += red[buf][1][w];
-        }
-        const float mean_a = a * inv_D, mean_b = b * inv_D;
-
-        // Phase 2: dX and the column partials, re-reading the staged row.
-        T* dxr = dX + r * D;
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int vi = tid + k * nthreads;
-            if (vi < nvec) {
-                float xv[E], dy[E], out[E];
-                lds_vec<Fmt>(st + (size_t)vi * 16, xv);
-                lds_vec<Fmt>(st + row_bytes + (size_t)vi * 16, dy);
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xh = (xv[e] - mu) * rs;
-                    const float dxh = dy[e] * g[k][e];
-                    out[e] = rs * (dxh - mean_a - xh * mean_b);
-                    acc_g[k][e] += dy[e] * xh;
-                    acc_b[k][e] += dy[e];
-                }
-                store_vec<Fmt>(dxr + (size_t)vi * E, out);
-            }
+        for (int i = 0; i < R; ++i) {
+            mu[i] = mu_n[i];
+            rs[i] = rs_n[i];
         }
     }
 
     if (fail_at >= 0) {
-        // Rows [fail_at, issued) still have copies in flight (at most one per
+        // Groups [fail_at, issued) still have copies in flight (at most one per
         // stage): wait for them, bounded, before the CTA's shared memory is freed.
         if (tid == 0) {
             atomicExch(err, (int)TB_ERR_TIMEOUT);
@@ -270,6 +384,8 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         __syncthreads();
         return;
     }
+    // Let the column reduction launch; it waits for this grid to finish before reading.
+    griddep_launch_dependents();
 
     float* pg = partials + (size_t)blockIdx.x * 2 * D;
     float* pb = pg + D;
@@ -278,11 +394,11 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         const int vi = tid + k * nthreads;
         if (vi < nvec) {
 #pragma unroll
-            for (int e = 0; e < E; e += 4) {
-                *reinterpret_cast<float4*>(pg + vi * E + e) =
-                    make_float4(acc_g[k][e], acc_g[k][e + 1], acc_g[k][e + 2], acc_g[k][e + 3]);
-                *reinterpret_cast<float4*>(pb + vi * E + e) =
-                    make_float4(acc_b[k][e], acc_b[k][e + 1], acc_b[k][e + 2], acc_b[k][e + 3]);
+            for (int q = 0; q < NP; q += 2) {
+                *reinterpret_cast<float4*>(pg + vi * E + 2 * q) =
+                    make_float4(acc_g[k][q].x, acc_g[k][q].y, acc_g[k][q + 1].x, acc_g[k][q + 1].y);
+                *reinterpret_cast<float4*>(pb + vi * E + 2 * q) =
+                    make_float4(acc_b[k][q].x, acc_b[k][q].y, acc_b[k][q + 1].x, acc_b[k][q + 1].y);
             }
         }
     }
@@ -311,7 +427,7 @@ ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename 
         float sa = 0.f, sb = 0.f;
         for (int64_t j = tid; j < D; j += blockDim.x) {
             const float xh = (Fmt::to_f32(x[off + j]) - mu) * rs;
-            const float dxh = Fmt::to_f32(dY[off + j]) * gamma[j];
+            const float dxh = __fmul_rn(Fmt::to_f32(dY[off + j]), gamma[j]);
             sa += dxh;
             sb += dxh * xh;
         }
@@ -334,52 +450,71 @@ ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename 
         for (int64_t j = tid; j < D; j += blockDim.x) {
             const float dyv = Fmt::to_f32(dY[off + j]);
             const float xh = (Fmt::to_f32(x[off + j]) - mu) * rs;
-            const float dxh = dyv * gamma[j];
+            const float dxh = __fmul_rn(dyv, gamma[j]);
             dX[off + j] = Fmt::from_f32(rs * (dxh - mean_a - xh * mean_b));
             pg[j] += dyv * xh;   // column j belongs to this thread only
             pb[j] += dyv;
         }
     }
+    griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------------ column reduction
 // partials: [G][2][D] fp32 viewed as [G][2D]; out column c < D -> dgamma, else dbeta.
-// Warp w of the CTA sums rows w, w+8, ... in ascending order; the 8 warp sums are
-// then added in warp order.  The order never depends on timing.
-constexpr int kColThreads = 256;
+// A CTA covers 32 columns with 32 warps: warp w sums partial rows w, w+32, ... in
+// ascending order, then the 32 warp sums are added in warp order.  The order never
+// depends on timing, so the result is bitwise reproducible.
+constexpr int kColThreads = 1024;
+constexpr int kColGroups = kColThreads / 32;
 
 __global__ void __launch_bounds__(kColThreads)
 ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t D,
                      float* __restrict__ dgamma, float* __restrict__ dbeta) {
-    __shared__ float sm[kColThreads / 32][33];
+    __shared__ float sm[kColGroups][33];
+    griddep_wait();   // the row kernel (if any) has completed and flushed its partials
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    constexpr int kGroups = kColThreads / 32;
     const int64_t W = 2 * D;
     const int64_t c = (int64_t)blockIdx.x * 32 + lane;
     float acc = 0.f;
     if (c < W) {
         int b = w;
-        // four independent loads in flight, added in the fixed ascending order
-        for (; b + 3 * kGroups < G; b += 4 * kGroups) {
+        for (; b + 3 * kColGroups < G; b += 4 * kColGroups) {
             const float v0 = partials[(int64_t)b * W + c];
-            const float v1 = partials[(int64_t)(b + kGroups) * W + c];
-            const float v2 = partials[(int64_t)(b + 2 * kGroups) * W + c];
-            const float v3 = partials[(int64_t)(b + 3 * kGroups) * W + c];
+            const float v1 = partials[(int64_t)(b + kColGroups) * W + c];
+            const float v2 = partials[(int64_t)(b + 2 * kColGroups) * W + c];
+            const float v3 = partials[(int64_t)(b + 3 * kColGroups) * W + c];
             acc += v0;
             acc += v1;
             acc += v2;
             acc += v3;
         }
-        for (; b < G; b += kGroups) acc += partials[(int64_t)b * W + c];
+        for (; b < G; b += kColGroups) acc += partials[(int64_t)b * W + c];
     }
     sm[w][lane] = acc;
     __syncthreads();
     if (w == 0 && c < W) {
         float t = 0.f;
 #pragma unroll
-        for (int q = 0; q < kGroups; ++q) t += sm[q][lane];
+        for (int q = 0; q < kColGroups; ++q) t += sm[q][lane];
         if (c < D) dgamma[c] = t; else dbeta[c - D] = t;
     }
+}
+
+// Launch the column reduction so that it may be scheduled while the row kernel
+// drains (programmatic dependent launch); it waits inside for the row kernel.
+cudaError_t launch_colsum(const float* ws, int G, int64_t D, float* dgamma, float* dbeta,
+                          cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((2 * D + 31) / 32));
+    cfg.blockDim = dim3(kColThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ln_bwd_colsum_kernel, ws, G, D, dgamma, dbeta);
 }
 
 // ------------------------------------------------------------------ launch planning
@@ -389,36 +524,54 @@ struct LnPlan {
     Path path;
     int threads;
     int nv;          // vectors per thread (ring path)
+    int r;           // rows per ring stage (ring path)
     int stages;      // ring stages
     size_t smem;     // dynamic shared memory (ring path)
     int grid;        // CTAs of the row kernel == partial rows in the workspace
     int64_t rows_per_cta;
 };
 
-template <class Fmt, int NV>
-const void* ring_kernel_ptr() {
-    return reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, NV>);
-}
-
 // Largest NV instantiated: kMaxElemsPerThread columns per thread.
 template <class Fmt>
 constexpr int max_nv() { return kMaxElemsPerThread / Vec<Fmt>::kElems; }
 
-template <class Fmt>
-const void* ring_kernel_for(int nv) {
-    switch (nv) {
-        case 1: return ring_kernel_ptr<Fmt, 1>();
-        case 2: return ring_kernel_ptr<Fmt, 2>();
-        case 4: return ring_kernel_ptr<Fmt, 4>();
-        default: return ring_kernel_ptr<Fmt, max_nv<Fmt>()>();
+// Rows per stage allowed for NV (registers: 2R sums, NV*E columns per thread).
+inline int max_r_for(int nv) { return nv == 1 ? 8 : nv == 2 ? 2 : 1; }
+
+// Op<Fmt, NV, R>::run(args...) for the instantiated (nv, r) pair.
+template <class Fmt, template <class, int, int> class Op, class... Args>
+auto with_ring_variant(int nv, int r, Args&&... args) {
+    if (nv == 1) {
+        if (r >= 8) return Op<Fmt, 1, 8>::run(args...);
+        if (r >= 4) return Op<Fmt, 1, 4>::run(args...);
+        if (r >= 2) return Op<Fmt, 1, 2>::run(args...);
+        return Op<Fmt, 1, 1>::run(args...);
     }
+    if (nv == 2) {
+        if (r >= 2) return Op<Fmt, 2, 2>::run(args...);
+        return Op<Fmt, 2, 1>::run(args...);
+    }
+    if (nv == 4) return Op<Fmt, 4, 1>::run(args...);
+    return Op<Fmt, max_nv<Fmt>(), 1>::run(args...);
 }
 
-const void* ring_kernel(tb_dtype dt, int nv) {
+template <class Fmt, int NV, int R>
+struct RingPtr {
+    static const void* run() {
+        return reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, NV, R>);
+    }
+};
+
+template <class Fmt>
+const void* ring_kernel_for(int nv, int r) {
+    return with_ring_variant<Fmt, RingPtr>(nv, r);
+}
+
+const void* ring_kernel(tb_dtype dt, int nv, int r) {
     switch (dt) {
-        case TB_F32: return ring_kernel_for<F32>(nv);
-        case TB_BF16: return ring_kernel_for<BF16>(nv);
-        default: return ring_kernel_for<F16>(nv);
+        case TB_F32: return ring_kernel_for<F32>(nv, r);
+        case TB_BF16: return ring_kernel_for<BF16>(nv, r);
+        default: return ring_kernel_for<F16>(nv, r);
     }
 }
 
@@ -441,14 +594,18 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
     // Ring path: at most kMaxElemsPerThread columns per thread (gamma and the two
     // partial sums live in registers), i.e. D <= 8192.
     if (aligned && row_bytes % 16 == 0 && D <= (int64_t)kMaxElemsPerThread * kRowThreads) {
-        int threads = (int)std::min<int64_t>(kRowThreads, (nvec + 31) / 32 * 32);
+        const int threads = (int)std::min<int64_t>(kRowThreads, (nvec + 31) / 32 * 32);
         int nv = (int)((nvec + threads - 1) / threads);
         nv = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : 8;
-        const int64_t stage_bytes = 2 * row_bytes;
-        int stages = (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
-        size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
+        // Rows per stage: about 16 KB of x (and as much dY) per stage.
+        int r = 1;
+        while (r < max_r_for(nv) && (int64_t)(2 * r) * row_bytes <= kStageTargetBytes / 2) r *= 2;
+        const int64_t stage_bytes = 2 * (int64_t)r * row_bytes;
+        const int stages =
+            (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
+        const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
         if ((int64_t)smem <= info.max_smem_optin) {
-            const void* k = ring_kernel(dt, nv);
+            const void* k = ring_kernel(dt, nv, r);
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
                 cudaSuccess)
                 return false;
@@ -458,6 +615,7 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
             p->path = Path::kRing;
             p->threads = threads;
             p->nv = nv;
+            p->r = r;
             p->stages = stages;
             p->smem = smem;
             p->grid = info.sm_count * std::max(per_sm, 1);
@@ -470,6 +628,7 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
             return false;
         p->threads = kRowThreads;
         p->nv = 0;
+        p->r = 0;
         p->stages = 0;
         p->smem = 0;
         p->grid = info.sm_count * std::min(std::max(per_sm, 1), 2);
@@ -483,6 +642,18 @@ size_t workspace_bytes_for(const LnPlan& p, int64_t D) {
     return (size_t)p.grid * 2 * (size_t)D * sizeof(float);
 }
 
+template <class Fmt, int NV, int R>
+struct RingLaunch {
+    using T = typename Fmt::T;
+    static int run(const LnPlan& p, const T* dy, const T* x, const float* mean, const float* inv_std,
+                   const float* gamma, T* dx, float* ws, int64_t rows, int D, int* err,
+                   cudaStream_t st) {
+        ln_bwd_rows_ring_kernel<Fmt, NV, R><<<p.grid, p.threads, p.smem, st>>>(
+            dy, x, mean, inv_std, gamma, dx, ws, rows, D, p.stages, p.rows_per_cta, err);
+        return 0;
+    }
+};
+
 template <class Fmt>
 void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* mean,
                  const float* inv_std, const float* gamma, void* dX, float* ws, int64_t rows,
@@ -492,25 +663,8 @@ void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* me
     const T* xx = static_cast<const T*>(x);
     T* dx = static_cast<T*>(dX);
     if (p.path == Path::kRing) {
-        const int Di = (int)D;
-        switch (p.nv) {
-            case 1:
-                ln_bwd_rows_ring_kernel<Fmt, 1><<<p.grid, p.threads, p.smem, st>>>(
-                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
-                break;
-            case 2:
-                ln_bwd_rows_ring_kernel<Fmt, 2><<<p.grid, p.threads, p.smem, st>>>(
-                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
-                break;
-            case 4:
-                ln_bwd_rows_ring_kernel<Fmt, 4><<<p.grid, p.threads, p.smem, st>>>(
-                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
-                break;
-            default:
-                ln_bwd_rows_ring_kernel<Fmt, max_nv<Fmt>()><<<p.grid, p.threads, p.smem, st>>>(
-                    dy, xx, mean, inv_std, gamma, dx, ws, rows, Di, p.stages, p.rows_per_cta, err);
-                break;
-        }
+        with_ring_variant<Fmt, RingLaunch>(p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws,
+                                            rows, (int)D, err, st);
     } else {
         ln_bwd_rows_plain_kernel<Fmt><<<p.grid, p.threads, 0, st>>>(dy, xx, mean, inv_std, gamma, dx,
                                                                    ws, rows, D, p.rows_per_cta);
@@ -574,12 +728,8 @@ extern "C" tb_status tb_layernorm_bwd(const void* dY, const void* x, const float
     DeviceInfo info{};
     if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int64_t W = 2 * D;
-    const unsigned col_grid = (unsigned)((W + 31) / 32);
-    if (rows == 0) {
-        ln_bwd_colsum_kernel<<<col_grid, kColThreads, 0, st>>>(nullptr, 0, D, dgamma, dbeta);
-        return launch_status();
-    }
+    if (rows == 0)
+        return launch_colsum(nullptr, 0, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
     const bool aligned = aligned_to(dY, 16) && aligned_to(x, 16) && aligned_to(dX, 16) &&
                          aligned_to(gamma, 16) && aligned_to(workspace, 16);
     LnPlan p;
@@ -595,6 +745,5 @@ extern "C" tb_status tb_layernorm_bwd(const void* dY, const void* x, const float
         default: launch_rows<F16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
     }
     if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
-    ln_bwd_colsum_kernel<<<col_grid, kColThreads, 0, st>>>(ws, p.grid, D, dgamma, dbeta);
-    return launch_status();
+    return launch_colsum(ws, p.grid, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }
