@@ -34,10 +34,24 @@ METRIC = ("AdamW step Gparams/s + GB/s as % of GB300 HBM peak; softmax/LN bwd GB
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 LOSS_SCALE = 65536.0
 
-# Workload (sizes of the full configurations).
+# Workloads.  "full": the sizes of the headline configurations.  "small": the same
+# kernels on the GPT-2-small table and half the attention rows (~3 GB resident),
+# used for profiler captures.
 SM_ROWS, SM_COLS = 8 * 12 * 1024, 1024
 LN_ROWS, LN_D = 8 * 2048, 4096
+WORKLOADS = {
+    "full": dict(table="llama7b", grad_std=1e-4, sm_rows=SM_ROWS, ln_rows=LN_ROWS),
+    "small": dict(table="gpt2", grad_std=1e-3, sm_rows=SM_ROWS // 2, ln_rows=LN_ROWS),
+}
 FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_TEXT = {
+    "full": ("Llama-7B-shaped fused AdamW (291 tensors, 6,738,415,616 params, bf16 grads x65536, "
+             "fp32 master/m/v, bf16 copy) + softmax bwd 98,304x1,024 causal fp32 and bf16 + "
+             "LayerNorm bwd 16,384x4,096 bf16"),
+    "small": ("GPT-2-small-shaped fused AdamW (148 tensors, 124,439,808 params) + softmax bwd "
+              "49,152x1,024 causal fp32 and bf16 + LayerNorm bwd 16,384x4,096 bf16 "
+              "(profiling size)"),
+}
 
 
 def adamw_bytes(n_params: int) -> int:
@@ -81,6 +95,11 @@ def reduce_over_ranks(values, op="max"):
     t = torch.tensor(list(values), dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return t.cpu().tolist()
+
+
+def job_gbs(world: int, bytes_per_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_step * steps / (max_ms / 1e3) / 1e9
 
 
 def barrier():
@@ -145,38 +164,41 @@ class ClockSampler:
 class HotPath:
     """Device buffers and the C-ABI calls of one step."""
 
-    def __init__(self, device):
+    def __init__(self, device, workload="full"):
         import torch
         import ln_backward_gb300 as tb
         from ln_backward_gb300 import synth
         self.tb, self.torch = tb, torch
         self.dev = device
-        self.st = synth.make_adamw_state(synth.llama7b_shapes(), seed=0, device=device,
-                                         grad_std=1e-4, loss_scale=LOSS_SCALE)
+        w = WORKLOADS[workload]
+        shapes = synth.llama7b_shapes() if w["table"] == "llama7b" else synth.gpt2_small_shapes()
+        sm_rows, ln_rows = w["sm_rows"], w["ln_rows"]
+        self.st = synth.make_adamw_state(shapes, seed=0, device=device,
+                                         grad_std=w["grad_std"], loss_scale=LOSS_SCALE)
         k = len(self.st.sizes)
         self.plan = tb.tb_adamw_plan_create(*[[self.st.tensor(a, i) for i in range(k)]
                                               for a in ("theta", "m", "v", "grad", "copy")])
-        self.P32, self.dY32 = synth.softmax_inputs(SM_ROWS, SM_COLS, torch.float32, seed=1,
+        self.P32, self.dY32 = synth.softmax_inputs(sm_rows, SM_COLS, torch.float32, seed=1,
                                                    device=device, causal_period=1024)
-        self.P16, self.dY16 = synth.softmax_inputs(SM_ROWS, SM_COLS, torch.bfloat16, seed=2,
+        self.P16, self.dY16 = synth.softmax_inputs(sm_rows, SM_COLS, torch.bfloat16, seed=2,
                                                    device=device, causal_period=1024)
         self.dX32 = torch.empty_like(self.P32)
         self.dX16 = torch.empty_like(self.P16)
         (self.x, self.ldY, self.mean, self.rstd,
-         self.gamma) = synth.layernorm_inputs(LN_ROWS, LN_D, torch.bfloat16, seed=3, device=device,
+         self.gamma) = synth.layernorm_inputs(ln_rows, LN_D, torch.bfloat16, seed=3, device=device,
                                               eps=1e-5, dy_std=1e-2)
         self.ldX = torch.empty_like(self.x)
         self.dg = torch.empty(LN_D, device=device)
         self.db = torch.empty(LN_D, device=device)
-        ws = tb.tb_layernorm_bwd_workspace_size(LN_ROWS, LN_D, torch.bfloat16)
+        ws = tb.tb_layernorm_bwd_workspace_size(ln_rows, LN_D, torch.bfloat16)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         self.t = 0
         self.n_params = self.st.n_params
         self.bytes = {
             "adamw": adamw_bytes(self.n_params),
-            "softmax_f32": softmax_bytes(SM_ROWS, SM_COLS, 4),
-            "softmax_bf16": softmax_bytes(SM_ROWS, SM_COLS, 2),
-            "layernorm_bf16": layernorm_bytes(LN_ROWS, LN_D, 2),
+            "softmax_f32": softmax_bytes(sm_rows, SM_COLS, 4),
+            "softmax_bf16": softmax_bytes(sm_rows, SM_COLS, 2),
+            "layernorm_bf16": layernorm_bytes(ln_rows, LN_D, 2),
         }
         self.launches_per_step = 1 + 1 + 1 + 2
 
@@ -204,7 +226,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    hp_path = HotPath(dev)
+    hp_path = HotPath(dev, args.workload)
     names = ["adamw", "softmax_f32", "softmax_bf16", "layernorm_bf16"]
     K, W = args.steps, args.warmup
 
@@ -237,7 +259,7 @@ def run_ours(args):
     total_ms, mean_ms = red[0], dict(zip(names, red[1:]))
 
     step_bytes = sum(hp_path.bytes.values())
-    value = world * step_bytes * K / (total_ms / 1e3) / 1e9
+    value = job_gbs(world, step_bytes, K, total_ms)
     peak, peak_kind = measured_peak()
     kernels = {}
     for n in names:
@@ -250,10 +272,10 @@ def run_ours(args):
     e2e = run_e2e(hp_path, K) if not args.no_e2e else None
     if e2e is not None:
         e2e_ms = reduce_over_ranks([e2e.pop("ms")], "max")[0]
-        e2e["value"] = round(world * step_bytes * K / (e2e_ms / 1e3) / 1e9, 1)
+        e2e["value"] = round(job_gbs(world, step_bytes, K, e2e_ms), 1)
 
     cpu = None
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and args.workload == "full":
         cpu = cpu_baseline(seconds_budget=args.cpu_seconds)
 
     if rank == 0:
@@ -263,9 +285,7 @@ def run_ours(args):
             "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {
-                "workload": ("Llama-7B-shaped fused AdamW (291 tensors, 6,738,415,616 params, bf16 "
-                             "grads x65536, fp32 master/m/v, bf16 copy) + softmax bwd 98,304x1,024 "
-                             "causal fp32 and bf16 + LayerNorm bwd 16,384x4,096 bf16"),
+                "workload": WORKLOAD_TEXT[args.workload],
                 "bytes_per_step": step_bytes,
                 "adamw_gparams_per_s": kernels["adamw"]["gparams_s"],
                 "l2": "no flush: every launch streams far more than the 129 MB L2",
@@ -443,6 +463,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
     args = ap.parse_args(argv)
     if args.warmup < 1:
         ap.error("--warmup must be >= 1 (timed numbers use the default of 3)")
