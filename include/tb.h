@@ -216,6 +216,44 @@ tb_status tb_layernorm_bwd(const void* dY, const void* x, const float* mean,
                            int64_t rows, int64_t D, tb_dtype io_dtype,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * tb_layernorm_bwd_noalloc -- the same LayerNorm backward as tb_layernorm_bwd,
+ * for callers that cannot allocate device memory when they run it.  (The pages
+ * have no counterpart: this is a convenience of this library.)
+ *
+ * Who needs it: code that runs where a cudaMalloc is not an option -- inside a
+ * framework that hands out every byte of device memory from its own pool (a
+ * stray allocation there fails or fragments the pool), or a step loop that must
+ * not call cudaMalloc/cudaFree because they can synchronise with the device.
+ * Such callers have no buffer to pass as `workspace`, so this entry point keeps
+ * its scratch (the per-CTA dgamma/dbeta partial sums) in a fixed array inside
+ * the library and allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library call.
+ *
+ * The array holds TB_LAYERNORM_NOALLOC_SCRATCH_BYTES (16 MiB).  Every GPU that
+ * loads the library holds it until the process exits.  A shape whose partial
+ * sums would not fit runs with fewer CTAs; D > 2,097,152 (more than the array
+ * holds for a single CTA) is rejected with TB_ERR_WORKSPACE.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the one array and it keeps the last
+ * call's contents (each call overwrites every part it later reads, so nothing
+ * has to start at zero): calls whose work overlaps on the GPU -- for example on
+ * two streams at once -- race on it and must be serialised by the caller.
+ *
+ * Arguments, results and errors are those of tb_layernorm_bwd without
+ * `workspace` and `workspace_bytes`; results equal tb_layernorm_bwd's bit for
+ * bit whenever the partial sums fit with the usual number of CTAs (for example
+ * 16,384 x 4,096 bf16), and agree within rounding otherwise.
+ */
+#define TB_LAYERNORM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+tb_status tb_layernorm_bwd_noalloc(const void* dY, const void* x, const float* mean,
+                                   const float* inv_std, const float* gamma,
+                                   void* dX, float* dgamma, float* dbeta,
+                                   int64_t rows, int64_t D, tb_dtype io_dtype, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -26,7 +26,7 @@ STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_VALUE", 2: "TB_ERR_UNSUPPORTED_DTYPE",
 # Every symbol include/tb.h declares.
 EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_create",
            "tb_adamw_step", "tb_adamw_plan_destroy", "tb_softmax_bwd",
-           "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd")
+           "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd", "tb_layernorm_bwd_noalloc")
 
 
 class TbError(RuntimeError):
@@ -71,6 +71,8 @@ def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.tb_layernorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, vp,
                                      ctypes.c_size_t, vp]
     lib.tb_layernorm_bwd.restype = i32
+    lib.tb_layernorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
+    lib.tb_layernorm_bwd_noalloc.restype = i32
     return lib
 
 
@@ -211,3 +213,22 @@ def tb_layernorm_bwd(dY: torch.Tensor, x: torch.Tensor, mean: torch.Tensor, inv_
            lib.tb_layernorm_bwd(_ptr(dY), _ptr(x), _ptr(mean), _ptr(inv_std), _ptr(gamma),
                                 _ptr(dX), _ptr(dgamma), _ptr(dbeta), rows, D, _dtype(x), ws_ptr,
                                 ws_bytes, _stream(stream)))
+
+
+def tb_layernorm_bwd_noalloc(dY: torch.Tensor, x: torch.Tensor, mean: torch.Tensor,
+                             inv_std: torch.Tensor, gamma: torch.Tensor, dX: torch.Tensor,
+                             dgamma: torch.Tensor, dbeta: torch.Tensor, stream=None) -> None:
+    """tb_layernorm_bwd without a workspace: the library's own fixed scratch array is
+    used, nothing is allocated (see include/tb.h for the limits)."""
+    if x.dim() != 2 or dY.shape != x.shape or dX.shape != x.shape:
+        raise ValueError("x, dY and dX must be [rows, D] tensors of one shape")
+    if not (dY.dtype == x.dtype == dX.dtype):
+        raise ValueError("x, dY and dX must share a dtype")
+    for t in (mean, inv_std, gamma, dgamma, dbeta):
+        if t.dtype != torch.float32:
+            raise ValueError("mean, inv_std, gamma, dgamma and dbeta are fp32")
+    rows, D = x.shape
+    _check("tb_layernorm_bwd_noalloc",
+           lib.tb_layernorm_bwd_noalloc(_ptr(dY), _ptr(x), _ptr(mean), _ptr(inv_std), _ptr(gamma),
+                                        _ptr(dX), _ptr(dgamma), _ptr(dbeta), rows, D, _dtype(x),
+                                        _stream(stream)))

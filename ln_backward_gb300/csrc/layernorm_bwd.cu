@@ -30,6 +30,7 @@
 // the CTA sets the device error word, waits (bounded) for the copies it issued
 // and returns.
 #include <algorithm>
+#include <mutex>
 
 #include "tb_common.cuh"
 
@@ -739,6 +740,94 @@ extern "C" tb_status tb_layernorm_bwd(const void* dY, const void* x, const float
     int* err = device_error_word();
     if (!err) return TB_ERR_CUDA;
     float* ws = static_cast<float*>(workspace);
+    switch (io_dtype) {
+        case TB_F32: launch_rows<F32>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
+        case TB_BF16: launch_rows<BF16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
+        default: launch_rows<F16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
+    return launch_colsum(ws, p.grid, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ entry point without allocation
+// Scratch for tb_layernorm_bwd_noalloc: the per-CTA column partials live in this
+// file-scope device array instead of a caller workspace.  Every device that loads
+// the library holds it (16 MiB) until the process exits.  Host code must not pass
+// the symbol itself to a kernel: its device address is looked up per device.
+namespace tb {
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+constexpr int64_t kNoAllocScratchFloats = (int64_t)(kNoAllocScratchBytes / sizeof(float));
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) float g_ln_scratch[kNoAllocScratchFloats];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_ln_scratch on `dev` (which must be current); nullptr on error.
+float* noalloc_scratch(int dev) {
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ln_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    return g_scratch_ptr[dev];
+}
+}  // namespace
+}  // namespace tb
+
+extern "C" tb_status tb_layernorm_bwd_noalloc(const void* dY, const void* x, const float* mean,
+                                              const float* inv_std, const float* gamma, void* dX,
+                                              float* dgamma, float* dbeta, int64_t rows, int64_t D,
+                                              tb_dtype io_dtype, void* stream) {
+    using namespace tb;
+    if (rows < 0 || D < 0) return TB_ERR_INVALID_VALUE;
+    if (!dtype_valid(io_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (D == 0) return TB_OK;
+    // Even one CTA needs 2*D partial sums: D beyond the scratch capacity is rejected.
+    if (2 * D > kNoAllocScratchFloats) return TB_ERR_WORKSPACE;
+    if (!dgamma || !dbeta || !gamma) return TB_ERR_INVALID_VALUE;
+    if (rows > 0 && (!dY || !x || !mean || !inv_std || !dX)) return TB_ERR_INVALID_VALUE;
+    if (rows > 0 && D > INT64_MAX / rows / 4) return TB_ERR_INVALID_VALUE;
+    const size_t es = dtype_size(io_dtype);
+    if (!aligned_to(dgamma, 4) || !aligned_to(dbeta, 4) || !aligned_to(gamma, 4)) return TB_ERR_MISALIGNED;
+    if (rows > 0 && (!aligned_to(dY, es) || !aligned_to(x, es) || !aligned_to(dX, es) ||
+                     !aligned_to(mean, 4) || !aligned_to(inv_std, 4)))
+        return TB_ERR_MISALIGNED;
+    const int64_t n = rows * D;
+    const Range ins[5] = {range_of(dY, n, es), range_of(x, n, es), range_of(mean, rows, 4),
+                          range_of(inv_std, rows, 4), range_of(gamma, D, 4)};
+    const Range outs[3] = {range_of(dX, n, es), range_of(dgamma, D, 4), range_of(dbeta, D, 4)};
+    for (const Range& o : outs)
+        for (const Range& in : ins)
+            if (overlap(o, in)) return TB_ERR_ALIAS;
+    for (int a = 0; a < 3; ++a)
+        for (int b = a + 1; b < 3; ++b)
+            if (overlap(outs[a], outs[b])) return TB_ERR_ALIAS;
+
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (rows == 0)
+        return launch_colsum(nullptr, 0, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+    float* ws = noalloc_scratch(dev);
+    int* err = device_error_word();
+    if (!ws || !err) return TB_ERR_CUDA;
+    const bool aligned = aligned_to(dY, 16) && aligned_to(x, 16) && aligned_to(dX, 16) &&
+                         aligned_to(gamma, 16);
+    LnPlan p;
+    if (!make_plan(rows, D, io_dtype, aligned, info, &p)) return TB_ERR_CUDA;
+    // Fewer CTAs when their partial sums would not fit in the scratch array.
+    const int64_t max_grid = kNoAllocScratchFloats / (2 * D);
+    if (p.grid > max_grid) {
+        p.grid = (int)max_grid;
+        p.rows_per_cta = (rows + p.grid - 1) / p.grid;
+    }
+    // Every CTA overwrites its whole partial row, so nothing needs clearing first.
     switch (io_dtype) {
         case TB_F32: launch_rows<F32>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
         case TB_BF16: launch_rows<BF16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
