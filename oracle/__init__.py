@@ -63,6 +63,7 @@ def _configure(lib):
         getattr(lib, name).argtypes = [i64, i64, vp, vp, vp]
     for name in ("orc_layernorm_bwd_f64", "orc_layernorm_bwd_f32"):
         getattr(lib, name).argtypes = [i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.orc_rmsnorm_bwd_f64.argtypes = [i64, i64, vp, vp, vp, vp, vp, vp]
     return lib
 
 
@@ -220,6 +221,22 @@ def layernorm_bwd_f32(dY, x, mean, inv_std, gamma):
     _load().orc_layernorm_bwd_f32(rows, D, _ptr(dY), _ptr(x), _ptr(mean), _ptr(inv_std),
                                   _ptr(gamma), _ptr(dX), _ptr(dg), _ptr(db))
     return dX, dg, db
+
+
+# --------------------------------------------------------------------------- RMSNorm bwd
+def rmsnorm_bwd_f64(dY, x, inv_rms, gamma):
+    """Returns ``(dX, dgamma)`` in float64."""
+    dY = _c(dY, np.float64)
+    x = _c(x, np.float64)
+    inv_rms = _c(inv_rms, np.float64)
+    gamma = _c(gamma, np.float64)
+    rows, D = x.shape
+    assert dY.shape == x.shape and inv_rms.shape == (rows,) and gamma.shape == (D,)
+    dX = np.empty_like(x)
+    dg = np.empty(D, np.float64)
+    _load().orc_rmsnorm_bwd_f64(rows, D, _ptr(dY), _ptr(x), _ptr(inv_rms), _ptr(gamma),
+                                _ptr(dX), _ptr(dg))
+    return dX, dg
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -1,7 +1,7 @@
 /*
  * oracle.c -- plain, slow, single-threaded CPU oracle for the memory-bound half
  * of an LLM training step: the fused mixed-precision AdamW update, the row-wise
- * softmax backward and the LayerNorm backward.
+ * softmax backward, the LayerNorm backward and the RMSNorm backward.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
  * this file.  Its users are the test-suite, the smoke check and the CPU-baseline
@@ -325,6 +325,39 @@ void orc_layernorm_bwd_f32(int64_t rows, int64_t D,
             dxr[j] = rs * (dxhat - mean_dxhat - xhat * mean_dxhat_xhat);
             dgamma[j] += dyr[j] * xhat;
             dbeta[j] += dyr[j];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* RMSNorm backward from the saved per-row inv_rms.                           */
+/*   Forward: y = gamma * xhat, xhat = x * inv_rms, inv_rms = 1/sqrt(mean_D(x^2) + eps): */
+/*   the LayerNorm of [GPU-Opt-P2] §2.2 "LayerNorm 反向" without the mean      */
+/*   subtraction and without beta (the norm layers of the Llama-7B table).     */
+/*   Chain rule through inv_rms gives, per row:                                */
+/*     dxhat = dY * gamma                                                      */
+/*     dX    = inv_rms * (dxhat - xhat * mean_D(dxhat * xhat))                 */
+/*   and per column j: dgamma_j = sum_rows dY*xhat.                             */
+/* ------------------------------------------------------------------------- */
+
+void orc_rmsnorm_bwd_f64(int64_t rows, int64_t D,
+                         const double* dY, const double* x, const double* inv_rms,
+                         const double* gamma, double* dX, double* dgamma)
+{
+    for (int64_t j = 0; j < D; ++j) dgamma[j] = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * D;
+        const double* dyr = dY + r * D;
+        double* dxr = dX + r * D;
+        double rs = inv_rms[r];
+        double sum_dxhat_xhat = 0.0;
+        for (int64_t j = 0; j < D; ++j) sum_dxhat_xhat += (dyr[j] * gamma[j]) * (xr[j] * rs);
+        double mean_dxhat_xhat = sum_dxhat_xhat / (double)D;
+        for (int64_t j = 0; j < D; ++j) {
+            double xhat = xr[j] * rs;
+            double dxhat = dyr[j] * gamma[j];
+            dxr[j] = rs * (dxhat - xhat * mean_dxhat_xhat);
+            dgamma[j] += dyr[j] * xhat;
         }
     }
 }

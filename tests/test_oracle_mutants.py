@@ -9,6 +9,7 @@ import pytest
 
 import test_oracle_adamw as A
 import test_oracle_layernorm as L
+import test_oracle_rmsnorm as RN
 import test_oracle_softmax as S
 
 ADAMW_PINS = [A.test_step1_closed_form, A.test_constant_gradient_no_decay,
@@ -20,7 +21,18 @@ LN_PINS = [L.test_dbeta_is_column_sum, L.test_rows_of_dx_sum_to_zero,
            L.test_dx_orthogonal_to_xhat_when_eps_zero, L.test_d_equals_one_is_degenerate,
            L.test_central_finite_differences, L.test_matches_torch_autograd_float64]
 
+RMS_PINS = [RN.test_dgamma_is_column_sum_of_dy_xhat, RN.test_dx_orthogonal_to_xhat_when_eps_zero,
+            RN.test_central_finite_differences, RN.test_matches_torch_rms_norm_autograd_float64]
+
 MUTANTS = [
+    ("rmsnorm: projection term dropped",
+     "dxr[j] = rs * (dxhat - xhat * mean_dxhat_xhat);", "dxr[j] = rs * dxhat;", RMS_PINS),
+    ("rmsnorm: projection term sign flipped",
+     "dxr[j] = rs * (dxhat - xhat * mean_dxhat_xhat);",
+     "dxr[j] = rs * (dxhat + xhat * mean_dxhat_xhat);", RMS_PINS),
+    ("rmsnorm: gamma not applied",
+     "sum_dxhat_xhat += (dyr[j] * gamma[j]) * (xr[j] * rs);",
+     "sum_dxhat_xhat += dyr[j] * (xr[j] * rs);", RMS_PINS),
     ("adamw: decay added instead of subtracted",
      "- lr * wd * th;", "+ lr * wd * th;", ADAMW_PINS),
     ("adamw: first-moment bias correction dropped",
