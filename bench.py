@@ -68,6 +68,21 @@ def layernorm_bytes(rows: int, D: int, esize: int) -> int:
     return 3 * esize * rows * D + 8 * rows + 12 * D
 
 
+def causal_softmax_bytes(rows: int, cols: int, period: int, offset: int, esize: int) -> int:
+    """Reads of the 16-byte vectors holding an open column of P and dY, plus all of dX."""
+    import numpy as np
+    per_vec = 16 // esize
+    r = np.arange(rows, dtype=np.int64)
+    valid = np.minimum(cols, r % period + 1 + offset)
+    vecs = (valid + per_vec - 1) // per_vec
+    return int(2 * 16 * vecs.sum() + esize * rows * cols)
+
+
+def rmsnorm_bytes(rows: int, D: int, esize: int) -> int:
+    # read x, dY; write dX; + inv_rms per row; + gamma, dgamma per column
+    return 3 * esize * rows * D + 4 * rows + 8 * D
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -201,6 +216,29 @@ class HotPath:
             "layernorm_bf16": layernorm_bytes(ln_rows, LN_D, 2),
         }
         self.launches_per_step = 1 + 1 + 1 + 2
+        self.sm_rows, self.ln_rows = sm_rows, ln_rows
+        # Inputs of the rows beyond the timed step (measured separately).
+        (self.rx, self.rdY, self.rinv, self.rgamma) = synth.rmsnorm_inputs(
+            ln_rows, LN_D, torch.bfloat16, seed=4, device=device, dy_std=1e-2)
+        self.rdX = torch.empty_like(self.rx)
+        self.rdg = torch.empty(LN_D, device=device)
+        self.rws = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(ln_rows, LN_D, torch.bfloat16),
+                               dtype=torch.uint8, device=device)
+
+    def extras(self):
+        """name -> (callable, algorithmic bytes) for the kernels outside the step."""
+        tb = self.tb
+        return {
+            "softmax_causal_f32": (lambda: tb.tb_softmax_bwd_causal(self.dY32, self.P32, self.dX32,
+                                                                    period=1024),
+                                   causal_softmax_bytes(self.sm_rows, SM_COLS, 1024, 0, 4)),
+            "softmax_causal_bf16": (lambda: tb.tb_softmax_bwd_causal(self.dY16, self.P16, self.dX16,
+                                                                     period=1024),
+                                    causal_softmax_bytes(self.sm_rows, SM_COLS, 1024, 0, 2)),
+            "rmsnorm_bf16": (lambda: tb.tb_rmsnorm_bwd(self.rdY, self.rx, self.rinv, self.rgamma,
+                                                       self.rdX, self.rdg, self.rws),
+                             rmsnorm_bytes(self.ln_rows, LN_D, 2)),
+        }
 
     def step(self, events=None):
         tb = self.tb
@@ -269,6 +307,7 @@ def run_ours(args):
     kernels["adamw"]["gparams_s"] = round(hp_path.n_params / (mean_ms["adamw"] / 1e3) / 1e9, 2)
     ad_gbs = kernels["adamw"]["GB_s"]
 
+    extras = time_extras(hp_path, reps=max(K, 10), peak=measured_peak()[0])
     e2e = run_e2e(hp_path, K) if not args.no_e2e else None
     if e2e is not None:
         e2e_ms = reduce_over_ranks([e2e.pop("ms")], "max")[0]
@@ -293,6 +332,7 @@ def run_ours(args):
                 "wall_s_timed_region": round(wall, 3),
             },
             "kernels": kernels,
+            "extras": extras,
             "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
                          "frac": round(ad_gbs / peak, 4), "traffic": ADAMW_TRAFFIC_PER_LAUNCH,
                          "kernel": "adamw_multi_tensor_kernel", "peak_source": peak_kind},
@@ -309,6 +349,27 @@ def run_ours(args):
 # Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, from
 # ncu; None until a capture of the current kernel exists.
 ADAMW_TRAFFIC_PER_LAUNCH = None
+
+
+def time_extras(hp_path, reps, peak):
+    """Per-kernel CUDA-event timing of the kernels that are not part of the step."""
+    import torch
+    out = {}
+    for name, (fn, nbytes) in hp_path.extras().items():
+        for _ in range(3):
+            fn()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        ms = reduce_over_ranks([s.elapsed_time(e) / reps], "max")[0]
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms": round(ms, 4), "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                     "bytes": nbytes}
+    return out
 
 
 def run_e2e(hp_path, K):

@@ -167,6 +167,24 @@ tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan);
 tb_status tb_softmax_bwd(const void* dY, const void* P, void* dX,
                          int64_t rows, int64_t cols, tb_dtype dtype, void* stream);
 
+/*
+ * tb_softmax_bwd_causal -- tb_softmax_bwd for the rows of causally masked
+ * attention, reading only the part of each row the mask left open.
+ * Row r can be nonzero only on its first
+ *     valid(r) = min(cols, (r mod period) + 1 + offset)
+ * columns: `period` is the query length S_q of one (batch, head) block whose
+ * rows are stacked, `offset` = S_k - S_q (0 for square self-attention).  P must
+ * be exactly 0 on every other column, as a masked forward softmax leaves it; the
+ * kernel never reads those columns of P or dY and writes +0 to dX there.  The
+ * result equals tb_softmax_bwd's on such inputs (masked entries are +-0 there).
+ * HBM traffic per row: reads of the valid columns (rounded up to 16-byte
+ * vectors) plus the full row of dX written.
+ *   period >= 1, offset >= 0; other arguments and errors as tb_softmax_bwd.
+ */
+tb_status tb_softmax_bwd_causal(const void* dY, const void* P, void* dX, int64_t rows,
+                                int64_t cols, int64_t period, int64_t offset,
+                                tb_dtype dtype, void* stream);
+
 /* ======================================================================== */
 /* LayerNorm backward                                                        */
 /* ======================================================================== */
@@ -215,6 +233,28 @@ tb_status tb_layernorm_bwd(const void* dY, const void* x, const float* mean,
                            void* dX, float* dgamma, float* dbeta,
                            int64_t rows, int64_t D, tb_dtype io_dtype,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ======================================================================== */
+/* RMSNorm backward                                                          */
+/* ======================================================================== */
+/*
+ * The LayerNorm above without the mean subtraction and without beta (the norm
+ * layers of Llama-style models): forward y = gamma * x * inv_rms with
+ * inv_rms = 1/sqrt(mean_D(x^2) + eps).  Backward, per row and per column:
+ *     dxhat  = dY * gamma,  xhat = x * inv_rms
+ *     dX     = inv_rms * (dxhat - xhat * mean_D(dxhat * xhat))
+ *     dgamma = sum over rows of dY * xhat      (overwritten, two-stage, deterministic)
+ * Same kernels, layouts, alignment rules and errors as tb_layernorm_bwd, with
+ * inv_rms in place of mean/inv_std and no dbeta.  The workspace is half the
+ * LayerNorm one (one partial row of D floats per CTA).
+ */
+tb_status tb_rmsnorm_bwd_workspace_size(int64_t rows, int64_t D, tb_dtype io_dtype,
+                                        size_t* bytes);
+
+tb_status tb_rmsnorm_bwd(const void* dY, const void* x, const float* inv_rms,
+                         const float* gamma, void* dX, float* dgamma,
+                         int64_t rows, int64_t D, tb_dtype io_dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * tb_layernorm_bwd_noalloc -- the same LayerNorm backward as tb_layernorm_bwd,

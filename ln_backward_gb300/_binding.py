@@ -26,7 +26,8 @@ STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_VALUE", 2: "TB_ERR_UNSUPPORTED_DTYPE",
 # Every symbol include/tb.h declares.
 EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_create",
            "tb_adamw_step", "tb_adamw_plan_destroy", "tb_softmax_bwd",
-           "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd", "tb_layernorm_bwd_noalloc")
+           "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd", "tb_layernorm_bwd_noalloc",
+           "tb_softmax_bwd_causal", "tb_rmsnorm_bwd_workspace_size", "tb_rmsnorm_bwd")
 
 
 class TbError(RuntimeError):
@@ -73,6 +74,12 @@ def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.tb_layernorm_bwd.restype = i32
     lib.tb_layernorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, vp]
     lib.tb_layernorm_bwd_noalloc.restype = i32
+    lib.tb_softmax_bwd_causal.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, vp]
+    lib.tb_softmax_bwd_causal.restype = i32
+    lib.tb_rmsnorm_bwd_workspace_size.argtypes = [i64, i64, i32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.tb_rmsnorm_bwd_workspace_size.restype = i32
+    lib.tb_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp, ctypes.c_size_t, vp]
+    lib.tb_rmsnorm_bwd.restype = i32
     return lib
 
 
@@ -186,6 +193,46 @@ def tb_softmax_bwd(dY: torch.Tensor, P: torch.Tensor, dX: torch.Tensor, stream=N
     rows, cols = dY.shape
     _check("tb_softmax_bwd", lib.tb_softmax_bwd(_ptr(dY), _ptr(P), _ptr(dX), rows, cols,
                                                 _dtype(dY), _stream(stream)))
+
+
+def tb_softmax_bwd_causal(dY: torch.Tensor, P: torch.Tensor, dX: torch.Tensor, period: int,
+                          offset: int = 0, stream=None) -> None:
+    """Softmax backward reading only the causally open columns of each row:
+    row r is nonzero only on its first min(cols, r % period + 1 + offset) columns."""
+    if not (dY.shape == P.shape == dX.shape) or dY.dim() != 2:
+        raise ValueError("dY, P and dX must be [rows, cols] tensors of one shape")
+    if not (dY.dtype == P.dtype == dX.dtype):
+        raise ValueError("dY, P and dX must share a dtype")
+    rows, cols = dY.shape
+    _check("tb_softmax_bwd_causal",
+           lib.tb_softmax_bwd_causal(_ptr(dY), _ptr(P), _ptr(dX), rows, cols, int(period),
+                                     int(offset), _dtype(dY), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- RMSNorm bwd
+def tb_rmsnorm_bwd_workspace_size(rows: int, D: int, dtype: torch.dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check("tb_rmsnorm_bwd_workspace_size",
+           lib.tb_rmsnorm_bwd_workspace_size(int(rows), int(D), _DTYPE[dtype], ctypes.byref(out)))
+    return out.value
+
+
+def tb_rmsnorm_bwd(dY: torch.Tensor, x: torch.Tensor, inv_rms: torch.Tensor, gamma: torch.Tensor,
+                   dX: torch.Tensor, dgamma: torch.Tensor, workspace: Optional[torch.Tensor],
+                   stream=None) -> None:
+    if x.dim() != 2 or dY.shape != x.shape or dX.shape != x.shape:
+        raise ValueError("x, dY and dX must be [rows, D] tensors of one shape")
+    if not (dY.dtype == x.dtype == dX.dtype):
+        raise ValueError("x, dY and dX must share a dtype")
+    for t in (inv_rms, gamma, dgamma):
+        if t.dtype != torch.float32:
+            raise ValueError("inv_rms, gamma and dgamma are fp32")
+    rows, D = x.shape
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("tb_rmsnorm_bwd",
+           lib.tb_rmsnorm_bwd(_ptr(dY), _ptr(x), _ptr(inv_rms), _ptr(gamma), _ptr(dX),
+                              _ptr(dgamma), rows, D, _dtype(x), ws_ptr, ws_bytes, _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- LayerNorm bwd

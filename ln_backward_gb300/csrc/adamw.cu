@@ -14,7 +14,7 @@
 // stream).  The flat unit space is cut into tiles of 512 units dealt
 // round-robin to a persistent grid (SM count x resident CTAs), so all CTAs
 // stream through the same region of HBM at once; each CTA follows its tensor
-// with a forward scan of the table.  Every thread moves 2 units per tile with
+// with a forward scan of the table.  Every thread moves 2 units per step with
 // 128-bit evict-first loads and stores: 14 B read and 16 B written per element,
 // one HBM pass.  Tensors whose five pointers are not all 16-byte aligned, and
 // the last partial unit of a tensor, take a scalar path.
@@ -32,7 +32,7 @@ namespace {
 constexpr int kUnit = 8;        // elements per unit
 constexpr int kThreads = 256;   // threads per CTA
 constexpr int kUnroll = 2;      // units in flight per thread
-constexpr int64_t kTileUnits = (int64_t)kThreads * kUnroll;   // 4096 elements
+constexpr int64_t kTileUnits = (int64_t)kThreads * kUnroll * 4;   // 16384 elements
 constexpr uint64_t kPlanMagic = 0x7462616461707731ull;
 
 struct alignas(16) TensorEntry {

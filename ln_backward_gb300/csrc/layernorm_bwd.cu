@@ -26,6 +26,10 @@
 //    beyond the register budget use a plain-load fallback of the same
 //    structure (two passes over the row, partials kept in the workspace).
 //
+// RMSNorm backward (tb_rmsnorm_bwd) runs the same kernels with kRms set:
+//   xhat = x * inv_rms, dX = inv_rms * (dxhat - xhat * mean_D(dxhat * xhat)),
+//   dgamma_j = sum_rows dY*xhat -- the LayerNorm above without the mean and beta.
+//
 // Every mbarrier wait is bounded (about one second of %globaltimer); on expiry
 // the CTA sets the device error word, waits (bounded) for the copies it issued
 // and returns.
@@ -131,6 +135,53 @@ __device__ __forceinline__ void lds_vec(const void* p, float (&f)[Vec<Fmt>::kEle
     for (int e = 0; e < Vec<Fmt>::kElems; ++e) f[e] = Fmt::to_f32(h[e]);
 }
 
+// Warp sum of V values per lane (V a power of two <= 16) with V-1+5-log2(V)
+// shuffles instead of 5V: each of the first log2(V) butterfly levels halves the
+// values a lane carries.  Afterwards lane l holds the full sum of value
+// multi_index<V>(l); the lanes whose bits below the last split are zero hold
+// all V sums between them.
+template <int V>
+struct Log2 { static constexpr int value = V <= 1 ? 0 : 1 + Log2<V / 2>::value; };
+template <>
+struct Log2<1> { static constexpr int value = 0; };
+
+template <int V>
+__device__ __forceinline__ float warp_sum_multi(float (&v)[V], int lane) {
+    constexpr int L = Log2<V>::value;
+#pragma unroll
+    for (int lvl = 0; lvl < L; ++lvl) {
+        const int o = 16 >> lvl;
+        const int half = V >> (lvl + 1);
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 >> L; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
+template <int V>
+__device__ __forceinline__ int multi_index(int lane) {
+    constexpr int L = Log2<V>::value;
+    int idx = 0;
+#pragma unroll
+    for (int lvl = 0; lvl < L; ++lvl)
+        if (lane & (16 >> lvl)) idx += V >> (lvl + 1);
+    return idx;
+}
+
+template <int V>
+__device__ __forceinline__ bool multi_writer(int lane) {
+    constexpr int L = Log2<V>::value;
+    return L == 0 ? lane == 0 : (lane & ((32 >> L) - 1)) == 0;
+}
+
 // One 16-byte shared-memory vector as E/2 fp32 pairs (packed f32x2 math below).
 // bf16 widens exactly with a shift / mask; fp16 with the half2 conversion.
 template <class Fmt>
@@ -193,7 +244,9 @@ __device__ __forceinline__ void stg_pairs<F16>(void* p, const float2 (&f)[4]) {
 // ------------------------------------------------------------------ row kernel (bulk-copy ring)
 // A ring stage holds a group of R consecutive rows: [R rows of x | R rows of dY].
 // Columns per thread NV*E up to 16 fit two CTAs per SM; 32 need the full budget.
-template <class Fmt, int NV, int R>
+// kRms: RMSNorm backward -- no mean subtraction (mean is not read), no sum of
+// dxhat, no beta: dX = rs*(dxhat - xhat*mean(dxhat*xhat)), partial rows of D.
+template <class Fmt, int NV, int R, bool kRms>
 __global__ void __launch_bounds__(kRowThreads, (NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
 ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
                         const float* __restrict__ mean, const float* __restrict__ inv_std,
@@ -203,13 +256,16 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
     using T = typename Fmt::T;
     constexpr int E = Vec<Fmt>::kElems;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[2][R][2][kMaxWarps];
+    // Per-warp row sums: value 2i is sum(dxhat) of row i, 2i+1 is sum(dxhat*xhat).
+    // Slots of warps the CTA does not have stay zero.
+    __shared__ __align__(16) float red[2][2 * R][kMaxWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int nthreads = blockDim.x;
     const int nvec = D / E;
     const uint32_t row_bytes = (uint32_t)D * (uint32_t)sizeof(T);
     const uint32_t grp_bytes = (uint32_t)R * row_bytes;
+    for (int i = tid; i < 2 * 2 * R * kMaxWarps; i += nthreads) (&red[0][0][0])[i] = 0.f;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* ring = smem + kBarRegion;   // stage s at ring + s * 2 * grp_bytes
 
@@ -253,7 +309,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
     float mu[R], rs[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
-        mu[i] = i < nrows ? mean[r0 + i] : 0.f;
+        mu[i] = (!kRms && i < nrows) ? mean[r0 + i] : 0.f;
         rs[i] = i < nrows ? inv_std[r0 + i] : 0.f;
     }
     __syncthreads();   // barriers initialised before anyone waits on them
@@ -271,7 +327,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         for (int i = 0; i < R; ++i) {
             const int64_t rn = first + R + i;
             const bool has = rn < r1;
-            mu_n[i] = has ? mean[rn] : 0.f;
+            mu_n[i] = (!kRms && has) ? mean[rn] : 0.f;
             rs_n[i] = has ? inv_std[rn] : 0.f;
         }
         const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity);
@@ -293,9 +349,10 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
                         lds_pairs<Fmt>(st + grp_bytes + (size_t)i * row_bytes + (size_t)vi * 16, dy);
 #pragma unroll
                         for (int q = 0; q < NP; ++q) {
-                            const float2 xh = __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
+                            const float2 xh = kRms ? __fmul2_rn(xv[q], rs2)
+                                                   : __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
                             const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
-                            sa2 = __fadd2_rn(sa2, dxh);
+                            if (!kRms) sa2 = __fadd2_rn(sa2, dxh);
                             sb2 = __ffma2_rn(dxh, xh, sb2);
                         }
                     }
@@ -304,22 +361,15 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
             sa[i] = sa2.x + sa2.y;
             sb[i] = sb2.x + sb2.y;
         }
+        float sums[2 * R];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                sa[i] += __shfl_xor_sync(0xffffffffu, sa[i], o);
-                sb[i] += __shfl_xor_sync(0xffffffffu, sb[i], o);
-            }
+        for (int i = 0; i < R; ++i) {
+            sums[2 * i] = sa[i];
+            sums[2 * i + 1] = sb[i];
         }
+        const float wsum = warp_sum_multi<2 * R>(sums, lane);
         const int buf = (int)(grp & 1);
-        if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                red[buf][i][0][wid] = sa[i];
-                red[buf][i][1][wid] = sb[i];
-            }
-        }
+        if (multi_writer<2 * R>(lane)) red[buf][multi_index<2 * R>(lane)][wid] = wsum;
         // Past this barrier every thread has finished the previous group entirely,
         // so its stage can be refilled; this group's stage is still read below.
         if (__syncthreads_or(!ok)) {
@@ -337,12 +387,13 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             if (i < nr) {
-                float a = 0.f, b = 0.f;
-                for (int w = 0; w < nwarps; ++w) {
-                    a += red[buf][i][0][w];
-                    b += red[buf][i][1][w];
-                }
-                const float mean_a = a * inv_D, mean_b = b * inv_D;
+                const float4 a0 = *reinterpret_cast<const float4*>(&red[buf][2 * i][0]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&red[buf][2 * i][4]);
+                const float4 b0 = *reinterpret_cast<const float4*>(&red[buf][2 * i + 1][0]);
+                const float4 b1 = *reinterpret_cast<const float4*>(&red[buf][2 * i + 1][4]);
+                const float a = ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
+                const float b = ((b0.x + b0.y) + (b0.z + b0.w)) + ((b1.x + b1.y) + (b1.z + b1.w));
+                const float mean_a = kRms ? 0.f : a * inv_D, mean_b = b * inv_D;
                 const float2 nmu = make_float2(-mu[i], -mu[i]), rs2 = make_float2(rs[i], rs[i]);
                 const float c0 = -(rs[i] * mean_a), c1 = -(rs[i] * mean_b);
                 const float2 nc0 = make_float2(c0, c0), nc1 = make_float2(c1, c1);
@@ -356,11 +407,12 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
                         lds_pairs<Fmt>(st + grp_bytes + (size_t)i * row_bytes + (size_t)vi * 16, dy);
 #pragma unroll
                         for (int q = 0; q < NP; ++q) {
-                            const float2 xh = __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
+                            const float2 xh = kRms ? __fmul2_rn(xv[q], rs2)
+                                                   : __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
                             const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
                             out[q] = __ffma2_rn(dxh, rs2, __ffma2_rn(xh, nc1, nc0));
                             acc_g[k][q] = __ffma2_rn(dy[q], xh, acc_g[k][q]);
-                            acc_b[k][q] = __fadd2_rn(acc_b[k][q], dy[q]);
+                            if (!kRms) acc_b[k][q] = __fadd2_rn(acc_b[k][q], dy[q]);
                         }
                         stg_pairs<Fmt>(dxr + (size_t)vi * E, out);
                     }
@@ -388,7 +440,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
     // Let the column reduction launch; it waits for this grid to finish before reading.
     griddep_launch_dependents();
 
-    float* pg = partials + (size_t)blockIdx.x * 2 * D;
+    float* pg = partials + (size_t)blockIdx.x * (kRms ? 1 : 2) * D;
     float* pb = pg + D;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
@@ -398,15 +450,16 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
             for (int q = 0; q < NP; q += 2) {
                 *reinterpret_cast<float4*>(pg + vi * E + 2 * q) =
                     make_float4(acc_g[k][q].x, acc_g[k][q].y, acc_g[k][q + 1].x, acc_g[k][q + 1].y);
-                *reinterpret_cast<float4*>(pb + vi * E + 2 * q) =
-                    make_float4(acc_b[k][q].x, acc_b[k][q].y, acc_b[k][q + 1].x, acc_b[k][q + 1].y);
+                if (!kRms)
+                    *reinterpret_cast<float4*>(pb + vi * E + 2 * q) =
+                        make_float4(acc_b[k][q].x, acc_b[k][q].y, acc_b[k][q + 1].x, acc_b[k][q + 1].y);
             }
         }
     }
 }
 
 // ------------------------------------------------------------------ row kernel (plain loads)
-template <class Fmt>
+template <class Fmt, bool kRms>
 __global__ void __launch_bounds__(kRowThreads)
 ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
                          const float* __restrict__ mean, const float* __restrict__ inv_std,
@@ -415,15 +468,18 @@ ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename 
     __shared__ float red[2][2][kMaxWarps];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nwarps = blockDim.x >> 5;
-    float* pg = partials + (size_t)blockIdx.x * 2 * D;
+    float* pg = partials + (size_t)blockIdx.x * (kRms ? 1 : 2) * D;
     float* pb = pg + D;
-    for (int64_t j = tid; j < D; j += blockDim.x) { pg[j] = 0.f; pb[j] = 0.f; }
+    for (int64_t j = tid; j < D; j += blockDim.x) {
+        pg[j] = 0.f;
+        if (!kRms) pb[j] = 0.f;
+    }
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = r0 + rows_per_cta < rows ? r0 + rows_per_cta : rows;
     const float inv_D = 1.0f / (float)D;
     int buf = 0;
     for (int64_t r = r0; r < r1; ++r, buf ^= 1) {
-        const float mu = mean[r], rs = inv_std[r];
+        const float mu = kRms ? 0.f : mean[r], rs = inv_std[r];
         const int64_t off = r * D;
         float sa = 0.f, sb = 0.f;
         for (int64_t j = tid; j < D; j += blockDim.x) {
@@ -447,21 +503,22 @@ ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename 
             a += red[buf][0][w];
             b += red[buf][1][w];
         }
-        const float mean_a = a * inv_D, mean_b = b * inv_D;
+        const float mean_a = kRms ? 0.f : a * inv_D, mean_b = b * inv_D;
         for (int64_t j = tid; j < D; j += blockDim.x) {
             const float dyv = Fmt::to_f32(dY[off + j]);
             const float xh = (Fmt::to_f32(x[off + j]) - mu) * rs;
             const float dxh = __fmul_rn(dyv, gamma[j]);
             dX[off + j] = Fmt::from_f32(rs * (dxh - mean_a - xh * mean_b));
             pg[j] += dyv * xh;   // column j belongs to this thread only
-            pb[j] += dyv;
+            if (!kRms) pb[j] += dyv;
         }
     }
     griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------------ column reduction
-// partials: [G][2][D] fp32 viewed as [G][2D]; out column c < D -> dgamma, else dbeta.
+// partials: [G][W] fp32 (W = 2D for LayerNorm: dgamma then dbeta partials; W = D
+// for RMSNorm); out column c < D -> out_a (dgamma), else out_b (dbeta).
 // A CTA covers 32 columns with 32 warps: warp w sums partial rows w, w+32, ... in
 // ascending order, then the 32 warp sums are added in warp order.  The order never
 // depends on timing, so the result is bitwise reproducible.
@@ -469,27 +526,25 @@ constexpr int kColThreads = 1024;
 constexpr int kColGroups = kColThreads / 32;
 
 __global__ void __launch_bounds__(kColThreads)
-ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t D,
+ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t W, int64_t D,
                      float* __restrict__ dgamma, float* __restrict__ dbeta) {
     __shared__ float sm[kColGroups][33];
     griddep_wait();   // the row kernel (if any) has completed and flushed its partials
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t W = 2 * D;
     const int64_t c = (int64_t)blockIdx.x * 32 + lane;
     float acc = 0.f;
     if (c < W) {
-        int b = w;
-        for (; b + 3 * kColGroups < G; b += 4 * kColGroups) {
-            const float v0 = partials[(int64_t)b * W + c];
-            const float v1 = partials[(int64_t)(b + kColGroups) * W + c];
-            const float v2 = partials[(int64_t)(b + 2 * kColGroups) * W + c];
-            const float v3 = partials[(int64_t)(b + 3 * kColGroups) * W + c];
-            acc += v0;
-            acc += v1;
-            acc += v2;
-            acc += v3;
+        // eight loads in flight per round, added in ascending row order
+        for (int b = w; b < G; b += 8 * kColGroups) {
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int bb = b + q * kColGroups;
+                v[q] = bb < G ? partials[(int64_t)bb * W + c] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc += v[q];
         }
-        for (; b < G; b += kColGroups) acc += partials[(int64_t)b * W + c];
     }
     sm[w][lane] = acc;
     __syncthreads();
@@ -503,10 +558,10 @@ ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t D,
 
 // Launch the column reduction so that it may be scheduled while the row kernel
 // drains (programmatic dependent launch); it waits inside for the row kernel.
-cudaError_t launch_colsum(const float* ws, int G, int64_t D, float* dgamma, float* dbeta,
-                          cudaStream_t st) {
+cudaError_t launch_colsum(const float* ws, int G, int64_t W, int64_t D, float* dgamma,
+                          float* dbeta, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((2 * D + 31) / 32));
+    cfg.gridDim = dim3((unsigned)((W + 31) / 32));
     cfg.blockDim = dim3(kColThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -515,7 +570,7 @@ cudaError_t launch_colsum(const float* ws, int G, int64_t D, float* dgamma, floa
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ln_bwd_colsum_kernel, ws, G, D, dgamma, dbeta);
+    return cudaLaunchKernelEx(&cfg, ln_bwd_colsum_kernel, ws, G, W, D, dgamma, dbeta);
 }
 
 // ------------------------------------------------------------------ launch planning
@@ -556,37 +611,47 @@ auto with_ring_variant(int nv, int r, Args&&... args) {
     return Op<Fmt, max_nv<Fmt>(), 1>::run(args...);
 }
 
-template <class Fmt, int NV, int R>
-struct RingPtr {
-    static const void* run() {
-        return reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, NV, R>);
-    }
+template <bool kRms>
+struct RingOps {
+    template <class Fmt, int NV, int R>
+    struct Ptr {
+        static const void* run() {
+            return reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, NV, R, kRms>);
+        }
+    };
 };
 
 template <class Fmt>
-const void* ring_kernel_for(int nv, int r) {
-    return with_ring_variant<Fmt, RingPtr>(nv, r);
+const void* ring_kernel_for(int nv, int r, bool rms) {
+    return rms ? with_ring_variant<Fmt, RingOps<true>::template Ptr>(nv, r)
+               : with_ring_variant<Fmt, RingOps<false>::template Ptr>(nv, r);
 }
 
-const void* ring_kernel(tb_dtype dt, int nv, int r) {
+const void* ring_kernel(tb_dtype dt, int nv, int r, bool rms) {
     switch (dt) {
-        case TB_F32: return ring_kernel_for<F32>(nv, r);
-        case TB_BF16: return ring_kernel_for<BF16>(nv, r);
-        default: return ring_kernel_for<F16>(nv, r);
+        case TB_F32: return ring_kernel_for<F32>(nv, r, rms);
+        case TB_BF16: return ring_kernel_for<BF16>(nv, r, rms);
+        default: return ring_kernel_for<F16>(nv, r, rms);
     }
 }
 
-const void* plain_kernel(tb_dtype dt) {
+template <class Fmt>
+const void* plain_kernel_for(bool rms) {
+    return rms ? reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<Fmt, true>)
+               : reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<Fmt, false>);
+}
+
+const void* plain_kernel(tb_dtype dt, bool rms) {
     switch (dt) {
-        case TB_F32: return reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<F32>);
-        case TB_BF16: return reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<BF16>);
-        default: return reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<F16>);
+        case TB_F32: return plain_kernel_for<F32>(rms);
+        case TB_BF16: return plain_kernel_for<BF16>(rms);
+        default: return plain_kernel_for<F16>(rms);
     }
 }
 
 // `aligned`: every row buffer 16-byte aligned (the caller checks pointers).
 bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceInfo& info,
-               LnPlan* p) {
+               LnPlan* p, bool rms = false) {
     const int64_t es = (int64_t)dtype_size(dt);
     const int64_t E = 16 / es;
     const int64_t row_bytes = D * es;
@@ -606,7 +671,7 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
             (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
         const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
         if ((int64_t)smem <= info.max_smem_optin) {
-            const void* k = ring_kernel(dt, nv, r);
+            const void* k = ring_kernel(dt, nv, r, rms);
             if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
                 cudaSuccess)
                 return false;
@@ -624,7 +689,7 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
     }
     if (p->path == Path::kPlain) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plain_kernel(dt), kRowThreads, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plain_kernel(dt, rms), kRowThreads, 0) !=
             cudaSuccess)
             return false;
         p->threads = kRowThreads;
@@ -639,36 +704,46 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
     return true;
 }
 
-size_t workspace_bytes_for(const LnPlan& p, int64_t D) {
-    return (size_t)p.grid * 2 * (size_t)D * sizeof(float);
+size_t workspace_bytes_for(const LnPlan& p, int64_t D, bool rms = false) {
+    return (size_t)p.grid * (rms ? 1 : 2) * (size_t)D * sizeof(float);
 }
 
-template <class Fmt, int NV, int R>
-struct RingLaunch {
-    using T = typename Fmt::T;
-    static int run(const LnPlan& p, const T* dy, const T* x, const float* mean, const float* inv_std,
-                   const float* gamma, T* dx, float* ws, int64_t rows, int D, int* err,
-                   cudaStream_t st) {
-        ln_bwd_rows_ring_kernel<Fmt, NV, R><<<p.grid, p.threads, p.smem, st>>>(
-            dy, x, mean, inv_std, gamma, dx, ws, rows, D, p.stages, p.rows_per_cta, err);
-        return 0;
-    }
+template <bool kRms>
+struct RingLaunchOps {
+    template <class Fmt, int NV, int R>
+    struct Launch {
+        using T = typename Fmt::T;
+        static int run(const LnPlan& p, const T* dy, const T* x, const float* mean,
+                       const float* inv_std, const float* gamma, T* dx, float* ws, int64_t rows,
+                       int D, int* err, cudaStream_t st) {
+            ln_bwd_rows_ring_kernel<Fmt, NV, R, kRms><<<p.grid, p.threads, p.smem, st>>>(
+                dy, x, mean, inv_std, gamma, dx, ws, rows, D, p.stages, p.rows_per_cta, err);
+            return 0;
+        }
+    };
 };
 
 template <class Fmt>
 void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* mean,
                  const float* inv_std, const float* gamma, void* dX, float* ws, int64_t rows,
-                 int64_t D, int* err, cudaStream_t st) {
+                 int64_t D, int* err, cudaStream_t st, bool rms = false) {
     using T = typename Fmt::T;
     const T* dy = static_cast<const T*>(dY);
     const T* xx = static_cast<const T*>(x);
     T* dx = static_cast<T*>(dX);
     if (p.path == Path::kRing) {
-        with_ring_variant<Fmt, RingLaunch>(p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws,
-                                            rows, (int)D, err, st);
+        if (rms)
+            with_ring_variant<Fmt, RingLaunchOps<true>::template Launch>(
+                p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
+        else
+            with_ring_variant<Fmt, RingLaunchOps<false>::template Launch>(
+                p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
+    } else if (rms) {
+        ln_bwd_rows_plain_kernel<Fmt, true><<<p.grid, p.threads, 0, st>>>(
+            dy, xx, mean, inv_std, gamma, dx, ws, rows, D, p.rows_per_cta);
     } else {
-        ln_bwd_rows_plain_kernel<Fmt><<<p.grid, p.threads, 0, st>>>(dy, xx, mean, inv_std, gamma, dx,
-                                                                   ws, rows, D, p.rows_per_cta);
+        ln_bwd_rows_plain_kernel<Fmt, false><<<p.grid, p.threads, 0, st>>>(
+            dy, xx, mean, inv_std, gamma, dx, ws, rows, D, p.rows_per_cta);
     }
 }
 
@@ -730,7 +805,7 @@ extern "C" tb_status tb_layernorm_bwd(const void* dY, const void* x, const float
     if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (rows == 0)
-        return launch_colsum(nullptr, 0, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+        return launch_colsum(nullptr, 0, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
     const bool aligned = aligned_to(dY, 16) && aligned_to(x, 16) && aligned_to(dX, 16) &&
                          aligned_to(gamma, 16) && aligned_to(workspace, 16);
     LnPlan p;
@@ -746,7 +821,7 @@ extern "C" tb_status tb_layernorm_bwd(const void* dY, const void* x, const float
         default: launch_rows<F16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
     }
     if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
-    return launch_colsum(ws, p.grid, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+    return launch_colsum(ws, p.grid, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ entry point without allocation
@@ -813,7 +888,7 @@ extern "C" tb_status tb_layernorm_bwd_noalloc(const void* dY, const void* x, con
     if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (rows == 0)
-        return launch_colsum(nullptr, 0, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+        return launch_colsum(nullptr, 0, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
     float* ws = noalloc_scratch(dev);
     int* err = device_error_word();
     if (!ws || !err) return TB_ERR_CUDA;
@@ -834,5 +909,76 @@ extern "C" tb_status tb_layernorm_bwd_noalloc(const void* dY, const void* x, con
         default: launch_rows<F16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
     }
     if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
-    return launch_colsum(ws, p.grid, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+    return launch_colsum(ws, p.grid, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ RMSNorm backward
+extern "C" tb_status tb_rmsnorm_bwd_workspace_size(int64_t rows, int64_t D, tb_dtype io_dtype,
+                                                   size_t* bytes) {
+    using namespace tb;
+    if (!bytes || rows < 0 || D < 0) return TB_ERR_INVALID_VALUE;
+    if (!dtype_valid(io_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
+    *bytes = 0;
+    if (rows == 0 || D == 0) return TB_OK;
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    LnPlan p, q;
+    if (!make_plan(rows, D, io_dtype, true, info, &p, true)) return TB_ERR_CUDA;
+    if (!make_plan(rows, D, io_dtype, false, info, &q, true)) return TB_ERR_CUDA;
+    *bytes = std::max(workspace_bytes_for(p, D, true), workspace_bytes_for(q, D, true));
+    return TB_OK;
+}
+
+extern "C" tb_status tb_rmsnorm_bwd(const void* dY, const void* x, const float* inv_rms,
+                                    const float* gamma, void* dX, float* dgamma, int64_t rows,
+                                    int64_t D, tb_dtype io_dtype, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    using namespace tb;
+    if (rows < 0 || D < 0) return TB_ERR_INVALID_VALUE;
+    if (!dtype_valid(io_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (D == 0) return TB_OK;
+    if (D > (int64_t)1 << 30) return TB_ERR_INVALID_VALUE;
+    if (!dgamma || !gamma) return TB_ERR_INVALID_VALUE;
+    if (rows > 0 && (!dY || !x || !inv_rms || !dX)) return TB_ERR_INVALID_VALUE;
+    if (rows > 0 && D > INT64_MAX / rows / 4) return TB_ERR_INVALID_VALUE;
+    const size_t es = dtype_size(io_dtype);
+    if (!aligned_to(dgamma, 4) || !aligned_to(gamma, 4)) return TB_ERR_MISALIGNED;
+    if (rows > 0 && (!aligned_to(dY, es) || !aligned_to(x, es) || !aligned_to(dX, es) ||
+                     !aligned_to(inv_rms, 4)))
+        return TB_ERR_MISALIGNED;
+    const int64_t n = rows * D;
+    const Range ins[4] = {range_of(dY, n, es), range_of(x, n, es), range_of(inv_rms, rows, 4),
+                          range_of(gamma, D, 4)};
+    const Range outs[3] = {range_of(dX, n, es), range_of(dgamma, D, 4),
+                           range_of(workspace, (int64_t)workspace_bytes, 1)};
+    for (const Range& o : outs)
+        for (const Range& in : ins)
+            if (overlap(o, in)) return TB_ERR_ALIAS;
+    for (int a = 0; a < 3; ++a)
+        for (int b = a + 1; b < 3; ++b)
+            if (overlap(outs[a], outs[b])) return TB_ERR_ALIAS;
+
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (rows == 0)
+        return launch_colsum(nullptr, 0, D, D, dgamma, nullptr, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+    const bool aligned = aligned_to(dY, 16) && aligned_to(x, 16) && aligned_to(dX, 16) &&
+                         aligned_to(gamma, 16) && aligned_to(workspace, 16);
+    LnPlan p;
+    if (!make_plan(rows, D, io_dtype, aligned, info, &p, true)) return TB_ERR_CUDA;
+    if (!workspace || workspace_bytes < workspace_bytes_for(p, D, true)) return TB_ERR_WORKSPACE;
+    if (!aligned_to(workspace, 4)) return TB_ERR_MISALIGNED;
+    int* err = device_error_word();
+    if (!err) return TB_ERR_CUDA;
+    float* ws = static_cast<float*>(workspace);
+    switch (io_dtype) {
+        case TB_F32: launch_rows<F32>(p, dY, x, nullptr, inv_rms, gamma, dX, ws, rows, D, err, st, true); break;
+        case TB_BF16: launch_rows<BF16>(p, dY, x, nullptr, inv_rms, gamma, dX, ws, rows, D, err, st, true); break;
+        default: launch_rows<F16>(p, dY, x, nullptr, inv_rms, gamma, dX, ws, rows, D, err, st, true); break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
+    return launch_colsum(ws, p.grid, D, D, dgamma, nullptr, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }

@@ -14,6 +14,12 @@
 //   group : rows of <= 256 vectors (1024 fp32 / 2048 16-bit), G lanes per row
 //   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
+//
+// Causal variant (tb_softmax_bwd_causal): row r of an attention block can only be
+// nonzero on its first min(cols, r mod period + 1 + offset) columns (the forward
+// masked the rest, so P is exactly 0 there).  The kernels then read only the
+// vectors that hold an unmasked column and write +0 to the others, which cuts the
+// HBM reads of a square causal block roughly in half.
 #include <algorithm>
 
 #include "tb_common.cuh"
@@ -39,10 +45,21 @@ __device__ __forceinline__ uint4 vec_from(const float (&f)[Vec<Fmt>::kElems]) {
 
 // ------------------------------------------------------------------ group path
 // G lanes per row (G divides 32), VPL vectors per lane; 256 threads per CTA.
+// Number of leading columns of row r that can be nonzero: all of them for a dense
+// matrix (period == 0); min(cols, r mod period + 1 + offset) under a causal mask.
+__device__ __forceinline__ int64_t valid_cols(int64_t r, int64_t cols, int64_t period,
+                                              int64_t offset) {
+    if (period <= 0) return cols;
+    const int64_t v = r % period + 1 + offset;
+    return v < cols ? v : cols;
+}
+
+// Up to 4 staged vectors per input per lane (8 for fp32) three CTAs fit per SM.
 template <class Fmt, int G, int VPL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, (VPL <= 4 || sizeof(typename Fmt::T) == 4) ? 3 : 2)
 softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
-                         uint4* __restrict__ dX, int64_t rows, int nv) {
+                         uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
+                         int64_t offset) {
     constexpr int E = Vec<Fmt>::kElems;
     constexpr int kRowsPerWarp = 32 / G;
     const int lane = threadIdx.x & 31;
@@ -54,11 +71,13 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
         const int64_t row = r0 + sub;
         const bool live = row < rows;
         const int64_t off = row * (int64_t)nv;
+        // vectors holding at least one unmasked column; the rest are never read
+        const int nvv = (int)((valid_cols(row, (int64_t)nv * E, period, offset) + E - 1) / E);
         uint4 p[VPL], d[VPL];
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int vi = gl + k * G;
-            if (live && vi < nv) {
+            if (live && vi < nvv) {
                 p[k] = __ldcs(P + off + vi);
                 d[k] = __ldcs(dY + off + vi);
             } else {
@@ -76,12 +95,14 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int vi = gl + k * G;
-            if (live && vi < nv) {
+            if (live && vi < nvv) {
                 float out[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e)
                     out[e] = vec_elem<Fmt>(p[k], e) * (vec_elem<Fmt>(d[k], e) - dot);
                 __stcs(dX + off + vi, vec_from<Fmt>(out));
+            } else if (live && vi < nv) {
+                __stcs(dX + off + vi, make_uint4(0u, 0u, 0u, 0u));   // masked: dX = +0
             }
         }
     }
@@ -93,7 +114,8 @@ constexpr int kCtaThreads = 512;
 template <class Fmt, int VPL>
 __global__ void __launch_bounds__(kCtaThreads)
 softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
-                       uint4* __restrict__ dX, int64_t rows, int nv) {
+                       uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
+                       int64_t offset) {
     constexpr int E = Vec<Fmt>::kElems;
     constexpr int kWarps = kCtaThreads / 32;
     __shared__ float red[2][kWarps];
@@ -101,11 +123,12 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
     int parity = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
         const int64_t off = row * (int64_t)nv;
+        const int nvv = (int)((valid_cols(row, (int64_t)nv * E, period, offset) + E - 1) / E);
         uint4 p[VPL], d[VPL];
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int vi = tid + k * kCtaThreads;
-            if (vi < nv) {
+            if (vi < nvv) {
                 p[k] = __ldcs(P + off + vi);
                 d[k] = __ldcs(dY + off + vi);
             } else {
@@ -128,12 +151,14 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int vi = tid + k * kCtaThreads;
-            if (vi < nv) {
+            if (vi < nvv) {
                 float out[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e)
                     out[e] = vec_elem<Fmt>(p[k], e) * (vec_elem<Fmt>(d[k], e) - dot);
                 __stcs(dX + off + vi, vec_from<Fmt>(out));
+            } else if (vi < nv) {
+                __stcs(dX + off + vi, make_uint4(0u, 0u, 0u, 0u));
             }
         }
     }
@@ -146,15 +171,17 @@ template <class Fmt>
 __global__ void __launch_bounds__(kTwoPassThreads)
 softmax_bwd_twopass_kernel(const typename Fmt::T* __restrict__ dY,
                            const typename Fmt::T* __restrict__ P,
-                           typename Fmt::T* __restrict__ dX, int64_t rows, int64_t cols) {
+                           typename Fmt::T* __restrict__ dX, int64_t rows, int64_t cols,
+                           int64_t period, int64_t offset) {
     constexpr int kWarps = kTwoPassThreads / 32;
     __shared__ float red[2][kWarps];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int parity = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
         const int64_t off = row * cols;
+        const int64_t nvalid = valid_cols(row, cols, period, offset);
         float dot = 0.f;
-        for (int64_t j = tid; j < cols; j += kTwoPassThreads)
+        for (int64_t j = tid; j < nvalid; j += kTwoPassThreads)
             dot += Fmt::to_f32(P[off + j]) * Fmt::to_f32(dY[off + j]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
@@ -164,8 +191,12 @@ softmax_bwd_twopass_kernel(const typename Fmt::T* __restrict__ dY,
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) dot += red[parity][w];
         for (int64_t j = tid; j < cols; j += kTwoPassThreads) {
-            const float p = Fmt::to_f32(P[off + j]);
-            dX[off + j] = Fmt::from_f32(p * (Fmt::to_f32(dY[off + j]) - dot));
+            if (j < nvalid) {
+                const float p = Fmt::to_f32(P[off + j]);
+                dX[off + j] = Fmt::from_f32(p * (Fmt::to_f32(dY[off + j]) - dot));
+            } else {
+                dX[off + j] = Fmt::from_f32(0.0f);
+            }
         }
     }
 }
@@ -173,7 +204,7 @@ softmax_bwd_twopass_kernel(const typename Fmt::T* __restrict__ dY,
 // ------------------------------------------------------------------ dispatch
 template <class Fmt, int G, int VPL>
 tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, int nv,
-                       int sms, cudaStream_t st) {
+                       int64_t period, int64_t offset, int sms, cudaStream_t st) {
     constexpr int kRowsPerCta = 256 / G;
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(
@@ -181,38 +212,39 @@ tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, in
     const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1)));
     softmax_bwd_group_kernel<Fmt, G, VPL><<<(unsigned)grid, 256, 0, st>>>(
-        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv);
+        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv, period, offset);
     return launch_status();
 }
 
 template <class Fmt, int VPL>
-tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int nv, int sms,
-                     cudaStream_t st) {
+tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int nv,
+                     int64_t period, int64_t offset, int sms, cudaStream_t st) {
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, VPL>), kCtaThreads, 0);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * std::max(per_sm, 1)));
     softmax_bwd_cta_kernel<Fmt, VPL><<<(unsigned)grid, kCtaThreads, 0, st>>>(
-        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv);
+        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv,
+        period, offset);
     return launch_status();
 }
 
 template <class Fmt>
 tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_t cols,
-                   bool aligned, int sms, cudaStream_t st) {
+                   int64_t period, int64_t offset, bool aligned, int sms, cudaStream_t st) {
     constexpr int E = Vec<Fmt>::kElems;
     if (aligned && cols % E == 0 && cols / E <= 2048) {
         const int nv = (int)(cols / E);
-        if (nv <= 4) return launch_group<Fmt, 4, 1>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 8) return launch_group<Fmt, 8, 1>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 16) return launch_group<Fmt, 16, 1>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 32) return launch_group<Fmt, 32, 1>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 64) return launch_group<Fmt, 32, 2>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 128) return launch_group<Fmt, 32, 4>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 256) return launch_group<Fmt, 32, 8>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 512) return launch_cta<Fmt, 1>(dY, P, dX, rows, nv, sms, st);
-        if (nv <= 1024) return launch_cta<Fmt, 2>(dY, P, dX, rows, nv, sms, st);
-        return launch_cta<Fmt, 4>(dY, P, dX, rows, nv, sms, st);
+        if (nv <= 4) return launch_group<Fmt, 4, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 8) return launch_group<Fmt, 8, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 16) return launch_group<Fmt, 16, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 32) return launch_group<Fmt, 32, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 64) return launch_group<Fmt, 32, 2>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 128) return launch_group<Fmt, 32, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 256) return launch_group<Fmt, 32, 8>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 512) return launch_cta<Fmt, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 1024) return launch_cta<Fmt, 2>(dY, P, dX, rows, nv, period, offset, sms, st);
+        return launch_cta<Fmt, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
     }
     using T = typename Fmt::T;
     int per_sm = 0;
@@ -220,17 +252,19 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
         &per_sm, reinterpret_cast<const void*>(&softmax_bwd_twopass_kernel<Fmt>), kTwoPassThreads, 0);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * std::max(per_sm, 1)));
     softmax_bwd_twopass_kernel<Fmt><<<(unsigned)grid, kTwoPassThreads, 0, st>>>(
-        static_cast<const T*>(dY), static_cast<const T*>(P), static_cast<T*>(dX), rows, cols);
+        static_cast<const T*>(dY), static_cast<const T*>(P), static_cast<T*>(dX), rows, cols, period,
+        offset);
     return launch_status();
 }
 
 }  // namespace
 }  // namespace tb
 
-extern "C" tb_status tb_softmax_bwd(const void* dY, const void* P, void* dX, int64_t rows,
-                                    int64_t cols, tb_dtype dtype, void* stream) {
-    using namespace tb;
-    if (rows < 0 || cols < 0) return TB_ERR_INVALID_VALUE;
+namespace tb {
+namespace {
+tb_status softmax_bwd_entry(const void* dY, const void* P, void* dX, int64_t rows, int64_t cols,
+                            int64_t period, int64_t offset, tb_dtype dtype, void* stream) {
+    if (rows < 0 || cols < 0 || period < 0 || offset < 0) return TB_ERR_INVALID_VALUE;
     if (!dtype_valid(dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
     if (rows == 0 || cols == 0) return TB_OK;
     if (!dY || !P || !dX) return TB_ERR_INVALID_VALUE;
@@ -247,8 +281,22 @@ extern "C" tb_status tb_softmax_bwd(const void* dY, const void* P, void* dX, int
                          (cols * (int64_t)es) % 16 == 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
-        case TB_F32: return dispatch<F32>(dY, P, dX, rows, cols, aligned, info.sm_count, st);
-        case TB_BF16: return dispatch<BF16>(dY, P, dX, rows, cols, aligned, info.sm_count, st);
-        default: return dispatch<F16>(dY, P, dX, rows, cols, aligned, info.sm_count, st);
+        case TB_F32: return dispatch<F32>(dY, P, dX, rows, cols, period, offset, aligned, info.sm_count, st);
+        case TB_BF16: return dispatch<BF16>(dY, P, dX, rows, cols, period, offset, aligned, info.sm_count, st);
+        default: return dispatch<F16>(dY, P, dX, rows, cols, period, offset, aligned, info.sm_count, st);
     }
+}
+}  // namespace
+}  // namespace tb
+
+extern "C" tb_status tb_softmax_bwd(const void* dY, const void* P, void* dX, int64_t rows,
+                                    int64_t cols, tb_dtype dtype, void* stream) {
+    return tb::softmax_bwd_entry(dY, P, dX, rows, cols, 0, 0, dtype, stream);
+}
+
+extern "C" tb_status tb_softmax_bwd_causal(const void* dY, const void* P, void* dX, int64_t rows,
+                                           int64_t cols, int64_t period, int64_t offset,
+                                           tb_dtype dtype, void* stream) {
+    if (period < 1) return TB_ERR_INVALID_VALUE;
+    return tb::softmax_bwd_entry(dY, P, dX, rows, cols, period, offset, dtype, stream);
 }

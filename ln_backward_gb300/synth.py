@@ -13,8 +13,10 @@ large inputs are drawn on the device, small ones on the host.  Value recipes:
   loss_scale rounded to the 16-bit gradient dtype (sigma is a standard
   deviation), a fresh draw for every (seed, step).
 * Softmax backward: P = row softmax of N(0,1) logits computed in float64 and
-  rounded to the I/O dtype; with ``causal_period=S`` row r only sees columns
-  j <= r mod S and the masked entries are exactly 0; dY ~ N(0,1).
+  rounded to the I/O dtype; with ``causal_period=S`` (and ``causal_offset=o``)
+  row r only sees columns j <= r mod S + o and the masked entries are exactly
+  0; dY ~ N(0,1).
+* RMSNorm backward: as LayerNorm, with inv_rms = 1/sqrt(mean(x^2) + eps).
 * LayerNorm backward: x ~ N(0,1) and dY ~ N(0, dy_std) in the I/O dtype,
   gamma ~ N(1, 0.1) fp32, and the forward's saved mean and inv_std =
   1/sqrt(var + eps) (biased variance) computed in float64 from the stored x
@@ -152,8 +154,11 @@ def fill_grads(st: AdamWState, step: int, chunk: int = 1 << 27) -> None:
 
 # ----------------------------------------------------------------------------- softmax bwd
 def softmax_inputs(rows: int, cols: int, dtype, seed: int, device,
-                   causal_period: int | None = None, chunk_rows: int = 8192):
-    """Returns ``(P, dY)`` as row-major [rows, cols] tensors of ``dtype``."""
+                   causal_period: int | None = None, causal_offset: int = 0,
+                   chunk_rows: int = 8192):
+    """Returns ``(P, dY)`` as row-major [rows, cols] tensors of ``dtype``.  With
+    ``causal_period`` row r is open on its first min(cols, r % period + 1 + offset)
+    columns and P is exactly 0 on the rest."""
     dev = torch.device(device)
     g = _gen(dev, seed, 2)
     P = torch.empty(rows, cols, dtype=dtype, device=dev)
@@ -164,7 +169,7 @@ def softmax_inputs(rows: int, cols: int, dtype, seed: int, device,
         z = torch.randn(k, cols, generator=g, device=dev, dtype=torch.float64)
         if causal_period:
             q = (torch.arange(r0, r0 + k, device=dev) % causal_period).unsqueeze(1)
-            z = z.masked_fill(col.unsqueeze(0) > q, float("-inf"))
+            z = z.masked_fill(col.unsqueeze(0) > q + causal_offset, float("-inf"))
         z = z - z.max(dim=1, keepdim=True).values
         e = torch.exp(z)
         P[r0:r0 + k] = (e / e.sum(dim=1, keepdim=True)).to(dtype)
@@ -197,3 +202,26 @@ def layernorm_inputs(rows: int, D: int, dtype, seed: int, device, eps: float = 1
         dY[r0:r0 + k] = (dy_std * torch.randn(k, D, generator=g, device=dev,
                                               dtype=torch.float32)).to(dtype)
     return x, dY, mean, inv_std, gamma
+
+
+# ----------------------------------------------------------------------------- RMSNorm bwd
+def rmsnorm_inputs(rows: int, D: int, dtype, seed: int, device, eps: float = 1e-5,
+                   dy_std: float = 1.0, chunk_rows: int = 4096):
+    """Returns ``(x, dY, inv_rms, gamma)``; x, dY in ``dtype``; inv_rms = 1/sqrt(mean(x^2)+eps)
+    from the stored x in float64, rounded to fp32; gamma ~ N(1, 0.1) fp32."""
+    dev = torch.device(device)
+    g = _gen(dev, seed, 4)
+    x = torch.empty(rows, D, dtype=dtype, device=dev)
+    dY = torch.empty(rows, D, dtype=dtype, device=dev)
+    inv_rms = torch.empty(rows, dtype=torch.float32, device=dev)
+    gamma = (1.0 + 0.1 * torch.randn(D, generator=g, device=dev,
+                                     dtype=torch.float32)).contiguous()
+    for r0 in range(0, rows, chunk_rows):
+        k = min(chunk_rows, rows - r0)
+        xs = torch.randn(k, D, generator=g, device=dev, dtype=torch.float32).to(dtype)
+        x[r0:r0 + k] = xs
+        xd = xs.to(torch.float64)
+        inv_rms[r0:r0 + k] = (1.0 / torch.sqrt((xd * xd).mean(dim=1) + eps)).to(torch.float32)
+        dY[r0:r0 + k] = (dy_std * torch.randn(k, D, generator=g, device=dev,
+                                              dtype=torch.float32)).to(dtype)
+    return x, dY, inv_rms, gamma

@@ -6,7 +6,9 @@ outputs that cancel far below their terms, within the fp32 arithmetic's own
 error bound -- see tests/tolerance.py).  Covers the tiny config (1024 x 128
 fp32, every element), the attention config (98,304 x 1,024 causal, fp32 and
 bf16, every element), a sweep of row lengths across every kernel path with a
-ragged row count, unaligned buffers (two-pass path) and empty inputs.
+ragged row count, unaligned buffers (two-pass path) and empty inputs, and the
+causal variant (reads only the open columns) on the attention config and on
+shapes that exercise every path with row offsets and wrap-around periods.
 """
 import numpy as np
 import pytest
@@ -128,3 +130,39 @@ def test_deterministic(tb, synth):
     tb.tb_softmax_bwd(dY, P, b)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------------------- causal variant
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_causal_variant_attention_config(tb, synth, dtype):
+    """tb_softmax_bwd_causal on the 98,304 x 1,024 causal block stack: same values as the
+    oracle (and as the dense kernel), every element."""
+    rows, cols = 8 * 12 * 1024, 1024
+    P, dY = synth.softmax_inputs(rows, cols, dtype, seed=5, device="cuda", causal_period=1024)
+    dX = torch.full_like(P, float("nan"))
+    tb.tb_softmax_bwd_causal(dY, P, dX, period=1024)
+    dense = torch.empty_like(P)
+    tb.tb_softmax_bwd(dY, P, dense)
+    torch.cuda.synchronize()
+    assert torch.equal(dX, dense)          # +0 == -0 under torch.equal's value comparison
+    for r0 in range(0, rows, 24576):
+        check(dX[r0:r0 + 24576], P[r0:r0 + 24576], dY[r0:r0 + 24576])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
+                         ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("rows, cols, period, offset", [
+    (300, 128, 128, 0), (300, 1024, 256, 768), (77, 1000, 1000, 0), (64, 33, 33, 0),
+    (129, 4096, 4096, 0), (50, 20000, 20000, 0), (40, 2048, 16, 5), (10, 512, 4, 600)])
+def test_causal_variant_shapes(tb, synth, rows, cols, period, offset, dtype):
+    P, dY = synth.softmax_inputs(rows, cols, dtype, seed=rows + cols, device="cuda",
+                                 causal_period=period, causal_offset=offset)
+    dX = torch.full_like(P, float("nan"))
+    tb.tb_softmax_bwd_causal(dY, P, dX, period=period, offset=offset)
+    check(dX, P, dY)
+
+
+def test_causal_variant_rejects_bad_period(tb, synth):
+    P, dY = synth.softmax_inputs(8, 64, torch.float32, seed=3, device="cuda")
+    with pytest.raises(tb.TbError):
+        tb.tb_softmax_bwd_causal(dY, P, torch.empty_like(P), period=0)
