@@ -64,6 +64,12 @@ def _configure(lib):
     for name in ("orc_layernorm_bwd_f64", "orc_layernorm_bwd_f32"):
         getattr(lib, name).argtypes = [i64, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.orc_rmsnorm_bwd_f64.argtypes = [i64, i64, vp, vp, vp, vp, vp, vp]
+    lib.orc_grad_sumsq_f64.argtypes = [i64, vp, i32, f64, ctypes.POINTER(i32)]
+    lib.orc_grad_sumsq_f64.restype = f64
+    lib.orc_clip_factor.argtypes = [f64, f64]
+    lib.orc_clip_factor.restype = f64
+    lib.orc_adamw_step_clipped_f64.argtypes = [i64, vp, vp, vp, vp, i32, f64, f64, i32, i64,
+                                               f32, f32, f32, f32, f32, vp, i32, vp]
     return lib
 
 
@@ -166,6 +172,40 @@ def adamw_step_f32(theta, m, v, grad_bits, grad_kind, inv_loss_scale, t,
                                KIND[grad_kind], float(inv_loss_scale), int(t),
                                lr, beta1, beta2, eps, weight_decay,
                                _ptr(copy), KIND[copy_kind], _ptr(gout))
+    return copy, gout
+
+
+# --------------------------------------------------------------------------- grad-norm clipping
+def grad_norm_f64(grad_bits_list, kind, inv_loss_scale):
+    """Global L2 norm of the unscaled gradients of several tensors, and whether any
+    element is non-finite.  Returns ``(norm, nonfinite)``."""
+    flag = ctypes.c_int(0)
+    total = 0.0
+    for gb in grad_bits_list:
+        g = _c(gb, np.uint16)
+        total += _load().orc_grad_sumsq_f64(g.size, _ptr(g), KIND[kind], float(inv_loss_scale),
+                                            ctypes.byref(flag))
+    return float(np.sqrt(total)), bool(flag.value)
+
+
+def clip_factor(norm, max_norm) -> float:
+    return _load().orc_clip_factor(float(norm), float(max_norm))
+
+
+def adamw_step_clipped_f64(theta, m, v, grad_bits, grad_kind, inv_loss_scale, clip, skip, t,
+                           lr, beta1, beta2, eps, weight_decay, copy_kind="bf16"):
+    """AdamW step on the clipped gradient (see oracle.c); same conventions as
+    ``adamw_step_f64``."""
+    for a in (theta, m, v):
+        assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"]
+    g = _c(grad_bits, np.uint16)
+    n = theta.size
+    copy = np.empty(n, np.uint16)
+    gout = np.empty(n, np.uint16)
+    _load().orc_adamw_step_clipped_f64(n, _ptr(theta), _ptr(m), _ptr(v), _ptr(g),
+                                       KIND[grad_kind], float(inv_loss_scale), float(clip),
+                                       int(bool(skip)), int(t), lr, beta1, beta2, eps,
+                                       weight_decay, _ptr(copy), KIND[copy_kind], _ptr(gout))
     return copy, gout
 
 

@@ -361,3 +361,65 @@ void orc_rmsnorm_bwd_f64(int64_t rows, int64_t D,
         }
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Global gradient-norm clipping with a non-finite flag                       */
+/*   [GPU-Opt-P2] §"完整训练循环（整合一切）" step 7: the L2 norm of the       */
+/*   unscaled gradient over all parameters, then the gradients are scaled by  */
+/*   max_norm / norm when norm > max_norm, before the AdamW step.             */
+/* ------------------------------------------------------------------------- */
+
+/* Sum of squares of the unscaled gradient over n elements, in double; sets
+ * *nonfinite to 1 when any element is NaN or infinite (it is left unchanged
+ * otherwise, so several tensors can share one flag). */
+double orc_grad_sumsq_f64(int64_t n, const uint16_t* grad, int kind, double inv_loss_scale,
+                          int* nonfinite)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double g = orc_decode16(grad[i], kind);
+        if (!isfinite(g)) *nonfinite = 1;
+        g *= inv_loss_scale;
+        s += g * g;
+    }
+    return s;
+}
+
+/* The factor the gradients are multiplied by: max_norm / norm when the norm
+ * exceeds max_norm, else 1 (max_norm <= 0 disables clipping). */
+double orc_clip_factor(double norm, double max_norm)
+{
+    if (max_norm > 0.0 && norm > max_norm) return max_norm / norm;
+    return 1.0;
+}
+
+/*
+ * One AdamW step on the clipped gradient g = (float(grad) * inv_loss_scale) * clip,
+ * in double; otherwise identical to orc_adamw_step_f64.  With skip != 0 (a
+ * non-finite gradient was found) theta, m, v and the copy are left as they are
+ * and only the gradient is zeroed.
+ */
+void orc_adamw_step_clipped_f64(int64_t n, double* theta, double* m, double* v,
+                                const uint16_t* grad, int grad_kind, double inv_loss_scale,
+                                double clip, int skip,
+                                int64_t t, float lr_f, float beta1_f, float beta2_f,
+                                float eps_f, float wd_f,
+                                uint16_t* copy, int copy_kind, uint16_t* grad_out)
+{
+    const double lr = lr_f, b1 = beta1_f, b2 = beta2_f, eps = eps_f, wd = wd_f;
+    const double bc1 = orc_bias_correction(beta1_f, t);
+    const double bc2 = orc_bias_correction(beta2_f, t);
+    for (int64_t i = 0; i < n; ++i) {
+        if (!skip) {
+            double g = orc_decode16(grad[i], grad_kind) * inv_loss_scale * clip;
+            m[i] = b1 * m[i] + (1.0 - b1) * g;
+            v[i] = b2 * v[i] + (1.0 - b2) * (g * g);
+            double m_hat = m[i] / bc1;
+            double v_hat = v[i] / bc2;
+            double th = theta[i];
+            theta[i] = th - lr * m_hat / (sqrt(v_hat) + eps) - lr * wd * th;
+        }
+        copy[i] = orc_encode16_rne(theta[i], copy_kind);
+        grad_out[i] = 0;
+    }
+}

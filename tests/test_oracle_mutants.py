@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import test_oracle_adamw as A
+import test_oracle_gradclip as GC
 import test_oracle_layernorm as L
 import test_oracle_rmsnorm as RN
 import test_oracle_softmax as S
@@ -24,7 +25,21 @@ LN_PINS = [L.test_dbeta_is_column_sum, L.test_rows_of_dx_sum_to_zero,
 RMS_PINS = [RN.test_dgamma_is_column_sum_of_dy_xhat, RN.test_dx_orthogonal_to_xhat_when_eps_zero,
             RN.test_central_finite_differences, RN.test_matches_torch_rms_norm_autograd_float64]
 
+CLIP_PINS = [GC.test_norm_matches_numpy_over_several_tensors, GC.test_norm_special_cases,
+             GC.test_clip_factor_closed_forms, GC.test_clipped_step_matches_torch_clip_then_adamw,
+             GC.test_skip_leaves_state_and_zeroes_gradient]
+
 MUTANTS = [
+    ("gradclip: norm misses the loss-scale removal",
+     "        g *= inv_loss_scale;\n        s += g * g;", "        s += g * g;", CLIP_PINS),
+    ("gradclip: clip factor inverted",
+     "return max_norm / norm;", "return norm / max_norm;", CLIP_PINS),
+    ("gradclip: clipping on norm >= max_norm only when below",
+     "if (max_norm > 0.0 && norm > max_norm)", "if (max_norm > 0.0 && norm < max_norm)", CLIP_PINS),
+    ("gradclip: clip not applied in the step",
+     "* inv_loss_scale * clip;", "* inv_loss_scale;", CLIP_PINS),
+    ("gradclip: non-finite gradient not flagged",
+     "if (!isfinite(g)) *nonfinite = 1;", "", CLIP_PINS),
     ("rmsnorm: projection term dropped",
      "dxr[j] = rs * (dxhat - xhat * mean_dxhat_xhat);", "dxr[j] = rs * dxhat;", RMS_PINS),
     ("rmsnorm: projection term sign flipped",
