@@ -193,14 +193,15 @@ def clip_factor(norm, max_norm) -> float:
 
 
 def adamw_step_clipped_f64(theta, m, v, grad_bits, grad_kind, inv_loss_scale, clip, skip, t,
-                           lr, beta1, beta2, eps, weight_decay, copy_kind="bf16"):
+                           lr, beta1, beta2, eps, weight_decay, copy_kind="bf16", copy_in=None):
     """AdamW step on the clipped gradient (see oracle.c); same conventions as
-    ``adamw_step_f64``."""
+    ``adamw_step_f64``.  ``copy_in`` is the working copy before the step (returned
+    unchanged when the step is skipped); zeros if omitted."""
     for a in (theta, m, v):
         assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"]
     g = _c(grad_bits, np.uint16)
     n = theta.size
-    copy = np.empty(n, np.uint16)
+    copy = np.zeros(n, np.uint16) if copy_in is None else _c(copy_in, np.uint16).copy()
     gout = np.empty(n, np.uint16)
     _load().orc_adamw_step_clipped_f64(n, _ptr(theta), _ptr(m), _ptr(v), _ptr(g),
                                        KIND[grad_kind], float(inv_loss_scale), float(clip),

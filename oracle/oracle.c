@@ -396,8 +396,9 @@ double orc_clip_factor(double norm, double max_norm)
 /*
  * One AdamW step on the clipped gradient g = (float(grad) * inv_loss_scale) * clip,
  * in double; otherwise identical to orc_adamw_step_f64.  With skip != 0 (a
- * non-finite gradient was found) theta, m, v and the copy are left as they are
- * and only the gradient is zeroed.
+ * non-finite gradient was found) the step does not happen: theta, m, v and the
+ * copy (an in/out array here) are left as they are and only the gradient is
+ * zeroed.
  */
 void orc_adamw_step_clipped_f64(int64_t n, double* theta, double* m, double* v,
                                 const uint16_t* grad, int grad_kind, double inv_loss_scale,
@@ -418,8 +419,8 @@ void orc_adamw_step_clipped_f64(int64_t n, double* theta, double* m, double* v,
             double v_hat = v[i] / bc2;
             double th = theta[i];
             theta[i] = th - lr * m_hat / (sqrt(v_hat) + eps) - lr * wd * th;
+            copy[i] = orc_encode16_rne(theta[i], copy_kind);
         }
-        copy[i] = orc_encode16_rne(theta[i], copy_kind);
         grad_out[i] = 0;
     }
 }
