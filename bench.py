@@ -224,6 +224,9 @@ class HotPath:
         self.rdg = torch.empty(LN_D, device=device)
         self.rws = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(ln_rows, LN_D, torch.bfloat16),
                                dtype=torch.uint8, device=device)
+        self.clip = torch.zeros(3, device=device)
+        self.nws = torch.empty(tb.tb_adamw_grad_norm_workspace_size(self.plan), dtype=torch.uint8,
+                               device=device)
 
     def extras(self):
         """name -> (callable, algorithmic bytes) for the kernels outside the step."""
@@ -238,6 +241,12 @@ class HotPath:
             "rmsnorm_bf16": (lambda: tb.tb_rmsnorm_bwd(self.rdY, self.rx, self.rinv, self.rgamma,
                                                        self.rdX, self.rdg, self.rws),
                              rmsnorm_bytes(self.ln_rows, LN_D, 2)),
+            "adamw_grad_norm": (lambda: tb.tb_adamw_grad_norm(self.plan, 1.0 / LOSS_SCALE, 1.0,
+                                                              self.clip, self.nws),
+                                2 * self.n_params),
+            "adamw_step_clipped": (lambda: tb.tb_adamw_step_clipped(
+                self.plan, self.t + 1, inv_loss_scale=1.0 / LOSS_SCALE, clip=self.clip, **HP),
+                adamw_bytes(self.n_params)),
         }
 
     def step(self, events=None):

@@ -142,6 +142,40 @@ tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
                         const tb_adamw_hparams* hp, float inv_loss_scale,
                         void* stream);
 
+/*
+ * Global gradient-norm clipping with a non-finite check, fused into the step
+ * without a host synchronisation ([GPU-Opt-P2] §"完整训练循环（整合一切）", step
+ * 7: the L2 norm of the unscaled gradient over all parameters; when it exceeds
+ * max_norm the gradients are scaled by max_norm / norm before the optimizer).
+ *
+ * tb_adamw_grad_norm reads every gradient of the plan once (2 bytes per
+ * parameter) and writes three floats to device memory `out`:
+ *     out[0] = norm   = sqrt(sum_i (float(grad_i) * inv_loss_scale)^2)
+ *     out[1] = factor = max_norm / norm if max_norm > 0 and norm > max_norm, else 1
+ *     out[2] = 1 if any gradient element is NaN or infinite, else 0
+ * Per-thread sums are fp32 over at most 64 squares and fp64 beyond; the CTA
+ * partials are added in a fixed order, so the result is reproducible.
+ *   workspace  device scratch of tb_adamw_grad_norm_workspace_size() bytes,
+ *              8-byte aligned (one fp64 partial and one flag per CTA)
+ * Errors: TB_ERR_INVALID_VALUE, TB_ERR_MISALIGNED, TB_ERR_WORKSPACE, TB_ERR_ALIAS,
+ * TB_ERR_DEVICE, TB_ERR_CUDA.
+ *
+ * tb_adamw_step_clipped is tb_adamw_step with the unscaled gradient multiplied by
+ * clip[1] (clip = the `out` of tb_adamw_grad_norm, read on the device).  When
+ * clip[2] != 0 the step does not happen: parameters, moments and the working copy
+ * are left as they are and only the gradient is reset to zero.  Whether the
+ * caller then advances its step counter is its choice (clip[2] can be read back
+ * later).  Errors as tb_adamw_step, plus TB_ERR_INVALID_VALUE for clip == NULL.
+ */
+tb_status tb_adamw_grad_norm_workspace_size(const tb_adamw_plan* plan, size_t* bytes);
+
+tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_loss_scale, float max_norm,
+                             float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t step,
+                                const tb_adamw_hparams* hp, float inv_loss_scale,
+                                const float* clip, void* stream);
+
 /* Free a plan (NULL is accepted).  Synchronises nothing: the caller must not
  * destroy a plan while a step that uses it may still be running. */
 tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan);

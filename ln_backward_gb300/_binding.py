@@ -27,7 +27,8 @@ STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_VALUE", 2: "TB_ERR_UNSUPPORTED_DTYPE",
 EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_create",
            "tb_adamw_step", "tb_adamw_plan_destroy", "tb_softmax_bwd",
            "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd", "tb_layernorm_bwd_noalloc",
-           "tb_softmax_bwd_causal", "tb_rmsnorm_bwd_workspace_size", "tb_rmsnorm_bwd")
+           "tb_softmax_bwd_causal", "tb_rmsnorm_bwd_workspace_size", "tb_rmsnorm_bwd",
+           "tb_adamw_grad_norm_workspace_size", "tb_adamw_grad_norm", "tb_adamw_step_clipped")
 
 
 class TbError(RuntimeError):
@@ -80,6 +81,12 @@ def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.tb_rmsnorm_bwd_workspace_size.restype = i32
     lib.tb_rmsnorm_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, vp, ctypes.c_size_t, vp]
     lib.tb_rmsnorm_bwd.restype = i32
+    lib.tb_adamw_grad_norm_workspace_size.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+    lib.tb_adamw_grad_norm_workspace_size.restype = i32
+    lib.tb_adamw_grad_norm.argtypes = [vp, f32, f32, vp, vp, ctypes.c_size_t, vp]
+    lib.tb_adamw_grad_norm.restype = i32
+    lib.tb_adamw_step_clipped.argtypes = [vp, i64, ctypes.POINTER(tb_adamw_hparams), f32, vp, vp]
+    lib.tb_adamw_step_clipped.restype = i32
     return lib
 
 
@@ -181,6 +188,36 @@ def tb_adamw_step(plan: AdamWPlan, step: int, lr: float, beta1: float, beta2: fl
 
 def tb_adamw_plan_destroy(plan: AdamWPlan) -> None:
     plan.close()
+
+
+def tb_adamw_grad_norm_workspace_size(plan: AdamWPlan) -> int:
+    out = ctypes.c_size_t(0)
+    _check("tb_adamw_grad_norm_workspace_size",
+           lib.tb_adamw_grad_norm_workspace_size(plan.handle, ctypes.byref(out)))
+    return out.value
+
+
+def tb_adamw_grad_norm(plan: AdamWPlan, inv_loss_scale: float, max_norm: float,
+                       out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Writes {norm, clip factor, nonfinite} (3 fp32 values) into ``out`` on the device."""
+    if out.dtype != torch.float32 or out.numel() < 3:
+        raise ValueError("out must hold 3 fp32 values")
+    _check("tb_adamw_grad_norm",
+           lib.tb_adamw_grad_norm(plan.handle, float(inv_loss_scale), float(max_norm), _ptr(out),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+
+
+def tb_adamw_step_clipped(plan: AdamWPlan, step: int, lr: float, beta1: float, beta2: float,
+                          eps: float, weight_decay: float, inv_loss_scale: float,
+                          clip: torch.Tensor, stream=None) -> None:
+    """tb_adamw_step with the gradient scaled by clip[1]; skipped when clip[2] != 0."""
+    if clip.dtype != torch.float32 or clip.numel() < 3:
+        raise ValueError("clip must hold 3 fp32 values")
+    hp = tb_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+    _check("tb_adamw_step_clipped",
+           lib.tb_adamw_step_clipped(plan.handle, int(step), ctypes.byref(hp), float(inv_loss_scale),
+                                     _ptr(clip), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- softmax bwd

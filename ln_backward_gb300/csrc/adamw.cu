@@ -54,11 +54,12 @@ struct Scalars {
     float omb1, omb2;   // 1 - beta, formed in fp32
     float bc1, bc2;     // 1 - beta^t, formed in double and rounded
     float inv_s;        // 1 / loss_scale
+    float clip;         // gradient-norm clip factor (exactly 1 when not clipping)
 };
 
 __device__ __forceinline__ void adamw_update(float& th, float& m, float& v, float g_scaled,
                                              const Scalars& s) {
-    const float g = g_scaled * s.inv_s;
+    const float g = (g_scaled * s.inv_s) * s.clip;
     m = s.beta1 * m + s.omb1 * g;
     v = s.beta2 * v + s.omb2 * (g * g);
     const float m_hat = m / s.bc1;
@@ -79,6 +80,25 @@ __device__ __forceinline__ void scalar_element(const TensorEntry& t, int64_t i, 
     t.v[i] = v;
     static_cast<CT*>(t.c)[i] = C::from_f32(th);
     gp[i] = G::from_f32(0.0f);
+}
+
+// Units [a, e) of one tensor when the step is skipped: only the gradient is reset.
+template <class G>
+__device__ __forceinline__ void zero_segment(const TensorEntry& t, int64_t a, int64_t e) {
+    using GT = typename G::T;
+    const int64_t n = t.n;
+    const int64_t full = n / kUnit;
+    GT* gp = static_cast<GT*>(t.g);
+    if (t.vec_ok) {
+        const int64_t fe = e < full ? e : full;
+        for (int64_t u = a + threadIdx.x; u < fe; u += kThreads)
+            st_stream_u4(gp + u * kUnit, make_uint4(0u, 0u, 0u, 0u));
+        if (full >= a && full < e)
+            for (int64_t i = full * kUnit + threadIdx.x; i < n; i += kThreads) gp[i] = G::from_f32(0.0f);
+    } else {
+        const int64_t hi = e * kUnit < n ? e * kUnit : n;
+        for (int64_t i = a * kUnit + threadIdx.x; i < hi; i += kThreads) gp[i] = G::from_f32(0.0f);
+    }
 }
 
 // Units [a, e) of one tensor (local unit indices).
@@ -160,10 +180,18 @@ __device__ __forceinline__ int tensor_of(const TensorEntry* __restrict__ tab, in
 
 // Tiles of kTileUnits consecutive units are dealt round-robin to the CTAs, so at
 // any moment all CTAs stream through one window of about grid*kTileUnits units.
+// clip (device memory, may be null): {norm, factor, nonfinite} as written by the
+// gradient-norm kernels; the gradient is multiplied by factor, and when nonfinite
+// is set the step is skipped (only the gradient is reset).
 template <class G, class C>
 __global__ void __launch_bounds__(kThreads, 2)
 adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
-                          int64_t n_tiles, Scalars s) {
+                          int64_t n_tiles, Scalars s, const float* __restrict__ clip) {
+    bool skip = false;
+    if (clip) {
+        s.clip = clip[1];
+        skip = clip[2] != 0.0f;
+    }
     int k = 0;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
         const int64_t u_lo = tile * kTileUnits;
@@ -175,10 +203,120 @@ adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t
             const TensorEntry t = tab[kk];
             const int64_t t_end = (kk + 1 < ntab) ? tab[kk + 1].unit_begin : total_units;
             const int64_t seg_hi = u_hi < t_end ? u_hi : t_end;
-            if (seg_hi > u) process_segment<G, C>(t, u - t.unit_begin, seg_hi - t.unit_begin, s);
+            if (seg_hi > u) {
+                if (skip) zero_segment<G>(t, u - t.unit_begin, seg_hi - t.unit_begin);
+                else process_segment<G, C>(t, u - t.unit_begin, seg_hi - t.unit_begin, s);
+            }
             u = seg_hi > u ? seg_hi : u;
             ++kk;
         }
+    }
+}
+
+// ------------------------------------------------------------------ gradient norm
+// Sum of squares of the unscaled gradient over every tensor (same tiles as the
+// step, reading only the 16-bit gradient), plus a non-finite flag.  Each thread
+// adds a tile's squares in fp32 and the tile sums in fp64; each CTA writes one
+// fp64 partial and one flag; the finalize kernel adds the partials in order.
+template <class G>
+__global__ void __launch_bounds__(kThreads)
+adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
+                        int64_t n_tiles, float inv_s, double* __restrict__ part,
+                        int* __restrict__ flags) {
+    using GT = typename G::T;
+    double acc = 0.0;
+    int bad = 0;
+    int k = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int64_t u_lo = tile * kTileUnits;
+        const int64_t u_hi = u_lo + kTileUnits < total_units ? u_lo + kTileUnits : total_units;
+        k = tensor_of(tab, ntab, k, u_lo);
+        float fs = 0.f;
+        int kk = k;
+        int64_t u = u_lo;
+        while (u < u_hi && kk < ntab) {
+            const TensorEntry t = tab[kk];
+            const int64_t t_end = (kk + 1 < ntab) ? tab[kk + 1].unit_begin : total_units;
+            const int64_t seg_hi = u_hi < t_end ? u_hi : t_end;
+            if (seg_hi > u) {
+                const int64_t a = u - t.unit_begin, e = seg_hi - t.unit_begin;
+                const int64_t n = t.n, full = n / kUnit;
+                const GT* gp = static_cast<const GT*>(t.g);
+                int64_t lo_elem = a * kUnit, hi_elem = (e * kUnit < n) ? e * kUnit : n;
+                if (t.vec_ok) {
+                    const int64_t fe = e < full ? e : full;
+                    // four 16-byte loads in flight per thread; absent ones read as zeros
+                    for (int64_t u0 = a + threadIdx.x; u0 < fe; u0 += 4 * kThreads) {
+                        uint4 r[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int64_t uu = u0 + (int64_t)j * kThreads;
+                            r[j] = uu < fe ? ld_stream_u4(gp + uu * kUnit) : make_uint4(0u, 0u, 0u, 0u);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float v[8];
+                            unpack8<G>(r[j], v);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                bad |= !isfinite(v[q]);
+                                const float x = v[q] * inv_s;
+                                fs += x * x;
+                            }
+                        }
+                    }
+                    lo_elem = fe > a ? fe * kUnit : lo_elem;   // scalar tail only
+                }
+                for (int64_t i = lo_elem + threadIdx.x; i < hi_elem; i += kThreads) {
+                    const float g = G::to_f32(gp[i]);
+                    bad |= !isfinite(g);
+                    const float x = g * inv_s;
+                    fs += x * x;
+                }
+            }
+            u = seg_hi > u ? seg_hi : u;
+            ++kk;
+        }
+        acc += (double)fs;
+    }
+    // CTA sum in a fixed order: warp butterfly, then warp 0 over the warp sums.
+    __shared__ double wsum[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = acc;
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) t += wsum[w];
+        part[blockIdx.x] = t;
+        flags[blockIdx.x] = bad;
+    }
+}
+
+// out = {norm, clip factor, nonfinite ? 1 : 0} from the per-CTA partials, added in
+// index order by one CTA (thread j takes j, j+256, ...; then a fixed tree).
+__global__ void __launch_bounds__(kThreads)
+adamw_grad_norm_finalize_kernel(const double* __restrict__ part, const int* __restrict__ flags,
+                                int nparts, float max_norm, float* __restrict__ out) {
+    __shared__ double sh[kThreads];
+    double acc = 0.0;
+    int bad = 0;
+    for (int i = threadIdx.x; i < nparts; i += kThreads) {
+        acc += part[i];
+        bad |= flags[i];
+    }
+    sh[threadIdx.x] = acc;
+    bad = __syncthreads_or(bad);
+    for (int w = kThreads / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double norm = sqrt(sh[0]);
+        const double f = (max_norm > 0.0f && norm > (double)max_norm) ? (double)max_norm / norm : 1.0;
+        out[0] = (float)norm;
+        out[1] = (float)f;
+        out[2] = bad ? 1.0f : 0.0f;
     }
 }
 
@@ -205,7 +343,8 @@ struct tb_adamw_plan {
     tb_dtype copy_dtype;
     tb::TensorEntry* d_table;
     int64_t total_units;
-    int grid;
+    int grid;        // CTAs of the step kernel
+    int norm_grid;   // CTAs of the gradient-norm kernel
 };
 
 extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
@@ -266,6 +405,11 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
                                                       kThreads, 0) != cudaSuccess)
         return TB_ERR_CUDA;
     per_sm = std::max(per_sm, 1);
+    int norm_per_sm = 0;
+    const void* nk = grad_dtype == TB_BF16 ? reinterpret_cast<const void*>(&adamw_grad_sumsq_kernel<BF16>)
+                                           : reinterpret_cast<const void*>(&adamw_grad_sumsq_kernel<F16>);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&norm_per_sm, nk, kThreads, 0) != cudaSuccess)
+        return TB_ERR_CUDA;
 
     tb_adamw_plan* plan = new (std::nothrow) tb_adamw_plan;
     if (!plan) return TB_ERR_OOM;
@@ -276,6 +420,7 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
     plan->copy_dtype = copy_dtype;
     plan->total_units = units;
     plan->grid = info.sm_count * per_sm;
+    plan->norm_grid = info.sm_count * std::max(norm_per_sm, 1);
     plan->d_table = nullptr;
     const size_t bytes = sizeof(TensorEntry) * (size_t)n_tensors;
     cudaError_t e = cudaMalloc(&plan->d_table, bytes);
@@ -293,10 +438,10 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
     return TB_OK;
 }
 
-extern "C" tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
-                                   const tb_adamw_hparams* hp, float inv_loss_scale,
-                                   void* stream) {
-    using namespace tb;
+namespace tb {
+namespace {
+tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adamw_hparams* hp,
+                          float inv_loss_scale, const float* clip, void* stream) {
     if (!plan || !hp || plan->magic != kPlanMagic) return TB_ERR_INVALID_VALUE;
     if (step < 1) return TB_ERR_INVALID_VALUE;
     const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
@@ -305,6 +450,7 @@ extern "C" tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
     if (!std::isfinite(eps) || eps < 0.f) return TB_ERR_INVALID_VALUE;
     if (!std::isfinite(wd) || wd < 0.f) return TB_ERR_INVALID_VALUE;
     if (!std::isfinite(inv_loss_scale) || !(inv_loss_scale > 0.f)) return TB_ERR_INVALID_VALUE;
+    if (clip && !aligned_to(clip, 4)) return TB_ERR_MISALIGNED;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return TB_ERR_CUDA;
     if (dev != plan->device) return TB_ERR_DEVICE;
@@ -321,22 +467,83 @@ extern "C" tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
     s.bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(b1), static_cast<double>(step)));
     s.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(b2), static_cast<double>(step)));
     s.inv_s = inv_loss_scale;
+    s.clip = 1.0f;
 
     const int64_t n_tiles = (plan->total_units + kTileUnits - 1) / kTileUnits;
     const int64_t grid = std::min<int64_t>(plan->grid, n_tiles);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const tb::TensorEntry* tab = plan->d_table;
+    const TensorEntry* tab = plan->d_table;
     const int nt = plan->n_tensors;
     const int64_t tu = plan->total_units;
     const tb_dtype g = plan->grad_dtype, c = plan->copy_dtype;
     if (g == TB_BF16 && c == TB_BF16)
-        adamw_multi_tensor_kernel<BF16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
+        adamw_multi_tensor_kernel<BF16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
     else if (g == TB_BF16 && c == TB_F16)
-        adamw_multi_tensor_kernel<BF16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
+        adamw_multi_tensor_kernel<BF16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
     else if (g == TB_F16 && c == TB_BF16)
-        adamw_multi_tensor_kernel<F16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
+        adamw_multi_tensor_kernel<F16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
     else
-        adamw_multi_tensor_kernel<F16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s);
+        adamw_multi_tensor_kernel<F16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
+    return launch_status();
+}
+
+// Partials of the gradient-norm kernel: one fp64 sum and one int flag per CTA.
+size_t grad_norm_workspace(const tb_adamw_plan* plan) {
+    return (size_t)plan->norm_grid * (sizeof(double) + sizeof(int));
+}
+}  // namespace
+}  // namespace tb
+
+extern "C" tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
+                                   const tb_adamw_hparams* hp, float inv_loss_scale,
+                                   void* stream) {
+    return tb::adamw_step_impl(plan, step, hp, inv_loss_scale, nullptr, stream);
+}
+
+extern "C" tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t step,
+                                           const tb_adamw_hparams* hp, float inv_loss_scale,
+                                           const float* clip, void* stream) {
+    if (!clip) return TB_ERR_INVALID_VALUE;
+    return tb::adamw_step_impl(plan, step, hp, inv_loss_scale, clip, stream);
+}
+
+extern "C" tb_status tb_adamw_grad_norm_workspace_size(const tb_adamw_plan* plan, size_t* bytes) {
+    if (!plan || !bytes || plan->magic != tb::kPlanMagic) return TB_ERR_INVALID_VALUE;
+    *bytes = tb::grad_norm_workspace(plan);
+    return TB_OK;
+}
+
+extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_loss_scale,
+                                        float max_norm, float* out, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    using namespace tb;
+    if (!plan || !out || plan->magic != kPlanMagic) return TB_ERR_INVALID_VALUE;
+    if (!std::isfinite(inv_loss_scale) || !(inv_loss_scale > 0.f)) return TB_ERR_INVALID_VALUE;
+    if (std::isnan(max_norm)) return TB_ERR_INVALID_VALUE;
+    if (!aligned_to(out, 4)) return TB_ERR_MISALIGNED;
+    if (!workspace || workspace_bytes < grad_norm_workspace(plan)) return TB_ERR_WORKSPACE;
+    if (!aligned_to(workspace, 8)) return TB_ERR_MISALIGNED;
+    if (overlap(range_of(out, 3, 4), range_of(workspace, (int64_t)workspace_bytes, 1))) return TB_ERR_ALIAS;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TB_ERR_CUDA;
+    if (dev != plan->device) return TB_ERR_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    double* part = static_cast<double*>(workspace);
+    int* flags = reinterpret_cast<int*>(part + plan->norm_grid);
+    const int64_t n_tiles = (plan->total_units + kTileUnits - 1) / kTileUnits;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(plan->norm_grid, n_tiles));
+    if (plan->total_units > 0) {
+        if (plan->grad_dtype == TB_BF16)
+            adamw_grad_sumsq_kernel<BF16><<<grid, kThreads, 0, st>>>(
+                plan->d_table, plan->n_tensors, plan->total_units, n_tiles, inv_loss_scale, part, flags);
+        else
+            adamw_grad_sumsq_kernel<F16><<<grid, kThreads, 0, st>>>(
+                plan->d_table, plan->n_tensors, plan->total_units, n_tiles, inv_loss_scale, part, flags);
+        if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
+    }
+    adamw_grad_norm_finalize_kernel<<<1, kThreads, 0, st>>>(part, flags,
+                                                            plan->total_units > 0 ? grid : 0,
+                                                            max_norm, out);
     return launch_status();
 }
 
