@@ -70,6 +70,8 @@ def _configure(lib):
     lib.orc_clip_factor.restype = f64
     lib.orc_adamw_step_clipped_f64.argtypes = [i64, vp, vp, vp, vp, i32, f64, f64, i32, i64,
                                                f32, f32, f32, f32, f32, vp, i32, vp]
+    lib.orc_cast_to_f32.argtypes = [i64, vp, i32, f32, vp]
+    lib.orc_cast_from_f32.argtypes = [i64, vp, i32, vp]
     return lib
 
 
@@ -208,6 +210,22 @@ def adamw_step_clipped_f64(theta, m, v, grad_bits, grad_kind, inv_loss_scale, cl
                                        int(bool(skip)), int(t), lr, beta1, beta2, eps,
                                        weight_decay, _ptr(copy), KIND[copy_kind], _ptr(gout))
     return copy, gout
+
+
+# --------------------------------------------------------------------------- casts
+def cast_to_f32(src, kind: str, scale: float) -> np.ndarray:
+    """float32(src * scale); ``src`` holds 16-bit patterns (kind f16/bf16) or float32."""
+    a = _c(src, np.float32 if kind == "f32" else np.uint16)
+    out = np.empty(a.shape, np.float32)
+    _load().orc_cast_to_f32(a.size, _ptr(a), KIND[kind], float(scale), _ptr(out))
+    return out
+
+
+def cast_from_f32(src, kind: str) -> np.ndarray:
+    a = _c(src, np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _load().orc_cast_from_f32(a.size, _ptr(a), KIND[kind], _ptr(out))
+    return out
 
 
 # --------------------------------------------------------------------------- softmax bwd

@@ -424,3 +424,27 @@ void orc_adamw_step_clipped_f64(int64_t n, double* theta, double* m, double* v,
         grad_out[i] = 0;
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Stand-alone casts of the mixed-precision loop                              */
+/*   [GPU-Opt-P2] §"混合精度训练（FP16 / BF16）" and §"完整训练循环（整合一切）"  */
+/*   steps 6 and 9: low-precision gradient -> fp32 times 1/loss_scale; fp32   */
+/*   master -> 16-bit working copy.                                            */
+/* ------------------------------------------------------------------------- */
+
+/* out = float(src * scale) with one rounding of the exact product (the product
+ * of a 16-bit or fp32 value and an fp32 scale is exact in double). */
+void orc_cast_to_f32(int64_t n, const void* src, int kind, float scale, float* out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double x = (kind == ORC_F32) ? (double)((const float*)src)[i]
+                                     : orc_decode16(((const uint16_t*)src)[i], kind);
+        out[i] = (float)(x * (double)scale);
+    }
+}
+
+/* out = the 16-bit value nearest to src (ties to even). */
+void orc_cast_from_f32(int64_t n, const float* src, int kind, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_encode16_rne((double)src[i], kind);
+}

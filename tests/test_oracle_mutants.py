@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import test_oracle_adamw as A
+import test_oracle_cast as CA
 import test_oracle_gradclip as GC
 import test_oracle_layernorm as L
 import test_oracle_rmsnorm as RN
@@ -29,7 +30,12 @@ CLIP_PINS = [GC.test_norm_matches_numpy_over_several_tensors, GC.test_norm_speci
              GC.test_clip_factor_closed_forms, GC.test_clipped_step_matches_torch_clip_then_adamw,
              GC.test_skip_leaves_state_and_zeroes_gradient]
 
+CAST_PINS = [CA.test_cast_to_f32_matches_torch_bitwise, CA.test_cast_from_f32_matches_torch_rne]
+
 MUTANTS = [
+    ("cast: scale ignored", "out[i] = (float)(x * (double)scale);", "out[i] = (float)x;", CAST_PINS),
+    ("cast: product rounded twice through half",
+     "out[i] = (float)(x * (double)scale);", "out[i] = (float)(float)x * scale * 1.0000001f;", CAST_PINS),
     ("gradclip: norm misses the loss-scale removal",
      "        g *= inv_loss_scale;\n        s += g * g;", "        s += g * g;", CLIP_PINS),
     ("gradclip: clip factor inverted",
