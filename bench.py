@@ -224,6 +224,13 @@ class HotPath:
         self.rdg = torch.empty(LN_D, device=device)
         self.rws = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(ln_rows, LN_D, torch.bfloat16),
                                dtype=torch.uint8, device=device)
+        # the pages' unfused tail: fp32 gradients, a plan without working copies
+        self.g32 = torch.zeros(self.st.grad.numel(), dtype=torch.float32, device=device)
+        self.plan32 = tb.tb_adamw_plan_create(
+            [self.st.tensor("theta", i) for i in range(k)], [self.st.tensor("m", i) for i in range(k)],
+            [self.st.tensor("v", i) for i in range(k)],
+            [self.g32.narrow(0, self.st.offsets[i], self.st.sizes[i]) for i in range(k)],
+            [None] * k)
         self.clip = torch.zeros(3, device=device)
         self.nws = torch.empty(tb.tb_adamw_grad_norm_workspace_size(self.plan), dtype=torch.uint8,
                                device=device)
@@ -247,7 +254,16 @@ class HotPath:
             "adamw_step_clipped": (lambda: tb.tb_adamw_step_clipped(
                 self.plan, self.t + 1, inv_loss_scale=1.0 / LOSS_SCALE, clip=self.clip, **HP),
                 adamw_bytes(self.n_params)),
+            # cast 16-bit grad -> fp32 (6 B) + AdamW on fp32 grads (32 B) + cast copy (6 B)
+            "unfused_adamw_pipeline": (self._unfused, 44 * self.n_params),
         }
+
+    def _unfused(self):
+        """The pages' unfused optimizer tail, for comparison with the fused step."""
+        tb = self.tb
+        tb.tb_cast_to_f32(self.st.grad, self.g32, scale=1.0 / LOSS_SCALE)
+        tb.tb_adamw_step(self.plan32, self.t + 1, inv_loss_scale=1.0, **HP)
+        tb.tb_cast_from_f32(self.st.theta, self.st.copy)
 
     def step(self, events=None):
         tb = self.tb

@@ -96,7 +96,7 @@ typedef struct tb_tensor_desc {
     float* m;       /* fp32 first moment   [n], read and written in place        */
     float* v;       /* fp32 second moment  [n], read and written in place        */
     void* grad;     /* loss-scaled gradient [n] in grad_dtype, read then zeroed  */
-    void* copy;     /* working copy [n] in copy_dtype, written                   */
+    void* copy;     /* working copy [n] in copy_dtype, written; NULL: none       */
     int64_t n;      /* element count (>= 0; 0 skips the tensor)                  */
 } tb_tensor_desc;
 
@@ -115,12 +115,15 @@ typedef struct tb_adamw_plan tb_adamw_plan;   /* opaque */
  * the current device once, so that every later step is a single launch.
  *   tensors     host array of n_tensors descriptors (read during the call only)
  *   n_tensors   >= 1
- *   grad_dtype  TB_F16 or TB_BF16
- *   copy_dtype  TB_BF16 or TB_F16
+ *   grad_dtype  TB_F16, TB_BF16 or TB_F32
+ *   copy_dtype  TB_BF16 or TB_F16 (unused when the tensors have no copy)
+ *               Either every tensor with n > 0 has a working copy, or none has
+ *               (copy == NULL: the step writes no copy).
  *   out         receives the plan; the caller owns it and frees it with
  *               tb_adamw_plan_destroy.  The plan owns a device copy of the table
  *               (64 bytes per tensor) and remembers the current device.
- * Errors: TB_ERR_INVALID_VALUE (null pointer with n > 0, n < 0, n_tensors < 1,
+ * Errors: TB_ERR_INVALID_VALUE (null param/m/v/grad with n > 0, copies given for
+ * some tensors only, n < 0, n_tensors < 1,
  * out == NULL), TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_MISALIGNED, TB_ERR_ALIAS (any
  * two of the 5*n_tensors buffers overlap), TB_ERR_OOM, TB_ERR_CUDA.
  */
@@ -179,6 +182,27 @@ tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t step,
 /* Free a plan (NULL is accepted).  Synchronises nothing: the caller must not
  * destroy a plan while a step that uses it may still be running. */
 tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan);
+
+/* ======================================================================== */
+/* Stand-alone casts                                                         */
+/* ======================================================================== */
+/*
+ * The two casts of the pages' mixed-precision loop that the fused step does
+ * internally ([GPU-Opt-P2] §"混合精度训练（FP16 / BF16）", §"完整训练循环（整合一切）"
+ * steps 6 and 9), for callers that keep the optimizer steps apart:
+ *   tb_cast_to_f32   : dst[i] = float(src[i]) * scale (one fp32 rounding),
+ *                      src in src_dtype (TB_F16, TB_BF16 or TB_F32), dst fp32
+ *   tb_cast_from_f32 : dst[i] = round-to-nearest-even(src[i]) in dst_dtype
+ *                      (TB_F16 or TB_BF16)
+ *   n >= 0 elements (0: nothing is enqueued); src and dst must not overlap.
+ * Errors: TB_ERR_INVALID_VALUE, TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_MISALIGNED,
+ * TB_ERR_ALIAS, TB_ERR_CUDA.
+ */
+tb_status tb_cast_to_f32(const void* src, tb_dtype src_dtype, float scale, float* dst,
+                         int64_t n, void* stream);
+
+tb_status tb_cast_from_f32(const float* src, void* dst, tb_dtype dst_dtype, int64_t n,
+                           void* stream);
 
 /* ======================================================================== */
 /* Softmax backward                                                          */

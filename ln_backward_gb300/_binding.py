@@ -28,7 +28,8 @@ EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_c
            "tb_adamw_step", "tb_adamw_plan_destroy", "tb_softmax_bwd",
            "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd", "tb_layernorm_bwd_noalloc",
            "tb_softmax_bwd_causal", "tb_rmsnorm_bwd_workspace_size", "tb_rmsnorm_bwd",
-           "tb_adamw_grad_norm_workspace_size", "tb_adamw_grad_norm", "tb_adamw_step_clipped")
+           "tb_adamw_grad_norm_workspace_size", "tb_adamw_grad_norm", "tb_adamw_step_clipped",
+           "tb_cast_to_f32", "tb_cast_from_f32")
 
 
 class TbError(RuntimeError):
@@ -87,6 +88,10 @@ def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.tb_adamw_grad_norm.restype = i32
     lib.tb_adamw_step_clipped.argtypes = [vp, i64, ctypes.POINTER(tb_adamw_hparams), f32, vp, vp]
     lib.tb_adamw_step_clipped.restype = i32
+    lib.tb_cast_to_f32.argtypes = [vp, i32, f32, vp, i64, vp]
+    lib.tb_cast_to_f32.restype = i32
+    lib.tb_cast_from_f32.argtypes = [vp, vp, i32, i64, vp]
+    lib.tb_cast_from_f32.restype = i32
     return lib
 
 
@@ -172,7 +177,8 @@ def tb_adamw_plan_create(params: Sequence[torch.Tensor], ms: Sequence[torch.Tens
         descs[i] = tb_tensor_desc(_ptr(params[i]), _ptr(ms[i]), _ptr(vs[i]), _ptr(grads[i]),
                                   _ptr(copies[i]), params[i].numel())
     gdt = _dtype(grads[0]) if n else TB_BF16
-    cdt = _dtype(copies[0]) if n else TB_BF16
+    with_copy = [c for c in copies if c is not None]
+    cdt = _dtype(with_copy[0]) if with_copy else TB_BF16
     handle = ctypes.c_void_p(None)
     _check("tb_adamw_plan_create",
            lib.tb_adamw_plan_create(descs, n, gdt, cdt, ctypes.byref(handle)))
@@ -218,6 +224,23 @@ def tb_adamw_step_clipped(plan: AdamWPlan, step: int, lr: float, beta1: float, b
     _check("tb_adamw_step_clipped",
            lib.tb_adamw_step_clipped(plan.handle, int(step), ctypes.byref(hp), float(inv_loss_scale),
                                      _ptr(clip), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- casts
+def tb_cast_to_f32(src: torch.Tensor, dst: torch.Tensor, scale: float = 1.0, stream=None) -> None:
+    """dst = float(src) * scale (dst fp32, same number of elements)."""
+    if dst.dtype != torch.float32 or dst.numel() != src.numel():
+        raise ValueError("dst must be fp32 with as many elements as src")
+    _check("tb_cast_to_f32", lib.tb_cast_to_f32(_ptr(src), _dtype(src), float(scale), _ptr(dst),
+                                                src.numel(), _stream(stream)))
+
+
+def tb_cast_from_f32(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """dst = round-to-nearest-even(src) in dst's 16-bit dtype."""
+    if src.dtype != torch.float32 or dst.numel() != src.numel():
+        raise ValueError("src must be fp32 with as many elements as dst")
+    _check("tb_cast_from_f32", lib.tb_cast_from_f32(_ptr(src), _ptr(dst), _dtype(dst), src.numel(),
+                                                    _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- softmax bwd

@@ -22,6 +22,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <new>
+#include <type_traits>
 #include <vector>
 
 #include "tb_common.cuh"
@@ -57,6 +58,15 @@ struct Scalars {
     float clip;         // gradient-norm clip factor (exactly 1 when not clipping)
 };
 
+// Copy-format tag of plans whose tensors have no working copy: nothing is written.
+struct NoCopy {
+    using T = uint16_t;
+};
+template <class C>
+constexpr bool kHasCopy = !std::is_same<C, NoCopy>::value;
+template <class G>
+constexpr bool kF32Grad = std::is_same<G, F32>::value;
+
 __device__ __forceinline__ void adamw_update(float& th, float& m, float& v, float g_scaled,
                                              const Scalars& s) {
     const float g = (g_scaled * s.inv_s) * s.clip;
@@ -78,7 +88,7 @@ __device__ __forceinline__ void scalar_element(const TensorEntry& t, int64_t i, 
     t.p[i] = th;
     t.m[i] = m;
     t.v[i] = v;
-    static_cast<CT*>(t.c)[i] = C::from_f32(th);
+    if constexpr (kHasCopy<C>) static_cast<CT*>(t.c)[i] = C::from_f32(th);
     gp[i] = G::from_f32(0.0f);
 }
 
@@ -91,8 +101,14 @@ __device__ __forceinline__ void zero_segment(const TensorEntry& t, int64_t a, in
     GT* gp = static_cast<GT*>(t.g);
     if (t.vec_ok) {
         const int64_t fe = e < full ? e : full;
-        for (int64_t u = a + threadIdx.x; u < fe; u += kThreads)
-            st_stream_u4(gp + u * kUnit, make_uint4(0u, 0u, 0u, 0u));
+        for (int64_t u = a + threadIdx.x; u < fe; u += kThreads) {
+            if constexpr (kF32Grad<G>) {
+                st_stream_f4(reinterpret_cast<float*>(gp) + u * kUnit, make_float4(0.f, 0.f, 0.f, 0.f));
+                st_stream_f4(reinterpret_cast<float*>(gp) + u * kUnit + 4, make_float4(0.f, 0.f, 0.f, 0.f));
+            } else {
+                st_stream_u4(gp + u * kUnit, make_uint4(0u, 0u, 0u, 0u));
+            }
+        }
         if (full >= a && full < e)
             for (int64_t i = full * kUnit + threadIdx.x; i < n; i += kThreads) gp[i] = G::from_f32(0.0f);
     } else {
@@ -123,14 +139,26 @@ __device__ __forceinline__ void process_segment(const TensorEntry& t, int64_t a,
                     float4 a0 = ld_stream_f4(t.p + i0), a1 = ld_stream_f4(t.p + i0 + 4);
                     float4 b0 = ld_stream_f4(t.m + i0), b1 = ld_stream_f4(t.m + i0 + 4);
                     float4 c0 = ld_stream_f4(t.v + i0), c1 = ld_stream_f4(t.v + i0 + 4);
-                    uint4 gr = ld_stream_u4(static_cast<const GT*>(t.g) + i0);
+                    uint4 gr;
+                    float4 gf0, gf1;
+                    if constexpr (kF32Grad<G>) {
+                        gf0 = ld_stream_f4(static_cast<const float*>(t.g) + i0);
+                        gf1 = ld_stream_f4(static_cast<const float*>(t.g) + i0 + 4);
+                    } else {
+                        gr = ld_stream_u4(static_cast<const GT*>(t.g) + i0);
+                    }
                     th[j][0] = a0.x; th[j][1] = a0.y; th[j][2] = a0.z; th[j][3] = a0.w;
                     th[j][4] = a1.x; th[j][5] = a1.y; th[j][6] = a1.z; th[j][7] = a1.w;
                     mm[j][0] = b0.x; mm[j][1] = b0.y; mm[j][2] = b0.z; mm[j][3] = b0.w;
                     mm[j][4] = b1.x; mm[j][5] = b1.y; mm[j][6] = b1.z; mm[j][7] = b1.w;
                     vv[j][0] = c0.x; vv[j][1] = c0.y; vv[j][2] = c0.z; vv[j][3] = c0.w;
                     vv[j][4] = c1.x; vv[j][5] = c1.y; vv[j][6] = c1.z; vv[j][7] = c1.w;
-                    unpack8<G>(gr, gg[j]);
+                    if constexpr (kF32Grad<G>) {
+                        gg[j][0] = gf0.x; gg[j][1] = gf0.y; gg[j][2] = gf0.z; gg[j][3] = gf0.w;
+                        gg[j][4] = gf1.x; gg[j][5] = gf1.y; gg[j][6] = gf1.z; gg[j][7] = gf1.w;
+                    } else {
+                        unpack8<G>(gr, gg[j]);
+                    }
                 }
             }
 #pragma unroll
@@ -145,8 +173,13 @@ __device__ __forceinline__ void process_segment(const TensorEntry& t, int64_t a,
                 st_stream_f4(t.m + i0 + 4, make_float4(mm[j][4], mm[j][5], mm[j][6], mm[j][7]));
                 st_stream_f4(t.v + i0, make_float4(vv[j][0], vv[j][1], vv[j][2], vv[j][3]));
                 st_stream_f4(t.v + i0 + 4, make_float4(vv[j][4], vv[j][5], vv[j][6], vv[j][7]));
-                st_stream_u4(static_cast<CT*>(t.c) + i0, pack8<C>(th[j]));
-                st_stream_u4(static_cast<GT*>(t.g) + i0, make_uint4(0u, 0u, 0u, 0u));
+                if constexpr (kHasCopy<C>) st_stream_u4(static_cast<CT*>(t.c) + i0, pack8<C>(th[j]));
+                if constexpr (kF32Grad<G>) {
+                    st_stream_f4(static_cast<float*>(t.g) + i0, make_float4(0.f, 0.f, 0.f, 0.f));
+                    st_stream_f4(static_cast<float*>(t.g) + i0 + 4, make_float4(0.f, 0.f, 0.f, 0.f));
+                } else {
+                    st_stream_u4(static_cast<GT*>(t.g) + i0, make_uint4(0u, 0u, 0u, 0u));
+                }
             }
         }
         // The tensor's last, partial unit (fewer than 8 elements).
@@ -245,7 +278,31 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
                 int64_t lo_elem = a * kUnit, hi_elem = (e * kUnit < n) ? e * kUnit : n;
                 if (t.vec_ok) {
                     const int64_t fe = e < full ? e : full;
-                    // four 16-byte loads in flight per thread; absent ones read as zeros
+                    // four units in flight per thread; absent ones read as zeros
+                    if constexpr (kF32Grad<G>) {
+                        const float* gf = reinterpret_cast<const float*>(gp);
+                        for (int64_t u0 = a + threadIdx.x; u0 < fe; u0 += 4 * kThreads) {
+                            float4 r[4][2];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int64_t uu = u0 + (int64_t)j * kThreads;
+                                const bool in = uu < fe;
+                                r[j][0] = in ? ld_stream_f4(gf + uu * kUnit) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                r[j][1] = in ? ld_stream_f4(gf + uu * kUnit + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float v[8] = {r[j][0].x, r[j][0].y, r[j][0].z, r[j][0].w,
+                                                    r[j][1].x, r[j][1].y, r[j][1].z, r[j][1].w};
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    bad |= !isfinite(v[q]);
+                                    const float x = v[q] * inv_s;
+                                    fs += x * x;
+                                }
+                            }
+                        }
+                    } else
                     for (int64_t u0 = a + threadIdx.x; u0 < fe; u0 += 4 * kThreads) {
                         uint4 r[4];
 #pragma unroll
@@ -320,16 +377,28 @@ adamw_grad_norm_finalize_kernel(const double* __restrict__ part, const int* __re
     }
 }
 
-template <class G, class C>
-const void* kernel_for() {
-    return reinterpret_cast<const void*>(&adamw_multi_tensor_kernel<G, C>);
+template <class G>
+const void* step_kernel_for(tb_dtype c, bool copy) {
+    if (!copy) return reinterpret_cast<const void*>(&adamw_multi_tensor_kernel<G, NoCopy>);
+    return c == TB_BF16 ? reinterpret_cast<const void*>(&adamw_multi_tensor_kernel<G, BF16>)
+                        : reinterpret_cast<const void*>(&adamw_multi_tensor_kernel<G, F16>);
 }
 
-const void* select_kernel(tb_dtype g, tb_dtype c) {
-    if (g == TB_BF16 && c == TB_BF16) return kernel_for<BF16, BF16>();
-    if (g == TB_BF16 && c == TB_F16) return kernel_for<BF16, F16>();
-    if (g == TB_F16 && c == TB_BF16) return kernel_for<F16, BF16>();
-    return kernel_for<F16, F16>();
+// The step kernel for a gradient format, copy format and presence of copies.
+const void* step_kernel(tb_dtype g, tb_dtype c, bool copy) {
+    switch (g) {
+        case TB_BF16: return step_kernel_for<BF16>(c, copy);
+        case TB_F16: return step_kernel_for<F16>(c, copy);
+        default: return step_kernel_for<F32>(c, copy);
+    }
+}
+
+const void* norm_kernel(tb_dtype g) {
+    switch (g) {
+        case TB_BF16: return reinterpret_cast<const void*>(&adamw_grad_sumsq_kernel<BF16>);
+        case TB_F16: return reinterpret_cast<const void*>(&adamw_grad_sumsq_kernel<F16>);
+        default: return reinterpret_cast<const void*>(&adamw_grad_sumsq_kernel<F32>);
+    }
 }
 
 }  // namespace
@@ -345,6 +414,7 @@ struct tb_adamw_plan {
     int64_t total_units;
     int grid;        // CTAs of the step kernel
     int norm_grid;   // CTAs of the gradient-norm kernel
+    bool has_copy;   // the tensors have working copies (all of them, or none)
 };
 
 extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
@@ -353,8 +423,19 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
     using namespace tb;
     if (!out || !tensors || n_tensors < 1) return TB_ERR_INVALID_VALUE;
     *out = nullptr;
-    if (grad_dtype != TB_BF16 && grad_dtype != TB_F16) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (!dtype_valid(grad_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
     if (copy_dtype != TB_BF16 && copy_dtype != TB_F16) return TB_ERR_UNSUPPORTED_DTYPE;
+    const size_t gs = dtype_size(grad_dtype);
+    // Working copies: every tensor with elements has one, or none has.
+    int with_copy = 0, sized = 0;
+    for (int i = 0; i < n_tensors; ++i) {
+        if (tensors[i].n > 0) {
+            ++sized;
+            with_copy += tensors[i].copy != nullptr;
+        }
+    }
+    if (with_copy != 0 && with_copy != sized) return TB_ERR_INVALID_VALUE;
+    const bool has_copy = with_copy > 0 || sized == 0;
 
     std::vector<TensorEntry> tab(n_tensors);
     std::vector<Range> ranges;
@@ -363,9 +444,9 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
     for (int i = 0; i < n_tensors; ++i) {
         const tb_tensor_desc& d = tensors[i];
         if (d.n < 0) return TB_ERR_INVALID_VALUE;
-        if (d.n > 0 && (!d.param || !d.m || !d.v || !d.grad || !d.copy)) return TB_ERR_INVALID_VALUE;
+        if (d.n > 0 && (!d.param || !d.m || !d.v || !d.grad)) return TB_ERR_INVALID_VALUE;
         if (d.n > 0 && (!aligned_to(d.param, 4) || !aligned_to(d.m, 4) || !aligned_to(d.v, 4) ||
-                        !aligned_to(d.grad, 2) || !aligned_to(d.copy, 2)))
+                        !aligned_to(d.grad, gs) || !aligned_to(d.copy, 2)))
             return TB_ERR_MISALIGNED;
         if (d.n > INT64_MAX / 8 - units * 8) return TB_ERR_INVALID_VALUE;
         TensorEntry& t = tab[i];
@@ -383,8 +464,8 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
         ranges.push_back(range_of(d.param, d.n, 4));
         ranges.push_back(range_of(d.m, d.n, 4));
         ranges.push_back(range_of(d.v, d.n, 4));
-        ranges.push_back(range_of(d.grad, d.n, 2));
-        ranges.push_back(range_of(d.copy, d.n, 2));
+        ranges.push_back(range_of(d.grad, d.n, gs));
+        if (d.copy) ranges.push_back(range_of(d.copy, d.n, 2));
     }
     // No two buffers may overlap: sort by start, compare with the furthest end so far.
     ranges.erase(std::remove_if(ranges.begin(), ranges.end(),
@@ -401,14 +482,13 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
     DeviceInfo info{};
     if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, select_kernel(grad_dtype, copy_dtype),
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_kernel(grad_dtype, copy_dtype, has_copy),
                                                       kThreads, 0) != cudaSuccess)
         return TB_ERR_CUDA;
     per_sm = std::max(per_sm, 1);
     int norm_per_sm = 0;
-    const void* nk = grad_dtype == TB_BF16 ? reinterpret_cast<const void*>(&adamw_grad_sumsq_kernel<BF16>)
-                                           : reinterpret_cast<const void*>(&adamw_grad_sumsq_kernel<F16>);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&norm_per_sm, nk, kThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&norm_per_sm, norm_kernel(grad_dtype), kThreads,
+                                                      0) != cudaSuccess)
         return TB_ERR_CUDA;
 
     tb_adamw_plan* plan = new (std::nothrow) tb_adamw_plan;
@@ -421,6 +501,7 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
     plan->total_units = units;
     plan->grid = info.sm_count * per_sm;
     plan->norm_grid = info.sm_count * std::max(norm_per_sm, 1);
+    plan->has_copy = has_copy;
     plan->d_table = nullptr;
     const size_t bytes = sizeof(TensorEntry) * (size_t)n_tensors;
     cudaError_t e = cudaMalloc(&plan->d_table, bytes);
@@ -469,22 +550,16 @@ tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adam
     s.inv_s = inv_loss_scale;
     s.clip = 1.0f;
 
-    const int64_t n_tiles = (plan->total_units + kTileUnits - 1) / kTileUnits;
-    const int64_t grid = std::min<int64_t>(plan->grid, n_tiles);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int64_t n_tiles = (plan->total_units + kTileUnits - 1) / kTileUnits;
+    const unsigned grid = (unsigned)std::min<int64_t>(plan->grid, n_tiles);
     const TensorEntry* tab = plan->d_table;
-    const int nt = plan->n_tensors;
-    const int64_t tu = plan->total_units;
-    const tb_dtype g = plan->grad_dtype, c = plan->copy_dtype;
-    if (g == TB_BF16 && c == TB_BF16)
-        adamw_multi_tensor_kernel<BF16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
-    else if (g == TB_BF16 && c == TB_F16)
-        adamw_multi_tensor_kernel<BF16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
-    else if (g == TB_F16 && c == TB_BF16)
-        adamw_multi_tensor_kernel<F16, BF16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
-    else
-        adamw_multi_tensor_kernel<F16, F16><<<(unsigned)grid, kThreads, 0, st>>>(tab, nt, tu, n_tiles, s, clip);
-    return launch_status();
+    int nt = plan->n_tensors;
+    int64_t tu = plan->total_units;
+    void* args[] = {&tab, &nt, &tu, &n_tiles, &s, &clip};
+    if (cudaLaunchKernel(step_kernel(plan->grad_dtype, plan->copy_dtype, plan->has_copy), dim3(grid),
+                         dim3(kThreads), args, 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TB_ERR_CUDA;
+    return TB_OK;
 }
 
 // Partials of the gradient-norm kernel: one fp64 sum and one int flag per CTA.
@@ -533,13 +608,15 @@ extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_los
     const int64_t n_tiles = (plan->total_units + kTileUnits - 1) / kTileUnits;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(plan->norm_grid, n_tiles));
     if (plan->total_units > 0) {
-        if (plan->grad_dtype == TB_BF16)
-            adamw_grad_sumsq_kernel<BF16><<<grid, kThreads, 0, st>>>(
-                plan->d_table, plan->n_tensors, plan->total_units, n_tiles, inv_loss_scale, part, flags);
-        else
-            adamw_grad_sumsq_kernel<F16><<<grid, kThreads, 0, st>>>(
-                plan->d_table, plan->n_tensors, plan->total_units, n_tiles, inv_loss_scale, part, flags);
-        if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
+        const TensorEntry* tab = plan->d_table;
+        int nt = plan->n_tensors;
+        int64_t tu = plan->total_units;
+        int64_t nti = n_tiles;
+        float inv = inv_loss_scale;
+        void* args[] = {&tab, &nt, &tu, &nti, &inv, &part, &flags};
+        if (cudaLaunchKernel(norm_kernel(plan->grad_dtype), dim3(grid), dim3(kThreads), args, 0, st) !=
+            cudaSuccess)
+            return TB_ERR_CUDA;
     }
     adamw_grad_norm_finalize_kernel<<<1, kThreads, 0, st>>>(part, flags,
                                                             plan->total_units > 0 ? grid : 0,

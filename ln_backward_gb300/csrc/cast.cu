@@ -1,0 +1,136 @@
+// cast.cu -- stand-alone precision casts of the mixed-precision training loop.
+//
+// "GPU 优化实战 Part 2：用 CUDA/ROCm 实现 LLM 反向传播与训练循环", sections
+// "混合精度训练（FP16 / BF16）" and "完整训练循环（整合一切）" (steps 6 and 9): the
+// low-precision gradient is cast to fp32 and multiplied by 1/loss_scale before
+// the optimizer, and the fp32 master weights are cast back to a 16-bit working
+// copy after it.  The fused AdamW step does both inside its single pass; these
+// kernels exist for callers that keep the steps apart (and to time that unfused
+// pipeline against the fused one).
+//
+//   tb_cast_to_f32   : dst = float(src) * scale   (one fp32 rounding of the product)
+//   tb_cast_from_f32 : dst = round-to-nearest-even(src) in a 16-bit format
+//
+// Grid-stride over 8-element units with 16-byte vector accesses when both
+// pointers are 16-byte aligned; a scalar loop otherwise and for the ragged tail.
+#include <algorithm>
+
+#include "tb_common.cuh"
+
+namespace tb {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Eight source elements as fp32 (16-bit formats: one 16-byte vector; fp32: two).
+template <class S>
+__device__ __forceinline__ void load8(const void* p, int64_t i0, float (&f)[8]) {
+    unpack8<S>(ld_stream_u4(static_cast<const typename S::T*>(p) + i0), f);
+}
+template <>
+__device__ __forceinline__ void load8<F32>(const void* p, int64_t i0, float (&f)[8]) {
+    const float* q = static_cast<const float*>(p) + i0;
+    const float4 a = ld_stream_f4(q), b = ld_stream_f4(q + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+template <class S>
+__global__ void __launch_bounds__(kThreads)
+cast_to_f32_kernel(const void* __restrict__ src, float* __restrict__ dst, int64_t n, float scale,
+                   int vec) {
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t units = n / 8;
+        for (int64_t u = tid; u < units; u += stride) {
+            float f[8];
+            load8<S>(src, u * 8, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) f[q] *= scale;
+            st_stream_f4(dst + u * 8, make_float4(f[0], f[1], f[2], f[3]));
+            st_stream_f4(dst + u * 8 + 4, make_float4(f[4], f[5], f[6], f[7]));
+        }
+        done = units * 8;
+    }
+    const typename S::T* s = static_cast<const typename S::T*>(src);
+    for (int64_t i = done + tid; i < n; i += stride) dst[i] = S::to_f32(s[i]) * scale;
+}
+
+template <class D>
+__global__ void __launch_bounds__(kThreads)
+cast_from_f32_kernel(const float* __restrict__ src, void* __restrict__ dst, int64_t n, int vec) {
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    typename D::T* d = static_cast<typename D::T*>(dst);
+    int64_t done = 0;
+    if (vec) {
+        const int64_t units = n / 8;
+        for (int64_t u = tid; u < units; u += stride) {
+            float f[8];
+            load8<F32>(src, u * 8, f);
+            st_stream_u4(d + u * 8, pack8<D>(f));
+        }
+        done = units * 8;
+    }
+    for (int64_t i = done + tid; i < n; i += stride) d[i] = D::from_f32(src[i]);
+}
+
+unsigned grid_for(const void* kernel, int64_t n, int sms) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+    const int64_t want = (n / 8 + kThreads - 1) / kThreads + 1;
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1)));
+}
+
+}  // namespace
+}  // namespace tb
+
+extern "C" tb_status tb_cast_to_f32(const void* src, tb_dtype src_dtype, float scale, float* dst,
+                                    int64_t n, void* stream) {
+    using namespace tb;
+    if (n < 0) return TB_ERR_INVALID_VALUE;
+    if (!dtype_valid(src_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (n == 0) return TB_OK;
+    if (!src || !dst) return TB_ERR_INVALID_VALUE;
+    const size_t es = dtype_size(src_dtype);
+    if (!aligned_to(src, es) || !aligned_to(dst, 4)) return TB_ERR_MISALIGNED;
+    if (overlap(range_of(src, n, es), range_of(dst, n, 4))) return TB_ERR_ALIAS;
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    int vec = aligned_to(src, 16) && aligned_to(dst, 16);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const void* k = src_dtype == TB_BF16 ? reinterpret_cast<const void*>(&cast_to_f32_kernel<BF16>)
+                  : src_dtype == TB_F16  ? reinterpret_cast<const void*>(&cast_to_f32_kernel<F16>)
+                                         : reinterpret_cast<const void*>(&cast_to_f32_kernel<F32>);
+    void* args[] = {&src, &dst, &n, &scale, &vec};
+    if (cudaLaunchKernel(k, dim3(grid_for(k, n, info.sm_count)), dim3(kThreads), args, 0, st) !=
+        cudaSuccess)
+        return TB_ERR_CUDA;
+    return TB_OK;
+}
+
+extern "C" tb_status tb_cast_from_f32(const float* src, void* dst, tb_dtype dst_dtype, int64_t n,
+                                      void* stream) {
+    using namespace tb;
+    if (n < 0) return TB_ERR_INVALID_VALUE;
+    if (dst_dtype != TB_BF16 && dst_dtype != TB_F16) return TB_ERR_UNSUPPORTED_DTYPE;
+    if (n == 0) return TB_OK;
+    if (!src || !dst) return TB_ERR_INVALID_VALUE;
+    if (!aligned_to(src, 4) || !aligned_to(dst, 2)) return TB_ERR_MISALIGNED;
+    if (overlap(range_of(src, n, 4), range_of(dst, n, 2))) return TB_ERR_ALIAS;
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    int vec = aligned_to(src, 16) && aligned_to(dst, 16);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const void* k = dst_dtype == TB_BF16 ? reinterpret_cast<const void*>(&cast_from_f32_kernel<BF16>)
+                                         : reinterpret_cast<const void*>(&cast_from_f32_kernel<F16>);
+    void* args[] = {&src, &dst, &n, &vec};
+    if (cudaLaunchKernel(k, dim3(grid_for(k, n, info.sm_count)), dim3(kThreads), args, 0, st) !=
+        cudaSuccess)
+        return TB_ERR_CUDA;
+    return TB_OK;
+}

@@ -89,7 +89,7 @@ def test_adamw_plan_validation(tb):
     arr = (tb._binding.tb_tensor_desc * 1)(ok)
     assert lib.tb_adamw_plan_create(arr, 0, BF16, BF16, ctypes.byref(h)) == INVALID
     assert lib.tb_adamw_plan_create(arr, 1, BF16, BF16, None) == INVALID
-    assert _create(tb, [ok], gdt=F32) == DTYPE
+    assert _create(tb, [ok], gdt=7) == DTYPE
     assert _create(tb, [ok], cdt=F32) == DTYPE
     assert _create(tb, [_desc(tb, base, base + 4096, base + 8192, base + 12288, base + 14336, -1)]) == INVALID
     assert _create(tb, [_desc(tb, None, base + 4096, base + 8192, base + 12288, base + 14336, 8)]) == INVALID
@@ -97,6 +97,12 @@ def test_adamw_plan_validation(tb):
     assert _create(tb, [_desc(tb, base, base + 4096, base + 8192, base + 12289, base + 14336, 8)]) == MISALIGNED
     # m overlaps param
     assert _create(tb, [_desc(tb, base, base + 2048, base + 8192, base + 12288, base + 14336, 1024)]) == ALIAS
+    # fp32 gradients must be 4-byte aligned
+    assert _create(tb, [_desc(tb, base, base + 4096, base + 8192, base + 12290, None, 8)],
+                   gdt=F32) == MISALIGNED
+    # working copies for some tensors only
+    other_nc = _desc(tb, base + 65536, base + 69632, base + 73728, base + 77824, None, 64)
+    assert _create(tb, [ok, other_nc]) == INVALID
     # two tensors sharing a grad buffer
     other = _desc(tb, base + 65536, base + 69632, base + 73728, base + 12288, base + 81920, 64)
     assert _create(tb, [ok, other]) == ALIAS
@@ -158,3 +164,16 @@ def test_product_path_does_not_touch_the_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text and "oracle.c" not in text, f
+
+
+def test_cast_validation(tb):
+    lib = tb._binding.lib
+    A, B = 0x10000, 0x40000
+    assert lib.tb_cast_to_f32(A, F16, 1.0, B, -1, None) == INVALID
+    assert lib.tb_cast_to_f32(A, 9, 1.0, B, 4, None) == DTYPE
+    assert lib.tb_cast_to_f32(A, F16, 1.0, B, 0, None) == TB_OK
+    assert lib.tb_cast_to_f32(A + 1, F16, 1.0, B, 4, None) == MISALIGNED
+    assert lib.tb_cast_to_f32(A, F16, 1.0, A + 4, 4, None) == ALIAS
+    assert lib.tb_cast_from_f32(A, B, F32, 4, None) == DTYPE
+    assert lib.tb_cast_from_f32(A, A + 2, BF16, 4, None) == ALIAS
+    assert lib.tb_cast_from_f32(None, B, BF16, 4, None) == INVALID
