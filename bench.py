@@ -332,7 +332,8 @@ def run_ours(args):
     kernels["adamw"]["gparams_s"] = round(hp_path.n_params / (mean_ms["adamw"] / 1e3) / 1e9, 2)
     ad_gbs = kernels["adamw"]["GB_s"]
 
-    extras = time_extras(hp_path, reps=max(K, 10), peak=measured_peak()[0])
+    extras = (None if args.no_extras
+              else time_extras(hp_path, reps=max(K, 10), peak=measured_peak()[0]))
     e2e = run_e2e(hp_path, K) if not args.no_e2e else None
     if e2e is not None:
         e2e_ms = reduce_over_ranks([e2e.pop("ms")], "max")[0]
@@ -371,9 +372,11 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-# Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, from
-# ncu; None until a capture of the current kernel exists.
-ADAMW_TRAFFIC_PER_LAUNCH = None
+# Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload: the ncu
+# capture of the GPT-2-small table (3.673029 GB) scaled by the parameter ratio 54.15
+# (profiles/adamw_multi_tensor_gpt2_small_table.md).  Must go back to None whenever
+# the kernel changes until it is captured again.
+ADAMW_TRAFFIC_PER_LAUNCH = 198.89e9
 
 
 def time_extras(hp_path, reps, peak):
@@ -548,6 +551,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip timing the kernels outside the step (for profiler launch lists)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
     args = ap.parse_args(argv)
