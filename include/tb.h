@@ -74,6 +74,22 @@ int tb_version(void);
  */
 tb_status tb_device_error(int* code, int reset);
 
+/*
+ * tb_layernorm_bwd_selftest_timeout -- exercises that failure path without a
+ * GPU fault.  It runs the LayerNorm backward's bulk-copy ring kernel on a small
+ * internal problem (4 x 256 bf16, zeroed buffers the call allocates and frees)
+ * with its copies withheld, so that every wait on them runs out after
+ * wait_limit_ns nanoseconds; the kernel then sets the device error word to
+ * TB_ERR_TIMEOUT, waits (bounded as well) for the copies it would have issued,
+ * and returns.  Nothing is in flight when it returns, so the context stays
+ * usable.  The call synchronises `stream`; afterwards tb_device_error reports
+ * TB_ERR_TIMEOUT.
+ *   wait_limit_ns  1,000 .. 1,000,000,000
+ * Returns TB_OK once the kernel has finished, TB_ERR_INVALID_VALUE (limit out of
+ * range), TB_ERR_OOM or TB_ERR_CUDA.
+ */
+tb_status tb_layernorm_bwd_selftest_timeout(int64_t wait_limit_ns, void* stream);
+
 /* ======================================================================== */
 /* Fused mixed-precision AdamW (multi-tensor)                               */
 /* ======================================================================== */
@@ -122,6 +138,10 @@ typedef struct tb_adamw_plan tb_adamw_plan;   /* opaque */
  *   out         receives the plan; the caller owns it and frees it with
  *               tb_adamw_plan_destroy.  The plan owns a device copy of the table
  *               (64 bytes per tensor) and remembers the current device.
+ *               Every call that takes a plan first looks it up among the plans
+ *               created and not yet destroyed; any other pointer (a destroyed
+ *               plan included) is rejected with TB_ERR_INVALID_VALUE without
+ *               being dereferenced.
  * Errors: TB_ERR_INVALID_VALUE (null param/m/v/grad with n > 0, copies given for
  * some tensors only, n < 0, n_tensors < 1,
  * out == NULL), TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_MISALIGNED, TB_ERR_ALIAS (any
@@ -179,8 +199,9 @@ tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t step,
                                 const tb_adamw_hparams* hp, float inv_loss_scale,
                                 const float* clip, void* stream);
 
-/* Free a plan (NULL is accepted).  Synchronises nothing: the caller must not
- * destroy a plan while a step that uses it may still be running. */
+/* Free a plan (NULL is accepted; a pointer that is not a live plan, e.g. one
+ * destroyed already, returns TB_ERR_INVALID_VALUE).  Synchronises nothing: the
+ * caller must not destroy a plan while a step that uses it may still be running. */
 tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan);
 
 /* ======================================================================== */

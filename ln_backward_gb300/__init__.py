@@ -11,7 +11,8 @@ from ._binding import (  # noqa: F401
     tb_adamw_grad_norm, tb_adamw_grad_norm_workspace_size, tb_adamw_plan_create,
     tb_adamw_plan_destroy, tb_adamw_step, tb_adamw_step_clipped, tb_cast_from_f32, tb_cast_to_f32,
     tb_device_error,
-    tb_layernorm_bwd, tb_layernorm_bwd_noalloc, tb_layernorm_bwd_workspace_size,
+    tb_layernorm_bwd, tb_layernorm_bwd_noalloc, tb_layernorm_bwd_selftest_timeout,
+    tb_layernorm_bwd_workspace_size,
     tb_rmsnorm_bwd, tb_rmsnorm_bwd_workspace_size, tb_softmax_bwd, tb_softmax_bwd_causal,
     tb_status_string, tb_version,
 )

@@ -29,7 +29,7 @@ EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_c
            "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd", "tb_layernorm_bwd_noalloc",
            "tb_softmax_bwd_causal", "tb_rmsnorm_bwd_workspace_size", "tb_rmsnorm_bwd",
            "tb_adamw_grad_norm_workspace_size", "tb_adamw_grad_norm", "tb_adamw_step_clipped",
-           "tb_cast_to_f32", "tb_cast_from_f32")
+           "tb_cast_to_f32", "tb_cast_from_f32", "tb_layernorm_bwd_selftest_timeout")
 
 
 class TbError(RuntimeError):
@@ -92,6 +92,8 @@ def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.tb_cast_to_f32.restype = i32
     lib.tb_cast_from_f32.argtypes = [vp, vp, i32, i64, vp]
     lib.tb_cast_from_f32.restype = i32
+    lib.tb_layernorm_bwd_selftest_timeout.argtypes = [i64, vp]
+    lib.tb_layernorm_bwd_selftest_timeout.restype = i32
     return lib
 
 
@@ -144,6 +146,13 @@ def tb_device_error(reset: bool = True) -> int:
     code = ctypes.c_int(0)
     _check("tb_device_error", lib.tb_device_error(ctypes.byref(code), int(reset)))
     return code.value
+
+
+def tb_layernorm_bwd_selftest_timeout(wait_limit_ns: int = 2_000_000, stream=None) -> None:
+    """Runs the LayerNorm ring kernel with its copies withheld so that its bounded
+    waits run out; synchronises. tb_device_error() then reports TB_ERR_TIMEOUT."""
+    _check("tb_layernorm_bwd_selftest_timeout",
+           lib.tb_layernorm_bwd_selftest_timeout(int(wait_limit_ns), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- AdamW

@@ -21,8 +21,10 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
+#include <mutex>
 #include <new>
 #include <type_traits>
+#include <unordered_set>
 #include <vector>
 
 #include "tb_common.cuh"
@@ -417,9 +419,36 @@ struct tb_adamw_plan {
     bool has_copy;   // the tensors have working copies (all of them, or none)
 };
 
-extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
-                                          tb_dtype grad_dtype, tb_dtype copy_dtype,
-                                          tb_adamw_plan** out) {
+namespace tb {
+namespace {
+// Plans handed out and not yet destroyed.  A handle is checked against this set
+// before it is dereferenced, so a destroyed or foreign pointer is rejected.
+std::mutex g_plans_mu;
+std::unordered_set<const tb_adamw_plan*> g_plans;
+
+bool plan_register(const tb_adamw_plan* p) {
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    try {
+        g_plans.insert(p);
+    } catch (...) {
+        return false;
+    }
+    return true;
+}
+bool plan_unregister(const tb_adamw_plan* p) {
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    return g_plans.erase(p) == 1;
+}
+bool plan_live(const tb_adamw_plan* p) {
+    if (!p) return false;
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    return g_plans.count(p) == 1 && p->magic == kPlanMagic;
+}
+}  // namespace
+}  // namespace tb
+
+static tb_status plan_create_impl(const tb_tensor_desc* tensors, int n_tensors,
+                                  tb_dtype grad_dtype, tb_dtype copy_dtype, tb_adamw_plan** out) {
     using namespace tb;
     if (!out || !tensors || n_tensors < 1) return TB_ERR_INVALID_VALUE;
     *out = nullptr;
@@ -515,15 +544,30 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
         delete plan;
         return TB_ERR_CUDA;
     }
+    if (!plan_register(plan)) {
+        cudaFree(plan->d_table);
+        delete plan;
+        return TB_ERR_OOM;
+    }
     *out = plan;
     return TB_OK;
+}
+
+extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
+                                          tb_dtype grad_dtype, tb_dtype copy_dtype,
+                                          tb_adamw_plan** out) {
+    try {
+        return plan_create_impl(tensors, n_tensors, grad_dtype, copy_dtype, out);
+    } catch (...) {   // host allocation of the table failed
+        return TB_ERR_OOM;
+    }
 }
 
 namespace tb {
 namespace {
 tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adamw_hparams* hp,
                           float inv_loss_scale, const float* clip, void* stream) {
-    if (!plan || !hp || plan->magic != kPlanMagic) return TB_ERR_INVALID_VALUE;
+    if (!hp || !plan_live(plan)) return TB_ERR_INVALID_VALUE;
     if (step < 1) return TB_ERR_INVALID_VALUE;
     const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
     if (!std::isfinite(lr) || lr < 0.f) return TB_ERR_INVALID_VALUE;
@@ -583,7 +627,7 @@ extern "C" tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t st
 }
 
 extern "C" tb_status tb_adamw_grad_norm_workspace_size(const tb_adamw_plan* plan, size_t* bytes) {
-    if (!plan || !bytes || plan->magic != tb::kPlanMagic) return TB_ERR_INVALID_VALUE;
+    if (!bytes || !tb::plan_live(plan)) return TB_ERR_INVALID_VALUE;
     *bytes = tb::grad_norm_workspace(plan);
     return TB_OK;
 }
@@ -592,7 +636,7 @@ extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_los
                                         float max_norm, float* out, void* workspace,
                                         size_t workspace_bytes, void* stream) {
     using namespace tb;
-    if (!plan || !out || plan->magic != kPlanMagic) return TB_ERR_INVALID_VALUE;
+    if (!out || !plan_live(plan)) return TB_ERR_INVALID_VALUE;
     if (!std::isfinite(inv_loss_scale) || !(inv_loss_scale > 0.f)) return TB_ERR_INVALID_VALUE;
     if (std::isnan(max_norm)) return TB_ERR_INVALID_VALUE;
     if (!aligned_to(out, 4)) return TB_ERR_MISALIGNED;
@@ -626,7 +670,7 @@ extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_los
 
 extern "C" tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan) {
     if (!plan) return TB_OK;
-    if (plan->magic != tb::kPlanMagic) return TB_ERR_INVALID_VALUE;
+    if (!tb::plan_unregister(plan)) return TB_ERR_INVALID_VALUE;
     plan->magic = 0;
     tb_status st = TB_OK;
     if (plan->d_table && cudaFree(plan->d_table) != cudaSuccess) st = TB_ERR_CUDA;

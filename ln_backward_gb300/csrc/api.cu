@@ -1,6 +1,8 @@
 // api.cu -- status strings, version, per-device property cache and the
 // device-side error word.
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "tb_common.cuh"
 
@@ -46,6 +48,40 @@ int* device_error_word() {
         g_err_ptr[dev] = static_cast<int*>(p);
     }
     return g_err_ptr[dev];
+}
+
+namespace {
+std::mutex g_occ_mu;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_occ;   // -> CTAs per SM
+std::map<std::pair<int, const void*>, size_t> g_smem_limit;        // -> limit set so far
+}  // namespace
+
+int resident_ctas_per_sm(const void* kernel, int threads, size_t dyn_smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    try {
+        const auto key = std::make_tuple(dev, kernel, threads, dyn_smem);
+        const auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+        if (dyn_smem > 48 * 1024) {
+            size_t& lim = g_smem_limit[std::make_pair(dev, kernel)];
+            if (lim < dyn_smem) {
+                if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)dyn_smem) != cudaSuccess)
+                    return 0;
+                lim = dyn_smem;
+            }
+        }
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) !=
+            cudaSuccess)
+            return 0;
+        g_occ.emplace(key, per_sm);
+        return per_sm;
+    } catch (...) {
+        return 0;
+    }
 }
 
 }  // namespace tb

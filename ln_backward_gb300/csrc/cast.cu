@@ -77,11 +77,12 @@ cast_from_f32_kernel(const float* __restrict__ src, void* __restrict__ dst, int6
     for (int64_t i = done + tid; i < n; i += stride) d[i] = D::from_f32(src[i]);
 }
 
+// 0 when the occupancy query failed.
 unsigned grid_for(const void* kernel, int64_t n, int sms) {
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+    const int per_sm = resident_ctas_per_sm(kernel, kThreads, 0);
+    if (per_sm == 0) return 0;
     const int64_t want = (n / 8 + kThreads - 1) / kThreads + 1;
-    return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1)));
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * per_sm));
 }
 
 }  // namespace
@@ -106,8 +107,8 @@ extern "C" tb_status tb_cast_to_f32(const void* src, tb_dtype src_dtype, float s
                   : src_dtype == TB_F16  ? reinterpret_cast<const void*>(&cast_to_f32_kernel<F16>)
                                          : reinterpret_cast<const void*>(&cast_to_f32_kernel<F32>);
     void* args[] = {&src, &dst, &n, &scale, &vec};
-    if (cudaLaunchKernel(k, dim3(grid_for(k, n, info.sm_count)), dim3(kThreads), args, 0, st) !=
-        cudaSuccess)
+    const unsigned grid = grid_for(k, n, info.sm_count);
+    if (grid == 0 || cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, st) != cudaSuccess)
         return TB_ERR_CUDA;
     return TB_OK;
 }
@@ -129,8 +130,8 @@ extern "C" tb_status tb_cast_from_f32(const float* src, void* dst, tb_dtype dst_
     const void* k = dst_dtype == TB_BF16 ? reinterpret_cast<const void*>(&cast_from_f32_kernel<BF16>)
                                          : reinterpret_cast<const void*>(&cast_from_f32_kernel<F16>);
     void* args[] = {&src, &dst, &n, &vec};
-    if (cudaLaunchKernel(k, dim3(grid_for(k, n, info.sm_count)), dim3(kThreads), args, 0, st) !=
-        cudaSuccess)
+    const unsigned grid = grid_for(k, n, info.sm_count);
+    if (grid == 0 || cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, st) != cudaSuccess)
         return TB_ERR_CUDA;
     return TB_OK;
 }

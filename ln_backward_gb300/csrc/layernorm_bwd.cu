@@ -86,13 +86,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Wait for the phase with this parity to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for the phase with this parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1; it < (1u << 30); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
@@ -252,7 +253,8 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
                         const float* __restrict__ mean, const float* __restrict__ inv_std,
                         const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
                         float* __restrict__ partials, int64_t rows, int D, int stages,
-                        int64_t rows_per_cta, int* err) {
+                        int64_t rows_per_cta, int* err, unsigned long long wait_limit_ns,
+                        int withhold_copies) {
     using T = typename Fmt::T;
     constexpr int E = Vec<Fmt>::kElems;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -283,6 +285,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         const uint32_t bar = smem_addr(&bars[s]);
         unsigned char* st = ring + (size_t)s * 2 * grp_bytes;
         mbar_arrive_expect_tx(bar, 2 * bytes);
+        if (withhold_copies) return;   // self-test: the stage's barrier never completes
         bulk_g2s(smem_addr(st), x + first * D, bytes, bar, pol);
         bulk_g2s(smem_addr(st + grp_bytes), dY + first * D, bytes, bar, pol);
     };
@@ -330,7 +333,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
             mu_n[i] = (!kRms && has) ? mean[rn] : 0.f;
             rs_n[i] = has ? inv_std[rn] : 0.f;
         }
-        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity);
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity, wait_limit_ns);
         const unsigned char* st = ring + (size_t)s * 2 * grp_bytes;
 
         // Phase 1: the two sums of every row of the group, from the staged rows.
@@ -432,7 +435,8 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         if (tid == 0) {
             atomicExch(err, (int)TB_ERR_TIMEOUT);
             for (int64_t q = fail_at; q < issued; ++q)
-                mbar_wait_bounded(smem_addr(&bars[q % stages]), (uint32_t)((q / stages) & 1));
+                mbar_wait_bounded(smem_addr(&bars[q % stages]), (uint32_t)((q / stages) & 1),
+                                  wait_limit_ns);
         }
         __syncthreads();
         return;
@@ -585,6 +589,8 @@ struct LnPlan {
     size_t smem;     // dynamic shared memory (ring path)
     int grid;        // CTAs of the row kernel == partial rows in the workspace
     int64_t rows_per_cta;
+    unsigned long long wait_limit_ns = kWaitLimitNs;   // bound of every wait (ring path)
+    int withhold_copies = 0;   // self-test only: issue no copies, so every wait runs out
 };
 
 // Largest NV instantiated: kMaxElemsPerThread columns per thread.
@@ -671,33 +677,26 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
             (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
         const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
         if ((int64_t)smem <= info.max_smem_optin) {
-            const void* k = ring_kernel(dt, nv, r, rms);
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-                cudaSuccess)
-                return false;
-            int per_sm = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) != cudaSuccess)
-                return false;
+            const int per_sm = resident_ctas_per_sm(ring_kernel(dt, nv, r, rms), threads, smem);
+            if (per_sm == 0) return false;
             p->path = Path::kRing;
             p->threads = threads;
             p->nv = nv;
             p->r = r;
             p->stages = stages;
             p->smem = smem;
-            p->grid = info.sm_count * std::max(per_sm, 1);
+            p->grid = info.sm_count * per_sm;
         }
     }
     if (p->path == Path::kPlain) {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plain_kernel(dt, rms), kRowThreads, 0) !=
-            cudaSuccess)
-            return false;
+        const int per_sm = resident_ctas_per_sm(plain_kernel(dt, rms), kRowThreads, 0);
+        if (per_sm == 0) return false;
         p->threads = kRowThreads;
         p->nv = 0;
         p->r = 0;
         p->stages = 0;
         p->smem = 0;
-        p->grid = info.sm_count * std::min(std::max(per_sm, 1), 2);
+        p->grid = info.sm_count * std::min(per_sm, 2);
     }
     p->grid = (int)std::min<int64_t>(p->grid, rows);
     p->rows_per_cta = p->grid > 0 ? (rows + p->grid - 1) / p->grid : 0;
@@ -717,7 +716,8 @@ struct RingLaunchOps {
                        const float* inv_std, const float* gamma, T* dx, float* ws, int64_t rows,
                        int D, int* err, cudaStream_t st) {
             ln_bwd_rows_ring_kernel<Fmt, NV, R, kRms><<<p.grid, p.threads, p.smem, st>>>(
-                dy, x, mean, inv_std, gamma, dx, ws, rows, D, p.stages, p.rows_per_cta, err);
+                dy, x, mean, inv_std, gamma, dx, ws, rows, D, p.stages, p.rows_per_cta, err,
+                p.wait_limit_ns, p.withhold_copies);
             return 0;
         }
     };
@@ -981,4 +981,44 @@ extern "C" tb_status tb_rmsnorm_bwd(const void* dY, const void* x, const float* 
     }
     if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
     return launch_colsum(ws, p.grid, D, D, dgamma, nullptr, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ self-test of the bounded waits
+extern "C" tb_status tb_layernorm_bwd_selftest_timeout(int64_t wait_limit_ns, void* stream) {
+    using namespace tb;
+    if (wait_limit_ns < 1000 || wait_limit_ns > (int64_t)kWaitLimitNs) return TB_ERR_INVALID_VALUE;
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    constexpr int64_t kRows = 4, kD = 256;
+    LnPlan p;
+    if (!make_plan(kRows, kD, TB_BF16, true, info, &p) || p.path != Path::kRing) return TB_ERR_CUDA;
+    p.wait_limit_ns = (unsigned long long)wait_limit_ns;
+    p.withhold_copies = 1;
+    int* err = device_error_word();
+    if (!err) return TB_ERR_CUDA;
+    // One zeroed allocation holds x, dY, dX, mean, inv_std, gamma and the workspace,
+    // each part starting on a 256-byte boundary.
+    const size_t mat = (size_t)kRows * kD * sizeof(uint16_t);
+    const size_t off_dy = mat, off_dx = 2 * mat, off_mu = 3 * mat, off_rs = off_mu + 256;
+    const size_t off_g = off_rs + 256, off_ws = off_g + (size_t)kD * sizeof(float);
+    const size_t total = off_ws + workspace_bytes_for(p, kD);
+    unsigned char* buf = nullptr;
+    if (cudaMalloc(&buf, total) != cudaSuccess) {
+        cudaGetLastError();
+        return TB_ERR_OOM;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    tb_status status = TB_OK;
+    if (cudaMemsetAsync(buf, 0, total, st) != cudaSuccess) {
+        status = TB_ERR_CUDA;
+    } else {
+        launch_rows<BF16>(p, buf + off_dy, buf, reinterpret_cast<float*>(buf + off_mu),
+                          reinterpret_cast<float*>(buf + off_rs), reinterpret_cast<float*>(buf + off_g),
+                          buf + off_dx, reinterpret_cast<float*>(buf + off_ws), kRows, kD, err, st);
+        if (cudaGetLastError() != cudaSuccess) status = TB_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(st) != cudaSuccess) status = TB_ERR_CUDA;
+    if (cudaFree(buf) != cudaSuccess) status = TB_ERR_CUDA;
+    return status;
 }

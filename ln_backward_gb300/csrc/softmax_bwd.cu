@@ -206,11 +206,11 @@ template <class Fmt, int G, int VPL>
 tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, int nv,
                        int64_t period, int64_t offset, int sms, cudaStream_t st) {
     constexpr int kRowsPerCta = 256 / G;
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, reinterpret_cast<const void*>(&softmax_bwd_group_kernel<Fmt, G, VPL>), 256, 0);
+    const int per_sm = resident_ctas_per_sm(
+        reinterpret_cast<const void*>(&softmax_bwd_group_kernel<Fmt, G, VPL>), 256, 0);
+    if (per_sm == 0) return TB_ERR_CUDA;
     const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * std::max(per_sm, 1)));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * per_sm));
     softmax_bwd_group_kernel<Fmt, G, VPL><<<(unsigned)grid, 256, 0, st>>>(
         static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv, period, offset);
     return launch_status();
@@ -219,10 +219,10 @@ tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, in
 template <class Fmt, int VPL>
 tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int nv,
                      int64_t period, int64_t offset, int sms, cudaStream_t st) {
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, VPL>), kCtaThreads, 0);
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * std::max(per_sm, 1)));
+    const int per_sm = resident_ctas_per_sm(
+        reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, VPL>), kCtaThreads, 0);
+    if (per_sm == 0) return TB_ERR_CUDA;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * per_sm));
     softmax_bwd_cta_kernel<Fmt, VPL><<<(unsigned)grid, kCtaThreads, 0, st>>>(
         static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv,
         period, offset);
@@ -247,10 +247,10 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
         return launch_cta<Fmt, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
     }
     using T = typename Fmt::T;
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, reinterpret_cast<const void*>(&softmax_bwd_twopass_kernel<Fmt>), kTwoPassThreads, 0);
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * std::max(per_sm, 1)));
+    const int per_sm = resident_ctas_per_sm(
+        reinterpret_cast<const void*>(&softmax_bwd_twopass_kernel<Fmt>), kTwoPassThreads, 0);
+    if (per_sm == 0) return TB_ERR_CUDA;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * per_sm));
     softmax_bwd_twopass_kernel<Fmt><<<(unsigned)grid, kTwoPassThreads, 0, st>>>(
         static_cast<const T*>(dY), static_cast<const T*>(P), static_cast<T*>(dX), rows, cols, period,
         offset);

@@ -48,6 +48,12 @@ bool current_device_info(int* device, DeviceInfo* info);
 // Address of the device-side error word on the current device (nullptr on error).
 int* device_error_word();
 
+// CTAs of `kernel` that fit on one SM of the current device with `threads`
+// threads and `dyn_smem` bytes of dynamic shared memory (0 on a CUDA error).
+// First raises the kernel's dynamic shared-memory limit to dyn_smem when that
+// is above the default; results are cached per (device, kernel, threads, smem).
+int resident_ctas_per_sm(const void* kernel, int threads, size_t dyn_smem);
+
 inline tb_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }

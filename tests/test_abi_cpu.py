@@ -115,6 +115,20 @@ def test_adamw_step_rejects_null_plan(tb):
     assert lib.tb_adamw_plan_destroy(None) == TB_OK
 
 
+def test_pointers_that_are_not_live_plans_are_never_dereferenced(tb):
+    """Handles are looked up among the live plans first: a pointer that was never a
+    plan (here an address with nothing mapped behind it) is rejected, not read."""
+    lib = tb._binding.lib
+    hp = tb._binding.tb_adamw_hparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    bogus = ctypes.c_void_p(0x1000)
+    size = ctypes.c_size_t(0)
+    assert lib.tb_adamw_step(bogus, 1, ctypes.byref(hp), 1.0, None) == INVALID
+    assert lib.tb_adamw_step_clipped(bogus, 1, ctypes.byref(hp), 1.0, 0x2000, None) == INVALID
+    assert lib.tb_adamw_grad_norm_workspace_size(bogus, ctypes.byref(size)) == INVALID
+    assert lib.tb_adamw_grad_norm(bogus, 1.0, 1.0, 0x2000, 0x3000, 64, None) == INVALID
+    assert lib.tb_adamw_plan_destroy(bogus) == INVALID
+
+
 # ----------------------------------------------------------------------------- LayerNorm
 def _ln(tb, dY, x, mean, rstd, gamma, dX, dg, db, rows, D, dt, ws, wsb):
     return tb._binding.lib.tb_layernorm_bwd(dY, x, mean, rstd, gamma, dX, dg, db, rows, D, dt,
@@ -177,3 +191,9 @@ def test_cast_validation(tb):
     assert lib.tb_cast_from_f32(A, B, F32, 4, None) == DTYPE
     assert lib.tb_cast_from_f32(A, A + 2, BF16, 4, None) == ALIAS
     assert lib.tb_cast_from_f32(None, B, BF16, 4, None) == INVALID
+
+
+def test_selftest_limit_validation(tb):
+    lib = tb._binding.lib
+    for bad in (-1, 0, 999, 1_000_000_001):
+        assert lib.tb_layernorm_bwd_selftest_timeout(bad, None) == INVALID
