@@ -184,7 +184,8 @@ __device__ __forceinline__ bool multi_writer(int lane) {
 }
 
 // One 16-byte shared-memory vector as E/2 fp32 pairs (packed f32x2 math below).
-// bf16 widens exactly with a shift / mask; fp16 with the half2 conversion.
+// bf16 widens exactly by moving its bits to the high half (a byte permute for the
+// low element, a mask for the high one); fp16 with the half2 conversion.
 template <class Fmt>
 struct Pairs {
     static constexpr int kN = Vec<Fmt>::kElems / 2;
@@ -204,7 +205,8 @@ __device__ __forceinline__ void lds_pairs<BF16>(const void* p, float2 (&f)[4]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+        f[i] = make_float2(__uint_as_float(__byte_perm(w[i], 0u, 0x1044)),
+                           __uint_as_float(w[i] & 0xffff0000u));
 }
 template <>
 __device__ __forceinline__ void lds_pairs<F16>(const void* p, float2 (&f)[4]) {
