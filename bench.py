@@ -543,13 +543,15 @@ def _oracle_rates(adamw_n, sm_rows, ln_rows, reps=1):
             t_l / (reps * ln_rows * LN_D), t_a + t_s + t_l)
 
 
+LLAMA7B_PARAMS = 6_738_415_616
+FULL_STEP_BYTES = (adamw_bytes(LLAMA7B_PARAMS) + softmax_bytes(SM_ROWS, SM_COLS, 4)
+                   + softmax_bytes(SM_ROWS, SM_COLS, 2) + layernorm_bytes(LN_ROWS, LN_D, 2))
+
+
 def _full_step_equivalent(per_param, per_sm, per_ln):
     """GB/s of the full workload at the oracle's per-unit speeds (single thread)."""
-    n = 6_738_415_616
-    t = (n * per_param + 2 * SM_ROWS * SM_COLS * per_sm + LN_ROWS * LN_D * per_ln)
-    b = (adamw_bytes(n) + softmax_bytes(SM_ROWS, SM_COLS, 4) + softmax_bytes(SM_ROWS, SM_COLS, 2)
-         + layernorm_bytes(LN_ROWS, LN_D, 2))
-    return b / t / 1e9, t
+    t = (LLAMA7B_PARAMS * per_param + 2 * SM_ROWS * SM_COLS * per_sm + LN_ROWS * LN_D * per_ln)
+    return FULL_STEP_BYTES / t / 1e9, t
 
 
 def cpu_baseline(seconds_budget=15.0):
@@ -590,9 +592,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_full * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": ("Llama-7B-shaped fused AdamW + softmax bwd 98,304x1,024 fp32 and "
-                                "bf16 + LayerNorm bwd 16,384x4,096 bf16 (per-unit oracle times "
-                                "on bounded samples, scaled to the full step)")},
+        "config": {"workload": WORKLOAD_TEXT["full"],
+                   "bytes_per_step": FULL_STEP_BYTES,
+                   "parallelism": f"replicas x{world}",
+                   "sampling": "per-unit oracle times on bounded samples, scaled to the full step"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": (f"each step: 2^22-param AdamW slice, {sm_rows}x1024 softmax, "
                                     f"{ln_rows}x4096 LayerNorm; {wall:.1f} s wall for the timed steps")},
