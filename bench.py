@@ -384,6 +384,7 @@ def time_extras(hp_path, reps, peak):
     import torch
     out = {}
     for name, (fn, nbytes) in hp_path.extras().items():
+        torch.cuda.nvtx.range_push(name)     # lets a profiler pick this kernel's launches
         for _ in range(3):
             fn()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -393,6 +394,7 @@ def time_extras(hp_path, reps, peak):
             fn()
         e.record()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         ms = reduce_over_ranks([s.elapsed_time(e) / reps], "max")[0]
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"ms": round(ms, 4), "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),

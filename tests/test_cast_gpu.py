@@ -41,10 +41,14 @@ def _src(n, dtype, offset=0, seed=0):
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32],
                          ids=["f16", "bf16", "f32"])
 @pytest.mark.parametrize("n", [1, 7, 8, 9, 1000, (1 << 20) + 3])
-@pytest.mark.parametrize("offset", [0, 1])
-def test_cast_to_f32_bit_exact(tb, dtype, n, offset):
-    src = _src(n, dtype, offset, seed=n)
-    dst = torch.full((n + offset,), float("nan"), device="cuda")[offset:]
+# (source offset, destination offset) in elements: both aligned for the 32-byte store
+# path; a 16- but not 32-byte aligned destination for the 16-byte path (the bf16/fp16
+# source offset of 8 keeps it 16-byte aligned); both misaligned for the scalar path
+@pytest.mark.parametrize("offsets", [(0, 0), (8, 4), (1, 1)], ids=["v32", "v16", "scalar"])
+def test_cast_to_f32_bit_exact(tb, dtype, n, offsets):
+    so, do = offsets
+    src = _src(n, dtype, so, seed=n)
+    dst = torch.full((n + do,), float("nan"), device="cuda")[do:]
     tb.tb_cast_to_f32(src, dst, scale=1 / 1024.0)
     raw = src.view(torch.int32 if dtype == torch.float32 else torch.int16).cpu().numpy()
     ref = oracle.cast_to_f32(raw.view(np.float32 if dtype == torch.float32 else np.uint16),
