@@ -176,8 +176,9 @@ tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
  *     out[0] = norm   = sqrt(sum_i (float(grad_i) * inv_loss_scale)^2)
  *     out[1] = factor = max_norm / norm if max_norm > 0 and norm > max_norm, else 1
  *     out[2] = 1 if any gradient element is NaN or infinite, else 0
- * Per-thread sums are fp32 over at most 64 squares and fp64 beyond; the CTA
- * partials are added in a fixed order, so the result is reproducible.
+ * Each thread adds its squares in fp32 in rounds of at most 32, adds the round
+ * sums of one tile (at most 256 squares) in fp32 and the tile sums in fp64; the
+ * CTA partials are added in a fixed order, so the result is reproducible.
  *   workspace  device scratch of tb_adamw_grad_norm_workspace_size() bytes,
  *              8-byte aligned (one fp64 partial and one flag per CTA)
  * Errors: TB_ERR_INVALID_VALUE, TB_ERR_MISALIGNED, TB_ERR_WORKSPACE, TB_ERR_ALIAS,

@@ -36,6 +36,9 @@ constexpr int kUnit = 8;        // elements per unit
 constexpr int kThreads = 256;   // threads per CTA
 constexpr int kUnroll = 2;      // units in flight per thread
 constexpr int64_t kTileUnits = (int64_t)kThreads * kUnroll * 4;   // 16384 elements
+// The gradient-norm pass reads 2 bytes per element instead of 30: it takes 4x
+// longer tiles (65,536 elements) so a CTA spends less of its time between tiles.
+constexpr int64_t kNormTileUnits = 4 * kTileUnits;
 constexpr uint64_t kPlanMagic = 0x7462616461707731ull;
 
 struct alignas(16) TensorEntry {
@@ -249,10 +252,11 @@ adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t
 }
 
 // ------------------------------------------------------------------ gradient norm
-// Sum of squares of the unscaled gradient over every tensor (same tiles as the
-// step, reading only the 16-bit gradient), plus a non-finite flag.  Each thread
-// adds a tile's squares in fp32 and the tile sums in fp64; each CTA writes one
-// fp64 partial and one flag; the finalize kernel adds the partials in order.
+// Sum of squares of the unscaled gradient over every tensor (reading only the
+// gradient), plus a non-finite flag.  Each thread adds its squares in fp32 in
+// rounds of at most 32, the round sums of a tile in fp32 and the tile sums in
+// fp64; each CTA writes one fp64 partial and one flag; the finalize kernel adds
+// the partials in order.
 template <class G>
 __global__ void __launch_bounds__(kThreads)
 adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
@@ -263,8 +267,8 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
     int bad = 0;
     int k = 0;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const int64_t u_lo = tile * kTileUnits;
-        const int64_t u_hi = u_lo + kTileUnits < total_units ? u_lo + kTileUnits : total_units;
+        const int64_t u_lo = tile * kNormTileUnits;
+        const int64_t u_hi = u_lo + kNormTileUnits < total_units ? u_lo + kNormTileUnits : total_units;
         k = tensor_of(tab, ntab, k, u_lo);
         float fs = 0.f;
         int kk = k;
@@ -293,6 +297,8 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
                                 r[j][1] = in ? ld_stream_f4(gf + uu * kUnit + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
 #pragma unroll
+                            float f1 = 0.f;   // the 32 squares of this round
+#pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const float v[8] = {r[j][0].x, r[j][0].y, r[j][0].z, r[j][0].w,
                                                     r[j][1].x, r[j][1].y, r[j][1].z, r[j][1].w};
@@ -300,9 +306,10 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
                                 for (int q = 0; q < 8; ++q) {
                                     bad |= !isfinite(v[q]);
                                     const float x = v[q] * inv_s;
-                                    fs += x * x;
+                                    f1 += x * x;
                                 }
                             }
+                            fs += f1;
                         }
                     } else
                     for (int64_t u0 = a + threadIdx.x; u0 < fe; u0 += 4 * kThreads) {
@@ -312,6 +319,7 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
                             const int64_t uu = u0 + (int64_t)j * kThreads;
                             r[j] = uu < fe ? ld_stream_u4(gp + uu * kUnit) : make_uint4(0u, 0u, 0u, 0u);
                         }
+                        float f1 = 0.f;   // the 32 squares of this round
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             float v[8];
@@ -320,18 +328,25 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
                             for (int q = 0; q < 8; ++q) {
                                 bad |= !isfinite(v[q]);
                                 const float x = v[q] * inv_s;
-                                fs += x * x;
+                                f1 += x * x;
                             }
                         }
+                        fs += f1;
                     }
                     lo_elem = fe > a ? fe * kUnit : lo_elem;   // scalar tail only
                 }
-                for (int64_t i = lo_elem + threadIdx.x; i < hi_elem; i += kThreads) {
+                float f1 = 0.f;
+                for (int64_t i = lo_elem + threadIdx.x, c = 1; i < hi_elem; i += kThreads, ++c) {
                     const float g = G::to_f32(gp[i]);
                     bad |= !isfinite(g);
                     const float x = g * inv_s;
-                    fs += x * x;
+                    f1 += x * x;
+                    if ((c & 31) == 0) {   // 32 squares per first-level sum here too
+                        fs += f1;
+                        f1 = 0.f;
+                    }
                 }
+                fs += f1;
             }
             u = seg_hi > u ? seg_hi : u;
             ++kk;
@@ -649,7 +664,7 @@ extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_los
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     double* part = static_cast<double*>(workspace);
     int* flags = reinterpret_cast<int*>(part + plan->norm_grid);
-    const int64_t n_tiles = (plan->total_units + kTileUnits - 1) / kTileUnits;
+    const int64_t n_tiles = (plan->total_units + kNormTileUnits - 1) / kNormTileUnits;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(plan->norm_grid, n_tiles));
     if (plan->total_units > 0) {
         const TensorEntry* tab = plan->d_table;

@@ -4,7 +4,8 @@ tb_adamw_grad_norm (global L2 norm of the unscaled gradient, clip factor,
 non-finite flag, all left on the device) and tb_adamw_step_clipped (the fused
 AdamW step reading that factor on the device, skipping the update on a
 non-finite gradient).  Tolerances: the norm and factor within 1e-5 relative
-(fp32 partial sums over at most 64 squares, fp64 beyond); the clipped step within
+(fp32 rounds of at most 32 squares, fp32 over a tile's rounds, fp64 beyond: a
+worst-case relative error of about 40 fp32 ulps); the clipped step within
 the AdamW targets (theta/m/v 1e-5 floored relative, copy exact RNE of the master).
 """
 import numpy as np
