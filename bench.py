@@ -607,6 +607,69 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_layernorm_sweep(args):
+    """LayerNorm (and RMSNorm) backward at D = 4096 over a range of row counts, and a
+    least-squares fit time = bytes / BW + F that separates the streaming rate from the
+    fixed cost of a call.  One JSON line per dtype; not part of the benchmark contract."""
+    import numpy as np
+    import torch
+    import ln_backward_gb300 as tb
+    from ln_backward_gb300 import synth
+    dev = torch.device("cuda")
+    D = LN_D
+
+    def best_ms(fn, reps=30):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(3):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(reps):
+                fn()
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e) / reps)
+        return best
+
+    for op in ("layernorm", "rmsnorm"):
+        for dt in (torch.bfloat16, torch.float32):
+            es = torch.empty((), dtype=dt).element_size()
+            pts = []
+            for rows in (2048, 4096, 8192, 16384, 32768, 65536, 131072):
+                dg = torch.empty(D, device=dev)
+                if op == "layernorm":
+                    x, dy, mu, rs, g = synth.layernorm_inputs(rows, D, dt, 3, dev, dy_std=1e-2)
+                    dX, db = torch.empty_like(x), torch.empty(D, device=dev)
+                    ws = torch.empty(tb.tb_layernorm_bwd_workspace_size(rows, D, dt),
+                                     dtype=torch.uint8, device=dev)
+                    fn = lambda: tb.tb_layernorm_bwd(dy, x, mu, rs, g, dX, dg, db, ws)
+                    nbytes = layernorm_bytes(rows, D, es)
+                else:
+                    x, dy, inv, g = synth.rmsnorm_inputs(rows, D, dt, 4, dev, dy_std=1e-2)
+                    dX = torch.empty_like(x)
+                    ws = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(rows, D, dt),
+                                     dtype=torch.uint8, device=dev)
+                    fn = lambda: tb.tb_rmsnorm_bwd(dy, x, inv, g, dX, dg, ws)
+                    nbytes = rmsnorm_bytes(rows, D, es)
+                ms = best_ms(fn)
+                pts.append((rows, nbytes, ms))
+                del x, dy, dX, ws
+                torch.cuda.empty_cache()
+            A = np.array([[b, 1.0] for _, b, _ in pts])
+            (inv_bw, fixed), *_ = np.linalg.lstsq(A, np.array([ms * 1e-3 for _, _, ms in pts]),
+                                                  rcond=None)
+            print(json.dumps({
+                "sweep": f"{op}_bwd", "dtype": str(dt).replace("torch.", ""), "D": D,
+                "points": [{"rows": r, "us": round(ms * 1e3, 1), "GB_s": round(b / ms / 1e6, 1)}
+                           for r, b, ms in pts],
+                "fit_streaming_GB_s": round(1.0 / inv_bw / 1e9, 1),
+                "fit_fixed_us": round(fixed * 1e6, 2)}))
+    if tb.tb_device_error(reset=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during the sweep")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -619,10 +682,15 @@ def main(argv=None):
                     help="skip timing the kernels outside the step (for profiler launch lists)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
+    ap.add_argument("--sweep-layernorm", action="store_true",
+                    help="time the LayerNorm/RMSNorm backward over row counts and fit "
+                         "bytes/BW + fixed cost (one JSON line per op and dtype)")
     args = ap.parse_args(argv)
     if args.warmup < 1:
         ap.error("--warmup must be >= 1 (timed numbers use the default of 3)")
-    if args.impl == "reference":
+    if args.sweep_layernorm:
+        run_layernorm_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
