@@ -242,3 +242,27 @@ def test_step_argument_errors(tb, synth):
     with pytest.raises(tb.TbError):
         tb.tb_adamw_step(p, 1, inv_loss_scale=-1.0, **HP)
     p.close()
+
+
+def test_plan_of_empty_tensors_is_a_no_op(tb):
+    """A plan whose tensors all have n = 0: every call succeeds and launches nothing
+    that could fail; the gradient norm of nothing is 0 with a clip factor of 1."""
+    empty = [torch.empty(0, device="cuda") for _ in range(3)]
+    g = [torch.empty(0, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    c = [torch.empty(0, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    plan = tb.tb_adamw_plan_create(empty[:2], empty[1:3], empty[:2], g, c)
+    tb.tb_adamw_step(plan, 1, inv_loss_scale=1.0, **HP)
+    out = torch.full((3,), float("nan"), device="cuda")
+    ws = torch.empty(max(tb.tb_adamw_grad_norm_workspace_size(plan), 1), dtype=torch.uint8,
+                     device="cuda")
+    tb.tb_adamw_grad_norm(plan, 1.0, 1.0, out, ws)
+    tb.tb_adamw_step_clipped(plan, 1, inv_loss_scale=1.0, clip=out, **HP)
+    torch.cuda.synchronize()
+    assert out.tolist() == [0.0, 1.0, 0.0]
+    plan.close()
+    # nothing left behind: a following call still reports success
+    P = torch.full((4, 8), 0.125, device="cuda")
+    dX = torch.empty_like(P)
+    tb.tb_softmax_bwd(torch.ones_like(P), P, dX)
+    torch.cuda.synchronize()
+    assert torch.all(dX == 0)
