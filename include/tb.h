@@ -167,9 +167,10 @@ tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
 
 /*
  * Global gradient-norm clipping with a non-finite check, fused into the step
- * without a host synchronisation ([GPU-Opt-P2] §"完整训练循环（整合一切）", step
- * 7: the L2 norm of the unscaled gradient over all parameters; when it exceeds
- * max_norm the gradients are scaled by max_norm / norm before the optimizer).
+ * without a host synchronisation ([GPU-Opt-P2] §"完整训练循环（整合一切）", its
+ * gradient-clipping step: the L2 norm of the unscaled gradient over all
+ * parameters; when it exceeds max_norm the gradients are scaled by
+ * max_norm / norm before the optimizer).
  *
  * tb_adamw_grad_norm reads every gradient of the plan once (2 bytes per
  * parameter) and writes three floats to device memory `out`:
@@ -211,7 +212,8 @@ tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan);
 /*
  * The two casts of the pages' mixed-precision loop that the fused step does
  * internally ([GPU-Opt-P2] §"混合精度训练（FP16 / BF16）", §"完整训练循环（整合一切）"
- * steps 6 and 9), for callers that keep the optimizer steps apart:
+ * its unscale cast and its copy-back cast), for callers that keep the optimizer
+ * steps apart:
  *   tb_cast_to_f32   : dst[i] = float(src[i]) * scale (one fp32 rounding),
  *                      src in src_dtype (TB_F16, TB_BF16 or TB_F32), dst fp32
  *   tb_cast_from_f32 : dst[i] = round-to-nearest-even(src[i]) in dst_dtype

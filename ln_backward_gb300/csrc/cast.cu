@@ -1,10 +1,10 @@
 // cast.cu -- stand-alone precision casts of the mixed-precision training loop.
 //
 // "GPU 优化实战 Part 2：用 CUDA/ROCm 实现 LLM 反向传播与训练循环", sections
-// "混合精度训练（FP16 / BF16）" and "完整训练循环（整合一切）" (steps 6 and 9): the
-// low-precision gradient is cast to fp32 and multiplied by 1/loss_scale before
-// the optimizer, and the fp32 master weights are cast back to a 16-bit working
-// copy after it.  The fused AdamW step does both inside its single pass; these
+// "混合精度训练（FP16 / BF16）" and "完整训练循环（整合一切）" (the unscale cast and the
+// copy-back cast of the loop): the low-precision gradient is cast to fp32 and
+// multiplied by 1/loss_scale before the optimizer, and the fp32 master weights
+// are cast back to a 16-bit working copy after it.  The fused AdamW step does both inside its single pass; these
 // kernels exist for callers that keep the steps apart (and to time that unfused
 // pipeline against the fused one).
 //

@@ -364,9 +364,9 @@ void orc_rmsnorm_bwd_f64(int64_t rows, int64_t D,
 
 /* ------------------------------------------------------------------------- */
 /* Global gradient-norm clipping with a non-finite flag                       */
-/*   [GPU-Opt-P2] §"完整训练循环（整合一切）" step 7: the L2 norm of the       */
-/*   unscaled gradient over all parameters, then the gradients are scaled by  */
-/*   max_norm / norm when norm > max_norm, before the AdamW step.             */
+/*   [GPU-Opt-P2] §"完整训练循环（整合一切）", gradient clipping: the L2 norm */
+/*   of the unscaled gradient over all parameters, then the gradients are     */
+/*   scaled by max_norm / norm when norm > max_norm, before the AdamW step.  */
 /* ------------------------------------------------------------------------- */
 
 /* Sum of squares of the unscaled gradient over n elements, in double; sets
@@ -428,8 +428,8 @@ void orc_adamw_step_clipped_f64(int64_t n, double* theta, double* m, double* v,
 /* ------------------------------------------------------------------------- */
 /* Stand-alone casts of the mixed-precision loop                              */
 /*   [GPU-Opt-P2] §"混合精度训练（FP16 / BF16）" and §"完整训练循环（整合一切）"  */
-/*   steps 6 and 9: low-precision gradient -> fp32 times 1/loss_scale; fp32   */
-/*   master -> 16-bit working copy.                                            */
+/*   unscale and copy-back casts: low-precision gradient -> fp32 times        */
+/*   1/loss_scale; fp32 master -> 16-bit working copy.                         */
 /* ------------------------------------------------------------------------- */
 
 /* out = float(src * scale) with one rounding of the exact product (the product

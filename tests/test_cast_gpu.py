@@ -111,11 +111,11 @@ def test_unfused_pipeline_equals_fused_step_bitwise(tb, synth):
         synth.fill_grads(b, t)
         tb.tb_adamw_step(pa, t, inv_loss_scale=1 / 65536.0, **HP)
         sentinel = b.copy.clone()
-        tb.tb_cast_to_f32(b.grad, g32, scale=1 / 65536.0)          # step 6: cast + unscale
+        tb.tb_cast_to_f32(b.grad, g32, scale=1 / 65536.0)          # the loop's unscale cast
         tb.tb_adamw_step(pb, t, inv_loss_scale=1.0, **HP)         # step 8: fp32 AdamW, no copy
         torch.cuda.synchronize()
         assert torch.equal(b.copy, sentinel)                      # the step wrote no copy
-        tb.tb_cast_from_f32(b.theta, b.copy)                      # step 9: working copy
+        tb.tb_cast_from_f32(b.theta, b.copy)                      # the loop's copy-back cast
     torch.cuda.synchronize()
     for k in ("theta", "m", "v"):
         assert torch.equal(getattr(a, k), getattr(b, k)), k

@@ -1,4 +1,4 @@
-"""Pins for the oracle's stand-alone casts (training loop steps 6 and 9).
+"""Pins for the oracle's stand-alone casts (the training loop's unscale and copy-back casts).
 
 Both casts have a plain definition that library routines implement exactly:
 fp16/bf16 -> fp32 times a scale is one fp32 rounding of an exact product

@@ -1,7 +1,7 @@
 """Pins for the oracle's global gradient-norm clipping.
 
 Source: "GPU 优化实战 Part 2：用 CUDA/ROCm 实现 LLM 反向传播与训练循环", section
-"完整训练循环（整合一切）", step 7: the L2 norm of the unscaled gradient over all
+"完整训练循环（整合一切）", gradient clipping: the L2 norm of the unscaled gradient over all
 parameters; when it exceeds max_norm the gradients are multiplied by
 max_norm / norm before the optimizer step.
 
