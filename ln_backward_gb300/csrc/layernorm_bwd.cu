@@ -526,12 +526,13 @@ ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename 
 // partials: [G][W] fp32 (W = 2D for LayerNorm: dgamma then dbeta partials; W = D
 // for RMSNorm); out column c < D -> out_a (dgamma), else out_b (dbeta).
 // A CTA covers 32 columns with 32 warps: warp w sums partial rows w, w+32, ... in
-// ascending order, then the 32 warp sums are added in warp order.  The order never
+// ascending order, then the 32 warp sums are added in warp order.  Two CTAs fit
+// per SM (32 registers), so the whole grid is resident at once.  The order never
 // depends on timing, so the result is bitwise reproducible.
 constexpr int kColThreads = 1024;
 constexpr int kColGroups = kColThreads / 32;
 
-__global__ void __launch_bounds__(kColThreads)
+__global__ void __launch_bounds__(kColThreads, 2)
 ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t W, int64_t D,
                      float* __restrict__ dgamma, float* __restrict__ dbeta) {
     __shared__ float sm[kColGroups][33];
@@ -540,16 +541,17 @@ ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t W, int64
     const int64_t c = (int64_t)blockIdx.x * 32 + lane;
     float acc = 0.f;
     if (c < W) {
-        // eight loads in flight per round, added in ascending row order
-        for (int b = w; b < G; b += 8 * kColGroups) {
-            float v[8];
+        // ten loads in flight per round, added in ascending row order: one round
+        // covers the 320 partial rows of two CTAs per SM on 160 SMs
+        for (int b = w; b < G; b += 10 * kColGroups) {
+            float v[10];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < 10; ++q) {
                 const int bb = b + q * kColGroups;
                 v[q] = bb < G ? partials[(int64_t)bb * W + c] : 0.f;
             }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc += v[q];
+            for (int q = 0; q < 10; ++q) acc += v[q];
         }
     }
     sm[w][lane] = acc;
