@@ -372,11 +372,11 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-# Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload: the ncu
-# capture of the GPT-2-small table (3.673029 GB) scaled by the parameter ratio 54.15
-# (profiles/adamw_multi_tensor_gpt2_small_table.md).  Must go back to None whenever
-# the kernel changes until it is captured again.
-ADAMW_TRAFFIC_PER_LAUNCH = 198.89e9
+# Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, from
+# one single-pass ncu capture of the full step (94.345 GB read + 107.754 GB written;
+# profiles/dram_traffic_full_step_llama7b.md).  Must go back to None whenever the
+# kernel changes until it is captured again.
+ADAMW_TRAFFIC_PER_LAUNCH = 202.099929344e9
 
 
 def time_extras(hp_path, reps, peak):
