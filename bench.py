@@ -376,7 +376,7 @@ def run_ours(args):
 # one single-pass ncu capture of the full step (94.345 GB read + 107.754 GB written;
 # profiles/dram_traffic_full_step_llama7b.md).  Must go back to None whenever the
 # kernel changes until it is captured again.
-ADAMW_TRAFFIC_PER_LAUNCH = 202.099929344e9
+ADAMW_TRAFFIC_PER_LAUNCH = None
 
 
 def time_extras(hp_path, reps, peak):

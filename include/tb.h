@@ -65,9 +65,11 @@ int tb_version(void);
 /*
  * tb_device_error -- read (and optionally clear) the device-side error word of
  * the current device.  Kernels that wait on an mbarrier for their own bulk
- * copies give up after about one second; they then set this word to a nonzero
- * code, drain what they issued and return early (their outputs are then
- * undefined).  This call synchronises the current device.
+ * copies give up after about one second; they then set this word to
+ * TB_ERR_TIMEOUT, drain what they issued and return early (their outputs are
+ * then undefined).  tb_adamw_step_device sets it to TB_ERR_INVALID_VALUE when
+ * the step counter it reads is below 1.  This call synchronises the current
+ * device.
  *   code   out: 0 when no kernel gave up since the last reset
  *   reset  nonzero: clear the word after reading it
  * Returns TB_OK, TB_ERR_INVALID_VALUE (code == NULL) or TB_ERR_CUDA.
@@ -200,6 +202,24 @@ tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_loss_scale, fl
 tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t step,
                                 const tb_adamw_hparams* hp, float inv_loss_scale,
                                 const float* clip, void* stream);
+
+/*
+ * tb_adamw_step_device -- tb_adamw_step (clip == NULL) or tb_adamw_step_clipped
+ * (clip != NULL) with the step counter in device memory: the kernel reads t from
+ * `step` when it runs and forms the bias corrections 1 - beta^t itself (in
+ * double, rounded to fp32, as the host does for the other entry points).  With
+ * every per-step input on the device, a whole optimizer step -- counter
+ * increment, gradient norm, update -- can be captured once in a CUDA graph and
+ * replayed every iteration.  The counter is only read: the caller advances it.
+ *   step   device int64, 8-byte aligned; a value below 1 makes the kernel set the
+ *          device error word to TB_ERR_INVALID_VALUE and update nothing
+ *   clip   NULL, or the device output of tb_adamw_grad_norm
+ * Errors: as tb_adamw_step, plus TB_ERR_INVALID_VALUE (step == NULL) and
+ * TB_ERR_MISALIGNED.
+ */
+tb_status tb_adamw_step_device(const tb_adamw_plan* plan, const int64_t* step,
+                               const tb_adamw_hparams* hp, float inv_loss_scale,
+                               const float* clip, void* stream);
 
 /* Free a plan (NULL is accepted; a pointer that is not a live plan, e.g. one
  * destroyed already, returns TB_ERR_INVALID_VALUE).  Synchronises nothing: the

@@ -29,7 +29,8 @@ EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_c
            "tb_layernorm_bwd_workspace_size", "tb_layernorm_bwd", "tb_layernorm_bwd_noalloc",
            "tb_softmax_bwd_causal", "tb_rmsnorm_bwd_workspace_size", "tb_rmsnorm_bwd",
            "tb_adamw_grad_norm_workspace_size", "tb_adamw_grad_norm", "tb_adamw_step_clipped",
-           "tb_cast_to_f32", "tb_cast_from_f32", "tb_layernorm_bwd_selftest_timeout")
+           "tb_cast_to_f32", "tb_cast_from_f32", "tb_layernorm_bwd_selftest_timeout",
+           "tb_adamw_step_device")
 
 
 class TbError(RuntimeError):
@@ -92,6 +93,8 @@ def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.tb_cast_to_f32.restype = i32
     lib.tb_cast_from_f32.argtypes = [vp, vp, i32, i64, vp]
     lib.tb_cast_from_f32.restype = i32
+    lib.tb_adamw_step_device.argtypes = [vp, vp, ctypes.POINTER(tb_adamw_hparams), f32, vp, vp]
+    lib.tb_adamw_step_device.restype = i32
     lib.tb_layernorm_bwd_selftest_timeout.argtypes = [i64, vp]
     lib.tb_layernorm_bwd_selftest_timeout.restype = i32
     return lib
@@ -199,6 +202,20 @@ def tb_adamw_step(plan: AdamWPlan, step: int, lr: float, beta1: float, beta2: fl
     hp = tb_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
     _check("tb_adamw_step", lib.tb_adamw_step(plan.handle, int(step), ctypes.byref(hp),
                                               float(inv_loss_scale), _stream(stream)))
+
+
+def tb_adamw_step_device(plan: AdamWPlan, step: torch.Tensor, lr: float, beta1: float, beta2: float,
+                         eps: float, weight_decay: float, inv_loss_scale: float,
+                         clip: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The step counter is a 1-element int64 CUDA tensor, read when the kernel runs."""
+    if step.dtype != torch.int64 or step.numel() != 1 or not step.is_cuda:
+        raise ValueError("step must be a 1-element int64 CUDA tensor")
+    if clip is not None and (clip.dtype != torch.float32 or clip.numel() < 3):
+        raise ValueError("clip must hold 3 fp32 values")
+    hp = tb_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+    _check("tb_adamw_step_device",
+           lib.tb_adamw_step_device(plan.handle, _ptr(step), ctypes.byref(hp), float(inv_loss_scale),
+                                    _ptr(clip), _stream(stream)))
 
 
 def tb_adamw_plan_destroy(plan: AdamWPlan) -> None:

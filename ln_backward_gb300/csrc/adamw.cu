@@ -221,14 +221,34 @@ __device__ __forceinline__ int tensor_of(const TensorEntry* __restrict__ tab, in
 // clip (device memory, may be null): {norm, factor, nonfinite} as written by the
 // gradient-norm kernels; the gradient is multiplied by factor, and when nonfinite
 // is set the step is skipped (only the gradient is reset).
+// step_dev (device memory, may be null): the step t, read when the kernel runs;
+// the bias corrections are then formed here, as the host forms them otherwise
+// (1 - beta^t in double, rounded to fp32).  A t below 1 sets the error word to
+// TB_ERR_INVALID_VALUE and nothing is updated.
 template <class G, class C>
 __global__ void __launch_bounds__(kThreads, 2)
 adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
-                          int64_t n_tiles, Scalars s, const float* __restrict__ clip) {
+                          int64_t n_tiles, Scalars s, const float* __restrict__ clip,
+                          const int64_t* __restrict__ step_dev, int* err) {
     bool skip = false;
     if (clip) {
         s.clip = clip[1];
         skip = clip[2] != 0.0f;
+    }
+    if (step_dev) {
+        __shared__ float s_bc[2];
+        __shared__ int s_bad;
+        if (threadIdx.x == 0) {
+            const int64_t t = *step_dev;
+            s_bad = t < 1;
+            if (t < 1 && blockIdx.x == 0) atomicExch(err, (int)TB_ERR_INVALID_VALUE);
+            s_bc[0] = (float)(1.0 - pow((double)s.beta1, (double)t));
+            s_bc[1] = (float)(1.0 - pow((double)s.beta2, (double)t));
+        }
+        __syncthreads();
+        if (s_bad) return;
+        s.bc1 = s_bc[0];
+        s.bc2 = s_bc[1];
     }
     int k = 0;
     for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
@@ -580,9 +600,13 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
 
 namespace tb {
 namespace {
+// step_dev non-null: the step is read on the device when the kernel runs and
+// `step` is ignored.
 tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adamw_hparams* hp,
-                          float inv_loss_scale, const float* clip, void* stream) {
+                          float inv_loss_scale, const float* clip, const int64_t* step_dev,
+                          void* stream) {
     if (!hp || !plan_live(plan)) return TB_ERR_INVALID_VALUE;
+    if (step_dev) step = 1;   // placeholder for the host-side scalars below
     if (step < 1) return TB_ERR_INVALID_VALUE;
     const float lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, eps = hp->eps, wd = hp->weight_decay;
     if (!std::isfinite(lr) || lr < 0.f) return TB_ERR_INVALID_VALUE;
@@ -591,10 +615,13 @@ tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adam
     if (!std::isfinite(wd) || wd < 0.f) return TB_ERR_INVALID_VALUE;
     if (!std::isfinite(inv_loss_scale) || !(inv_loss_scale > 0.f)) return TB_ERR_INVALID_VALUE;
     if (clip && !aligned_to(clip, 4)) return TB_ERR_MISALIGNED;
+    if (step_dev && !aligned_to(step_dev, 8)) return TB_ERR_MISALIGNED;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return TB_ERR_CUDA;
     if (dev != plan->device) return TB_ERR_DEVICE;
     if (plan->total_units == 0) return TB_OK;
+    int* err = device_error_word();
+    if (!err) return TB_ERR_CUDA;
 
     Scalars s;
     s.lr = lr;
@@ -614,7 +641,7 @@ tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adam
     const TensorEntry* tab = plan->d_table;
     int nt = plan->n_tensors;
     int64_t tu = plan->total_units;
-    void* args[] = {&tab, &nt, &tu, &n_tiles, &s, &clip};
+    void* args[] = {&tab, &nt, &tu, &n_tiles, &s, &clip, &step_dev, &err};
     if (cudaLaunchKernel(step_kernel(plan->grad_dtype, plan->copy_dtype, plan->has_copy), dim3(grid),
                          dim3(kThreads), args, 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return TB_ERR_CUDA;
@@ -631,14 +658,21 @@ size_t grad_norm_workspace(const tb_adamw_plan* plan) {
 extern "C" tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
                                    const tb_adamw_hparams* hp, float inv_loss_scale,
                                    void* stream) {
-    return tb::adamw_step_impl(plan, step, hp, inv_loss_scale, nullptr, stream);
+    return tb::adamw_step_impl(plan, step, hp, inv_loss_scale, nullptr, nullptr, stream);
 }
 
 extern "C" tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t step,
                                            const tb_adamw_hparams* hp, float inv_loss_scale,
                                            const float* clip, void* stream) {
     if (!clip) return TB_ERR_INVALID_VALUE;
-    return tb::adamw_step_impl(plan, step, hp, inv_loss_scale, clip, stream);
+    return tb::adamw_step_impl(plan, step, hp, inv_loss_scale, clip, nullptr, stream);
+}
+
+extern "C" tb_status tb_adamw_step_device(const tb_adamw_plan* plan, const int64_t* step,
+                                          const tb_adamw_hparams* hp, float inv_loss_scale,
+                                          const float* clip, void* stream) {
+    if (!step) return TB_ERR_INVALID_VALUE;
+    return tb::adamw_step_impl(plan, 1, hp, inv_loss_scale, clip, step, stream);
 }
 
 extern "C" tb_status tb_adamw_grad_norm_workspace_size(const tb_adamw_plan* plan, size_t* bytes) {

@@ -94,3 +94,114 @@ def test_cuda_graph_capture_and_replay(tb, synth):
     for a, b in zip(got, want):
         assert torch.equal(a, b)
     assert tb.tb_device_error() == 0
+
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+def _clone_state(st):
+    import copy
+    c = copy.copy(st)
+    for k in ("theta", "m", "v", "grad", "copy"):
+        setattr(c, k, getattr(st, k).clone())
+    return c
+
+
+def _plan(tb, st):
+    k = len(st.sizes)
+    return tb.tb_adamw_plan_create(*[[st.tensor(a, i) for i in range(k)]
+                                     for a in ("theta", "m", "v", "grad", "copy")])
+
+
+def _close(a, b):
+    """fp32 state agreeing to 1e-6 relative (the device forms 1 - beta^t with CUDA's
+    pow and the host with the C library's; both round to fp32, so they differ at
+    most in a rare last bit of the bias correction)."""
+    return torch.allclose(a, b, rtol=1e-6, atol=1e-12)
+
+
+def test_device_step_counter_matches_host_steps(tb, synth):
+    a = synth.make_adamw_state(synth.gpt2_small_shapes()[:12], seed=61, device="cuda")
+    b = _clone_state(a)
+    pa, pb = _plan(tb, a), _plan(tb, b)
+    step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for t in range(1, 6):
+        synth.fill_grads(a, t)
+        b.grad.copy_(a.grad)
+        tb.tb_adamw_step(pa, t, inv_loss_scale=1 / 65536.0, **HP)
+        step.add_(1)
+        tb.tb_adamw_step_device(pb, step, inv_loss_scale=1 / 65536.0, **HP)
+    torch.cuda.synchronize()
+    for k in ("theta", "m", "v"):
+        assert _close(getattr(a, k), getattr(b, k)), k
+    assert torch.equal(b.grad, torch.zeros_like(b.grad))
+    assert tb.tb_device_error() == 0
+    pa.close()
+    pb.close()
+
+
+def test_whole_optimizer_step_replayed_from_a_cuda_graph(tb, synth):
+    """Counter increment, gradient norm and clipped update captured once and replayed
+    for three steps, against the same three steps called eagerly with host steps."""
+    shapes = synth.gpt2_small_shapes()[:12]
+    a = synth.make_adamw_state(shapes, seed=62, device="cuda")
+    b = _clone_state(a)
+    pa, pb = _plan(tb, a), _plan(tb, b)
+    max_norm = 0.05
+    grads = []
+    for t in range(1, 4):
+        synth.fill_grads(a, t)
+        grads.append(a.grad.clone())
+    # eager reference on a, host step counter
+    clip_a = torch.zeros(3, device="cuda")
+    ws_a = torch.empty(tb.tb_adamw_grad_norm_workspace_size(pa), dtype=torch.uint8, device="cuda")
+    for t in range(1, 4):
+        a.grad.copy_(grads[t - 1])
+        tb.tb_adamw_grad_norm(pa, 1 / 65536.0, max_norm, clip_a, ws_a)
+        tb.tb_adamw_step_clipped(pa, t, inv_loss_scale=1 / 65536.0, clip=clip_a, **HP)
+    # graph on b: everything per step lives on the device
+    step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    clip_b = torch.zeros(3, device="cuda")
+    ws_b = torch.empty(tb.tb_adamw_grad_norm_workspace_size(pb), dtype=torch.uint8, device="cuda")
+
+    def one_step():
+        step.add_(1)
+        tb.tb_adamw_grad_norm(pb, 1 / 65536.0, max_norm, clip_b, ws_b)
+        tb.tb_adamw_step_device(pb, step, inv_loss_scale=1 / 65536.0, clip=clip_b, **HP)
+
+    # warm up on a throw-away copy of the state so that b itself starts untouched
+    w = _clone_state(b)
+    pw = _plan(tb, w)
+    ws_w = torch.empty_like(ws_b)
+    tb.tb_adamw_grad_norm(pw, 1 / 65536.0, max_norm, clip_b, ws_w)
+    tb.tb_adamw_step_device(pw, torch.ones(1, dtype=torch.int64, device="cuda"),
+                            inv_loss_scale=1 / 65536.0, clip=clip_b, **HP)
+    torch.cuda.synchronize()
+    pw.close()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        one_step()
+    for t in range(1, 4):
+        b.grad.copy_(grads[t - 1])
+        graph.replay()
+    torch.cuda.synchronize()
+    assert step.item() == 3
+    assert _close(clip_a, clip_b)
+    for k in ("theta", "m", "v"):
+        assert _close(getattr(a, k), getattr(b, k)), k
+    assert tb.tb_device_error() == 0
+    pa.close()
+    pb.close()
+
+
+def test_device_step_below_one_updates_nothing(tb, synth):
+    st = synth.make_adamw_state([("a", (4096,))], seed=63, device="cuda")
+    plan = _plan(tb, st)
+    before = st.theta.clone()
+    tb.tb_adamw_step_device(plan, torch.zeros(1, dtype=torch.int64, device="cuda"),
+                            inv_loss_scale=1.0, **HP)
+    torch.cuda.synchronize()
+    assert torch.equal(st.theta, before)
+    assert tb.tb_device_error(reset=True) == 1        # TB_ERR_INVALID_VALUE
+    assert tb.tb_device_error(reset=True) == 0
+    plan.close()
