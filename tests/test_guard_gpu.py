@@ -181,6 +181,40 @@ def test_adamw_touches_only_its_tensors(tb, grad_dtype, with_copy):
         assert torch.equal(gap_now, gap_before), f"{k}: a gap between tensors was written"
     # and the live elements did change where they must
     assert not torch.equal(theta.view(torch.int32)[live], before["theta"].view(torch.int32)[live])
+    # the same steps on the same values packed without gaps give the same results, so
+    # no read of a gap (filled with NaN payloads) reached a result
+    n_live = int(live.sum())
+    packed = {k: before[k][live].clone() for k in before}
+    poffs, o = [], 0
+    for n in ADAMW_SIZES:
+        poffs.append(o)
+        o += n
+
+    def pviews(t):
+        return [t.narrow(0, off, n) for off, n in zip(poffs, ADAMW_SIZES)]
+
+    gen = torch.Generator(device="cuda").manual_seed(21)
+    for off, n in zip(offs, ADAMW_SIZES):             # replay the generator draws of the state
+        torch.randn(n, device="cuda", generator=gen)
+    plan = tb.tb_adamw_plan_create(pviews(packed["theta"]), pviews(packed["m"]), pviews(packed["v"]),
+                                   pviews(packed["grad"]),
+                                   pviews(packed["copy"]) if with_copy else [None] * len(offs))
+    clip2 = torch.zeros(3, device="cuda")
+    ws2 = torch.empty(tb.tb_adamw_grad_norm_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    for t in (1, 2):
+        parts = [(torch.randn(n, device="cuda", generator=gen) * 65.536).to(grad_dtype) for n in ADAMW_SIZES]
+        packed["grad"].copy_(torch.cat(parts))
+        tb.tb_adamw_step(plan, t, inv_loss_scale=1 / 65536.0, **hp)
+    parts = [(torch.randn(n, device="cuda", generator=gen) * 65.536).to(grad_dtype) for n in ADAMW_SIZES]
+    packed["grad"].copy_(torch.cat(parts))
+    tb.tb_adamw_grad_norm(plan, 1 / 65536.0, 1.0, clip2, ws2)
+    tb.tb_adamw_step_clipped(plan, 3, inv_loss_scale=1 / 65536.0, clip=clip2, **hp)
+    torch.cuda.synchronize()
+    plan.close()
+    assert packed["theta"].numel() == n_live
+    for k, t in (("theta", theta), ("m", m), ("v", v), ("grad", grad), ("copy", copy)):
+        itype = torch.int32 if t.element_size() == 4 else torch.int16
+        assert torch.equal(t.view(itype)[live], packed[k].view(itype)), f"{k}: differs from the packed run"
 
 
 def test_grad_norm_outputs_stay_in_bounds(tb, synth):
@@ -194,3 +228,86 @@ def test_grad_norm_outputs_stay_in_bounds(tb, synth):
     tb.tb_adamw_grad_norm(plan, 1 / 65536.0, 1.0, out.t, ws.t)
     assert out.margins_intact() and ws.margins_intact()
     plan.close()
+
+
+# ----------------------------------------------------------------------------- input guards
+# Each input is placed twice at the same offset from a 16-byte boundary: once between
+# margins of 0xFF bytes (a NaN in fp32, bf16 and fp16) and once between finite margins
+# (0xA5 bytes).  Both runs take the same code path, so a read past an input's end or
+# before its start that reached a result would make the two differ; every result must
+# be equal bit for bit.
+POISON = 0xFF
+
+
+class Poisoned(Guarded):
+    def __init__(self, values, shift=0, poison=True):
+        super().__init__(tuple(values.shape), values.dtype, shift)
+        if poison:
+            self.buf.fill_(POISON)
+        self.t.copy_(values)
+
+
+def _both(values, shift=0):
+    """The same values between finite margins and between NaN margins."""
+    return Poisoned(values, shift, poison=False).t, Poisoned(values, shift).t
+
+
+@pytest.mark.parametrize("rows, cols, dtype, shift", SOFTMAX_SHAPES)
+def test_softmax_reads_only_its_inputs(tb, synth, rows, cols, dtype, shift):
+    P, dY = synth.softmax_inputs(rows, cols, dtype, seed=15, device="cuda")
+    (fP, gP), (fdY, gdY) = _both(P, shift), _both(dY, shift)
+    ref, out = torch.empty_like(P), torch.empty_like(P)
+    tb.tb_softmax_bwd(fdY, fP, ref)
+    tb.tb_softmax_bwd(gdY, gP, out)
+    refc, outc = torch.empty_like(P), torch.empty_like(P)
+    tb.tb_softmax_bwd_causal(fdY, fP, refc, period=max(1, cols // 3), offset=1)
+    tb.tb_softmax_bwd_causal(gdY, gP, outc, period=max(1, cols // 3), offset=1)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert torch.equal(outc, refc)
+
+
+@pytest.mark.parametrize("rows, D, dtype, shift", LN_SHAPES)
+def test_layernorm_and_rmsnorm_read_only_their_inputs(tb, synth, rows, D, dtype, shift):
+    x, dY, mean, rstd, gamma = synth.layernorm_inputs(rows, D, dtype, seed=16, device="cuda")
+    pairs = [_both(dY, shift), _both(x, shift), _both(mean), _both(rstd), _both(gamma)]
+    outs = []
+    for side in (0, 1):
+        dX, dg, db = torch.empty_like(x), torch.empty(D, device="cuda"), torch.empty(D, device="cuda")
+        ws = torch.empty(tb.tb_layernorm_bwd_workspace_size(rows, D, dtype), dtype=torch.uint8,
+                         device="cuda")
+        tb.tb_layernorm_bwd(*[p[side] for p in pairs], dX, dg, db, ws)
+        outs.append((dX, dg, db))
+    xr, dYr, inv, gr = synth.rmsnorm_inputs(rows, D, dtype, seed=17, device="cuda")
+    pairs = [_both(dYr, shift), _both(xr, shift), _both(inv), _both(gr)]
+    for side in (0, 1):
+        dX, dg = torch.empty_like(xr), torch.empty(D, device="cuda")
+        ws = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(rows, D, dtype), dtype=torch.uint8,
+                         device="cuda")
+        tb.tb_rmsnorm_bwd(*[p[side] for p in pairs], dX, dg, ws)
+        outs.append((dX, dg))
+    torch.cuda.synchronize()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    for a, b in zip(outs[2], outs[3]):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("src_dtype", [torch.float16, torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("n, shift", [(1, 0), (8191, 0), (100_003, 4)])
+def test_casts_read_only_their_inputs(tb, src_dtype, n, shift):
+    src = (torch.randn(n, device="cuda") * 100).to(src_dtype)
+    sh = shift if src_dtype == torch.float32 else shift // 2
+    fs, gs = _both(src, sh)
+    ref, out = torch.empty(n, device="cuda"), torch.empty(n, device="cuda")
+    tb.tb_cast_to_f32(fs, ref, scale=0.5)
+    tb.tb_cast_to_f32(gs, out, scale=0.5)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    if src_dtype != torch.float32:
+        fr, gr = _both(ref, shift)
+        r16, o16 = torch.empty(n, dtype=src_dtype, device="cuda"), torch.empty(n, dtype=src_dtype, device="cuda")
+        tb.tb_cast_from_f32(fr, r16)
+        tb.tb_cast_from_f32(gr, o16)
+        torch.cuda.synchronize()
+        assert torch.equal(o16.view(torch.int16), r16.view(torch.int16))
