@@ -238,7 +238,8 @@ tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan);
  *                      src in src_dtype (TB_F16, TB_BF16 or TB_F32), dst fp32
  *   tb_cast_from_f32 : dst[i] = round-to-nearest-even(src[i]) in dst_dtype
  *                      (TB_F16 or TB_BF16)
- *   n >= 0 elements (0: nothing is enqueued); src and dst must not overlap.
+ *   0 <= n <= INT64_MAX / 8 elements (0: nothing is enqueued); src and dst must not
+ *   overlap.
  * Errors: TB_ERR_INVALID_VALUE, TB_ERR_UNSUPPORTED_DTYPE, TB_ERR_MISALIGNED,
  * TB_ERR_ALIAS, TB_ERR_CUDA.
  */

@@ -121,11 +121,24 @@ def _stream(stream) -> Optional[int]:
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    """Device pointer of a contiguous CUDA tensor on the current device (the C entry
+    points take device pointers and launch on the current device)."""
     if t is None:
         return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libtb must be CUDA tensors")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError("tensors passed to libtb must be contiguous")
     return t.data_ptr() if t.numel() > 0 else (t.data_ptr() or None)
+
+
+def _want(t: torch.Tensor, n: int, dtype: torch.dtype, name: str) -> None:
+    """The kernels index `t` by the sizes of the other arguments: check it holds them."""
+    if t.numel() != n or t.dtype != dtype:
+        raise ValueError(f"{name} must hold {n} {dtype} values, got {t.numel()} {t.dtype}")
 
 
 def _dtype(t: torch.Tensor) -> int:
@@ -184,6 +197,18 @@ def tb_adamw_plan_create(params: Sequence[torch.Tensor], ms: Sequence[torch.Tens
     n = len(params)
     if not (len(ms) == len(vs) == len(grads) == len(copies) == n):
         raise ValueError("params, m, v, grads and copies must have one entry per tensor")
+    gdtype = grads[0].dtype if n else None
+    cdtypes = {c.dtype for c in copies if c is not None}
+    if len(cdtypes) > 1:
+        raise ValueError("every working copy must have the same dtype")
+    for i in range(n):
+        k = params[i].numel()
+        _want(params[i], k, torch.float32, f"params[{i}]")
+        _want(ms[i], k, torch.float32, f"m[{i}]")
+        _want(vs[i], k, torch.float32, f"v[{i}]")
+        _want(grads[i], k, gdtype, f"grads[{i}]")
+        if copies[i] is not None:
+            _want(copies[i], k, copies[i].dtype, f"copies[{i}]")
     descs = (tb_tensor_desc * max(n, 1))()
     for i in range(n):
         descs[i] = tb_tensor_desc(_ptr(params[i]), _ptr(ms[i]), _ptr(vs[i]), _ptr(grads[i]),
@@ -310,10 +335,10 @@ def tb_rmsnorm_bwd(dY: torch.Tensor, x: torch.Tensor, inv_rms: torch.Tensor, gam
         raise ValueError("x, dY and dX must be [rows, D] tensors of one shape")
     if not (dY.dtype == x.dtype == dX.dtype):
         raise ValueError("x, dY and dX must share a dtype")
-    for t in (inv_rms, gamma, dgamma):
-        if t.dtype != torch.float32:
-            raise ValueError("inv_rms, gamma and dgamma are fp32")
     rows, D = x.shape
+    _want(inv_rms, rows, torch.float32, "inv_rms")
+    _want(gamma, D, torch.float32, "gamma")
+    _want(dgamma, D, torch.float32, "dgamma")
     ws_ptr = _ptr(workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("tb_rmsnorm_bwd",
@@ -336,10 +361,12 @@ def tb_layernorm_bwd(dY: torch.Tensor, x: torch.Tensor, mean: torch.Tensor, inv_
         raise ValueError("x, dY and dX must be [rows, D] tensors of one shape")
     if not (dY.dtype == x.dtype == dX.dtype):
         raise ValueError("x, dY and dX must share a dtype")
-    for t in (mean, inv_std, gamma, dgamma, dbeta):
-        if t.dtype != torch.float32:
-            raise ValueError("mean, inv_std, gamma, dgamma and dbeta are fp32")
     rows, D = x.shape
+    _want(mean, rows, torch.float32, "mean")
+    _want(inv_std, rows, torch.float32, "inv_std")
+    _want(gamma, D, torch.float32, "gamma")
+    _want(dgamma, D, torch.float32, "dgamma")
+    _want(dbeta, D, torch.float32, "dbeta")
     ws_ptr = _ptr(workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("tb_layernorm_bwd",
@@ -357,10 +384,12 @@ def tb_layernorm_bwd_noalloc(dY: torch.Tensor, x: torch.Tensor, mean: torch.Tens
         raise ValueError("x, dY and dX must be [rows, D] tensors of one shape")
     if not (dY.dtype == x.dtype == dX.dtype):
         raise ValueError("x, dY and dX must share a dtype")
-    for t in (mean, inv_std, gamma, dgamma, dbeta):
-        if t.dtype != torch.float32:
-            raise ValueError("mean, inv_std, gamma, dgamma and dbeta are fp32")
     rows, D = x.shape
+    _want(mean, rows, torch.float32, "mean")
+    _want(inv_std, rows, torch.float32, "inv_std")
+    _want(gamma, D, torch.float32, "gamma")
+    _want(dgamma, D, torch.float32, "dgamma")
+    _want(dbeta, D, torch.float32, "dbeta")
     _check("tb_layernorm_bwd_noalloc",
            lib.tb_layernorm_bwd_noalloc(_ptr(dY), _ptr(x), _ptr(mean), _ptr(inv_std), _ptr(gamma),
                                         _ptr(dX), _ptr(dgamma), _ptr(dbeta), rows, D, _dtype(x),

@@ -316,7 +316,6 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
                                 r[j][0] = in ? ld_stream_f4(gf + uu * kUnit) : make_float4(0.f, 0.f, 0.f, 0.f);
                                 r[j][1] = in ? ld_stream_f4(gf + uu * kUnit + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
                             }
-#pragma unroll
                             float f1 = 0.f;   // the 32 squares of this round
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {

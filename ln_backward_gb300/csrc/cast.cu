@@ -123,7 +123,7 @@ extern "C" tb_status tb_cast_to_f32(const void* src, tb_dtype src_dtype, float s
     if (n < 0) return TB_ERR_INVALID_VALUE;
     if (!dtype_valid(src_dtype)) return TB_ERR_UNSUPPORTED_DTYPE;
     if (n == 0) return TB_OK;
-    if (!src || !dst) return TB_ERR_INVALID_VALUE;
+    if (!src || !dst || n > INT64_MAX / 8) return TB_ERR_INVALID_VALUE;
     const size_t es = dtype_size(src_dtype);
     if (!aligned_to(src, es) || !aligned_to(dst, 4)) return TB_ERR_MISALIGNED;
     if (overlap(range_of(src, n, es), range_of(dst, n, 4))) return TB_ERR_ALIAS;
@@ -148,7 +148,7 @@ extern "C" tb_status tb_cast_from_f32(const float* src, void* dst, tb_dtype dst_
     if (n < 0) return TB_ERR_INVALID_VALUE;
     if (dst_dtype != TB_BF16 && dst_dtype != TB_F16) return TB_ERR_UNSUPPORTED_DTYPE;
     if (n == 0) return TB_OK;
-    if (!src || !dst) return TB_ERR_INVALID_VALUE;
+    if (!src || !dst || n > INT64_MAX / 8) return TB_ERR_INVALID_VALUE;
     if (!aligned_to(src, 4) || !aligned_to(dst, 2)) return TB_ERR_MISALIGNED;
     if (overlap(range_of(src, n, 4), range_of(dst, n, 2))) return TB_ERR_ALIAS;
     int dev = 0;

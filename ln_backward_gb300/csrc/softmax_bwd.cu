@@ -330,6 +330,9 @@ tb_status softmax_bwd_entry(const void* dY, const void* P, void* dX, int64_t row
     if (rows == 0 || cols == 0) return TB_OK;
     if (!dY || !P || !dX) return TB_ERR_INVALID_VALUE;
     if (cols > INT64_MAX / rows / 4) return TB_ERR_INVALID_VALUE;
+    // An offset of cols or more opens every column: clamp it so that the kernels'
+    // r mod period + 1 + offset cannot overflow.
+    if (offset > cols) offset = cols;
     const size_t es = dtype_size(dtype);
     if (!aligned_to(dY, es) || !aligned_to(P, es) || !aligned_to(dX, es)) return TB_ERR_MISALIGNED;
     const int64_t n = rows * cols;

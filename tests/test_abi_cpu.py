@@ -193,6 +193,9 @@ def test_cast_validation(tb):
     assert lib.tb_cast_from_f32(A, B, F32, 4, None) == DTYPE
     assert lib.tb_cast_from_f32(A, A + 2, BF16, 4, None) == ALIAS
     assert lib.tb_cast_from_f32(None, B, BF16, 4, None) == INVALID
+    # element counts whose byte ranges would overflow are rejected before any CUDA call
+    assert lib.tb_cast_to_f32(A, F16, 1.0, B, 2**62, None) == INVALID
+    assert lib.tb_cast_from_f32(A, B, BF16, 2**62, None) == INVALID
 
 
 def test_selftest_limit_validation(tb):

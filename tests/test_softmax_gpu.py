@@ -166,3 +166,16 @@ def test_causal_variant_rejects_bad_period(tb, synth):
     P, dY = synth.softmax_inputs(8, 64, torch.float32, seed=3, device="cuda")
     with pytest.raises(tb.TbError):
         tb.tb_softmax_bwd_causal(dY, P, torch.empty_like(P), period=0)
+
+
+def test_causal_variant_huge_offset_opens_every_column(tb, synth):
+    """An offset far beyond cols (up to the int64 limit) leaves no column masked: the
+    result is the dense one, bit for bit."""
+    P, dY = synth.softmax_inputs(100, 1000, torch.float32, seed=7, device="cuda")
+    dense = torch.empty_like(P)
+    tb.tb_softmax_bwd(dY, P, dense)
+    for offset in (1000, 2**40, 2**63 - 1):
+        dX = torch.full_like(P, float("nan"))
+        tb.tb_softmax_bwd_causal(dY, P, dX, period=2**62, offset=offset)
+        torch.cuda.synchronize()
+        assert torch.equal(dX, dense), offset
