@@ -373,10 +373,10 @@ def run_ours(args):
 
 
 # Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, from
-# one single-pass ncu capture of the full step (94.346 GB read + 107.755 GB written;
+# one single-pass ncu capture of the full step (94.343 GB read + 107.754 GB written;
 # profiles/dram_traffic_full_step_llama7b.md).  Must go back to None whenever the
 # kernel changes until it is captured again.
-ADAMW_TRAFFIC_PER_LAUNCH = 202.100529152e9
+ADAMW_TRAFFIC_PER_LAUNCH = 202.097223168e9
 
 
 def time_extras(hp_path, reps, peak):

@@ -11,16 +11,22 @@
 // Design (GB300): one launch covers every tensor of the model.  The host plan
 // holds a device table of tensors and a prefix sum of their "units" (8
 // elements = one 16-byte vector of the 16-bit gradient and two of each fp32
-// stream).  The flat unit space is cut into tiles of 512 units dealt
-// round-robin to a persistent grid (SM count x resident CTAs), so all CTAs
-// stream through the same region of HBM at once; each CTA follows its tensor
-// with a forward scan of the table.  Every thread moves 2 units per step with
-// 128-bit evict-first loads and stores: 14 B read and 16 B written per element,
-// one HBM pass.  Tensors whose five pointers are not all 16-byte aligned, and
-// the last partial unit of a tensor, take a scalar path.
+// stream).  The flat unit space is cut into tiles of 2048 units (16,384
+// elements) for a persistent grid (SM count x resident CTAs).  CTA b starts on
+// tile b; every further tile is claimed from a counter in the plan, in
+// increasing order, so all CTAs stream through the same region of HBM at once
+// and a CTA on a faster SM simply takes more tiles (on GB300 some SMs stream a
+// few per cent slower than others; with a fixed share per CTA the step would
+// end with them).  The update is elementwise, so which CTA takes which tile
+// changes no result bit.  Each CTA follows its tensor with a forward scan of
+// the table.  Every thread moves 2 units per step with 128-bit evict-first
+// loads and stores: 14 B read and 16 B written per element, one HBM pass.
+// Tensors whose five pointers are not all 16-byte aligned, and the last
+// partial unit of a tensor, take a scalar path.
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <new>
 #include <type_traits>
@@ -53,6 +59,15 @@ struct alignas(16) TensorEntry {
     int32_t pad;
 };
 static_assert(sizeof(TensorEntry) == 64, "table entry is one 64-byte line");
+
+// Tile counter of a plan's step kernel, in device memory after the table.  It is
+// zero when a launch starts; the last CTA to finish sets it back to zero, so
+// launches of one plan must be stream-ordered (they update the same tensors).
+struct alignas(16) TileQueue {
+    unsigned long long next;   // tiles claimed so far beyond the first one of each CTA
+    unsigned int done;         // CTAs finished
+    unsigned int pad;
+};
 
 // Per-step scalars, hoisted on the host.
 struct Scalars {
@@ -229,7 +244,7 @@ template <class G, class C>
 __global__ void __launch_bounds__(kThreads, 2)
 adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
                           int64_t n_tiles, Scalars s, const float* __restrict__ clip,
-                          const int64_t* __restrict__ step_dev, int* err) {
+                          const int64_t* __restrict__ step_dev, int* err, TileQueue* q) {
     bool skip = false;
     if (clip) {
         s.clip = clip[1];
@@ -250,8 +265,14 @@ adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t
         s.bc1 = s_bc[0];
         s.bc2 = s_bc[1];
     }
+    // The next tile is claimed while this one streams (the claim's round trip
+    // stays off the critical path); two slots, so one barrier per tile suffices.
+    __shared__ long long s_tile[2];
     int k = 0;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; ++it) {
+        if (threadIdx.x == 0)
+            s_tile[(it + 1) & 1] = (long long)gridDim.x + (long long)atomicAdd(&q->next, 1ull);
         const int64_t u_lo = tile * kTileUnits;
         const int64_t u_hi = u_lo + kTileUnits < total_units ? u_lo + kTileUnits : total_units;
         k = tensor_of(tab, ntab, k, u_lo);
@@ -268,6 +289,14 @@ adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t
             u = seg_hi > u ? seg_hi : u;
             ++kk;
         }
+        __syncthreads();
+        tile = s_tile[(it + 1) & 1];
+    }
+    // Every CTA's last claim came back past the end; the last CTA out resets the
+    // counter for the next launch.
+    if (threadIdx.x == 0 && atomicAdd(&q->done, 1u) == gridDim.x - 1) {
+        q->next = 0ull;
+        q->done = 0u;
     }
 }
 
@@ -566,7 +595,11 @@ static tb_status plan_create_impl(const tb_tensor_desc* tensors, int n_tensors,
     plan->norm_grid = info.sm_count * std::max(norm_per_sm, 1);
     plan->has_copy = has_copy;
     plan->d_table = nullptr;
-    const size_t bytes = sizeof(TensorEntry) * (size_t)n_tensors;
+    // The table, then the step kernel's tile counter (zero), copied up together.
+    const size_t bytes = sizeof(TensorEntry) * (size_t)n_tensors + sizeof(TileQueue);
+    tab.resize((size_t)n_tensors + 1);
+    std::memset(static_cast<void*>(&tab[(size_t)n_tensors]), 0, sizeof(TensorEntry));
+    static_assert(sizeof(TileQueue) <= sizeof(TensorEntry), "the counter fits in one table slot");
     cudaError_t e = cudaMalloc(&plan->d_table, bytes);
     if (e != cudaSuccess) {
         delete plan;
@@ -640,7 +673,8 @@ tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adam
     const TensorEntry* tab = plan->d_table;
     int nt = plan->n_tensors;
     int64_t tu = plan->total_units;
-    void* args[] = {&tab, &nt, &tu, &n_tiles, &s, &clip, &step_dev, &err};
+    TileQueue* q = reinterpret_cast<TileQueue*>(plan->d_table + plan->n_tensors);
+    void* args[] = {&tab, &nt, &tu, &n_tiles, &s, &clip, &step_dev, &err, &q};
     if (cudaLaunchKernel(step_kernel(plan->grad_dtype, plan->copy_dtype, plan->has_copy), dim3(grid),
                          dim3(kThreads), args, 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return TB_ERR_CUDA;
