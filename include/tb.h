@@ -159,6 +159,11 @@ tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
  *   hp              hyperparameters (read during the call only)
  *   inv_loss_scale  1/loss_scale (exact for a power-of-two scale); > 0
  *   stream          cudaStream_t or NULL
+ * The kernel's CTAs claim tiles of the flat parameter space from a counter kept
+ * in the plan's device memory (so CTAs on faster SMs take more tiles); the
+ * last CTA to finish resets it.  Steps of one plan (plain, clipped or device)
+ * must therefore run one after another: on one stream, or ordered by events.
+ * They update the same tensors, so they must be ordered in any case.
  * Errors: TB_ERR_INVALID_VALUE (plan/hp NULL, step < 1, beta outside [0,1),
  * eps, lr or weight_decay negative or not finite, inv_loss_scale <= 0),
  * TB_ERR_DEVICE (another device is current), TB_ERR_CUDA.

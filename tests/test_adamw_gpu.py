@@ -266,3 +266,78 @@ def test_plan_of_empty_tensors_is_a_no_op(tb):
     tb.tb_softmax_bwd(torch.ones_like(P), P, dX)
     torch.cuda.synchronize()
     assert torch.all(dX == 0)
+
+
+def test_tile_counter_is_reset_on_every_path(tb, synth):
+    """The step kernel's CTAs claim tiles from a counter in the plan that the last CTA
+    out resets.  After every kind of call (a device step that returns early for t < 1,
+    a step skipped for a non-finite gradient, plain, clipped and device steps) the next
+    step must still visit every element: each step leaves every gradient element +0.
+    Two tables: one with many more tiles than CTAs, one with a single tile."""
+    for shapes in (synth.gpt2_small_shapes()[:30], [("a", (4096,)), ("b", (77,))]):
+        st = synth.make_adamw_state(shapes, seed=71, device="cuda")
+        plan = _plan(tb, st)
+        k = len(st.sizes)
+        clip = torch.zeros(3, device="cuda")
+        ws = torch.empty(tb.tb_adamw_grad_norm_workspace_size(plan), dtype=torch.uint8,
+                         device="cuda")
+        inv = 1 / 65536.0
+
+        def grads_zero():
+            torch.cuda.synchronize()
+            return all(bool((st.tensor("grad", i) == 0).all()) for i in range(k))
+
+        def clipped(t):
+            tb.tb_adamw_grad_norm(plan, inv, 1.0, clip, ws)
+            tb.tb_adamw_step_clipped(plan, t, inv_loss_scale=inv, clip=clip, **HP)
+
+        calls = [
+            ("device step with t = 0", False,
+             lambda: tb.tb_adamw_step_device(plan, torch.zeros(1, dtype=torch.int64, device="cuda"),
+                                             inv_loss_scale=inv, **HP)),
+            ("plain step", True, lambda: tb.tb_adamw_step(plan, 1, inv_loss_scale=inv, **HP)),
+            ("clipped step", True, lambda: clipped(2)),
+            ("skipped step", True, lambda: clipped(3)),
+            ("device step", True,
+             lambda: tb.tb_adamw_step_device(plan, torch.full((1,), 3, dtype=torch.int64, device="cuda"),
+                                             inv_loss_scale=inv, **HP)),
+            ("plain step again", True, lambda: tb.tb_adamw_step(plan, 4, inv_loss_scale=inv, **HP)),
+        ]
+        for i, (name, runs, call) in enumerate(calls):
+            synth.fill_grads(st, i + 2)
+            if name == "skipped step":
+                st.tensor("grad", k - 1)[-1] = float("inf")
+            before = st.theta.clone()
+            call()
+            if runs:
+                assert grads_zero(), f"{name}: some gradient elements were not visited"
+            else:
+                assert not grads_zero() and torch.equal(st.theta, before), name
+            if name == "skipped step":
+                assert clip[2].item() == 1.0 and torch.equal(st.theta, before)
+        assert tb.tb_device_error(reset=True) == 1      # from the t = 0 call
+        plan.close()
+
+
+def test_steps_of_one_plan_on_two_streams_ordered_by_events(tb, synth):
+    """Steps of one plan alternate between two streams, each waiting for the other;
+    the result equals the same steps on one stream, bit for bit."""
+    shapes = synth.gpt2_small_shapes()[:16]
+    a = synth.make_adamw_state(shapes, seed=72, device="cuda")
+    b = synth.make_adamw_state(shapes, seed=72, device="cuda")
+    pa, pb = _plan(tb, a), _plan(tb, b)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for t in range(1, 7):
+        synth.fill_grads(a, t)
+        synth.fill_grads(b, t)
+        torch.cuda.synchronize()
+        tb.tb_adamw_step(pa, t, inv_loss_scale=1 / 65536.0, **HP)
+        s, other = (s1, s2) if t % 2 else (s2, s1)
+        s.wait_stream(other)
+        tb.tb_adamw_step(pb, t, inv_loss_scale=1 / 65536.0, stream=s, **HP)
+        torch.cuda.synchronize()
+    for key in ("theta", "m", "v", "copy", "grad"):
+        assert torch.equal(getattr(a, key), getattr(b, key)), key
+    pa.close()
+    pb.close()
