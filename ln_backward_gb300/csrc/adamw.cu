@@ -231,8 +231,9 @@ __device__ __forceinline__ int tensor_of(const TensorEntry* __restrict__ tab, in
     return lo;
 }
 
-// Tiles of kTileUnits consecutive units are dealt round-robin to the CTAs, so at
-// any moment all CTAs stream through one window of about grid*kTileUnits units.
+// Tiles of kTileUnits consecutive units: CTA b takes tile b first, then claims
+// tiles from q->next in increasing order, so at any moment all CTAs stream
+// through one window of about grid*kTileUnits units and faster SMs take more.
 // clip (device memory, may be null): {norm, factor, nonfinite} as written by the
 // gradient-norm kernels; the gradient is multiplied by factor, and when nonfinite
 // is set the step is skipped (only the gradient is reset).
