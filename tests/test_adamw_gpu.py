@@ -84,6 +84,11 @@ def _run(tb, synth, st, steps, idx, first_step=1):
         torch.cuda.synchronize()
         gz = to_bits(st.grad.index_select(0, it))
         assert np.all(gz == 0), f"gradient not zeroed at step {t}"
+        # every element of every tensor, not only the sampled ones: each tile was visited
+        ity = torch.int16 if st.grad.element_size() == 2 else torch.int32
+        assert all(bool((st.tensor("grad", i).view(ity) == 0).all())
+                   for i in range(len(st.sizes)) if st.sizes[i] > 0), \
+            f"gradient not zeroed everywhere at step {t}"
     plan.close()
     got_th = st.theta.index_select(0, it).double().cpu().numpy()
     got_m = st.m.index_select(0, it).double().cpu().numpy()
