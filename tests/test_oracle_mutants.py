@@ -19,7 +19,7 @@ ADAMW_PINS = [A.test_step1_closed_form, A.test_constant_gradient_no_decay,
 SOFTMAX_PINS = [S.test_one_hot_rows_give_exact_zero, S.test_uniform_rows_give_centered_dy,
                 S.test_rows_sum_to_zero, S.test_central_finite_differences,
                 S.test_matches_torch_autograd_float64]
-LN_PINS = [L.test_dbeta_is_column_sum, L.test_rows_of_dx_sum_to_zero,
+LN_PINS = [L.test_dbeta_is_column_sum, L.test_dgamma_is_column_sum_of_dy_xhat, L.test_rows_of_dx_sum_to_zero,
            L.test_dx_orthogonal_to_xhat_when_eps_zero, L.test_d_equals_one_is_degenerate,
            L.test_central_finite_differences, L.test_matches_torch_autograd_float64]
 
@@ -64,6 +64,11 @@ MUTANTS = [
      "(1.0 - b2) * (g * g);", "(1.0 - b2) * g;", ADAMW_PINS),
     ("adamw: decay on the updated theta",
      "- lr * wd * th;", "- lr * wd * (th - lr * m_hat / (sqrt(v_hat) + eps));", ADAMW_PINS),
+    ("adamw: second-moment bias correction dropped",
+     "double v_hat = v[i] / bc2;", "double v_hat = v[i];", ADAMW_PINS),
+    ("adamw: working copy rounded from the pre-update theta",
+     "copy[i] = orc_encode16_rne(theta[i], copy_kind);", "copy[i] = orc_encode16_rne(th, copy_kind);",
+     ADAMW_PINS),
     ("adamw: loss scale not removed",
      "* inv_loss_scale;\n        /* first", ";\n        /* first", ADAMW_PINS),
     ("softmax: dot added instead of subtracted",
@@ -72,6 +77,8 @@ MUTANTS = [
      "for (int64_t j = 0; j < cols; ++j) dot += p[j] * dy[j];\n        for (int64_t j = 0; j < cols; ++j) dx[j] = p[j] * (dy[j] - dot);\n    }\n}\n\nvoid orc_softmax_bwd_f32",
      "for (int64_t j = 0; j < cols; ++j) dot += dy[j] * dy[j];\n        for (int64_t j = 0; j < cols; ++j) dx[j] = p[j] * (dy[j] - dot);\n    }\n}\n\nvoid orc_softmax_bwd_f32",
      SOFTMAX_PINS),
+    ("softmax: every row reads the first row of P",
+     "const double* p = P + r * cols;", "const double* p = P;", SOFTMAX_PINS),
     ("softmax: P factor dropped",
      "dx[j] = p[j] * (dy[j] - dot);", "dx[j] = (dy[j] - dot);", SOFTMAX_PINS),
     ("layernorm: mean of dxhat dropped",
@@ -88,6 +95,12 @@ MUTANTS = [
     ("layernorm: dbeta accumulates dxhat",
      "dbeta[j] += dyr[j];\n        }\n    }\n}\n\nvoid orc_layernorm_bwd_f32",
      "dbeta[j] += dxhat;\n        }\n    }\n}\n\nvoid orc_layernorm_bwd_f32", LN_PINS),
+    ("layernorm: dgamma from the raw x instead of xhat",
+     "dgamma[j] += dyr[j] * xhat;\n            dbeta[j] += dyr[j];\n        }\n    }\n}\n\nvoid orc_layernorm_bwd_f32",
+     "dgamma[j] += dyr[j] * xr[j];\n            dbeta[j] += dyr[j];\n        }\n    }\n}\n\nvoid orc_layernorm_bwd_f32",
+     LN_PINS),
+    ("layernorm: projection sum takes dY instead of dxhat",
+     "sum_dxhat_xhat += dxhat * xhat;", "sum_dxhat_xhat += dyr[j] * xhat;", LN_PINS),
     ("layernorm: inv_std factor dropped from dX",
      "dxr[j] = rs * (dxhat - mean_dxhat - xhat * mean_dxhat_xhat);\n            dgamma[j] += dyr[j] * xhat;\n            dbeta[j] += dyr[j];\n        }\n    }\n}\n\nvoid orc_layernorm_bwd_f32",
      "dxr[j] = (dxhat - mean_dxhat - xhat * mean_dxhat_xhat);\n            dgamma[j] += dyr[j] * xhat;\n            dbeta[j] += dyr[j];\n        }\n    }\n}\n\nvoid orc_layernorm_bwd_f32",
