@@ -139,7 +139,8 @@ typedef struct tb_adamw_plan tb_adamw_plan;   /* opaque */
  *               (copy == NULL: the step writes no copy).
  *   out         receives the plan; the caller owns it and frees it with
  *               tb_adamw_plan_destroy.  The plan owns a device copy of the table
- *               (64 bytes per tensor) and remembers the current device.
+ *               (64 bytes per tensor) followed by the step kernel's 16-byte tile
+ *               counter, and remembers the current device.
  *               Every call that takes a plan first looks it up among the plans
  *               created and not yet destroyed; any other pointer (a destroyed
  *               plan included) is rejected with TB_ERR_INVALID_VALUE without
