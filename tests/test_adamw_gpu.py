@@ -65,8 +65,9 @@ def _all_live(st):
     return np.concatenate([np.arange(o, o + n) for o, n in zip(st.offsets, st.sizes) if n > 0])
 
 
-def _run(tb, synth, st, steps, idx, first_step=1):
+def _run(tb, synth, st, steps, idx, first_step=1, hp=None):
     """Runs `steps` GPU steps and the oracle on arena indices `idx`; returns errors."""
+    hp = HP if hp is None else hp
     dev = st.theta.device
     gkind, ckind = KIND[st.grad.dtype], KIND[st.copy.dtype]
     inv = 1.0 / st.loss_scale
@@ -79,8 +80,8 @@ def _run(tb, synth, st, steps, idx, first_step=1):
         if t != 1:
             synth.fill_grads(st, t)
         gb = to_bits(st.grad.index_select(0, it))
-        tb.tb_adamw_step(plan, t, inv_loss_scale=inv, **HP)
-        cb, _ = oracle.adamw_step_f64(th, m, v, gb, gkind, inv, t, copy_kind=ckind, **HP)
+        tb.tb_adamw_step(plan, t, inv_loss_scale=inv, **hp)
+        cb, _ = oracle.adamw_step_f64(th, m, v, gb, gkind, inv, t, copy_kind=ckind, **hp)
         torch.cuda.synchronize()
         gz = to_bits(st.grad.index_select(0, it))
         assert np.all(gz == 0), f"gradient not zeroed at step {t}"
@@ -346,3 +347,23 @@ def test_steps_of_one_plan_on_two_streams_ordered_by_events(tb, synth):
         assert torch.equal(getattr(a, key), getattr(b, key)), key
     pa.close()
     pb.close()
+
+
+@pytest.mark.parametrize("hp", [
+    dict(lr=1e-3, beta1=0.0, beta2=0.999, eps=1e-8, weight_decay=0.01),
+    dict(lr=1e-3, beta1=0.9, beta2=0.0, eps=1e-8, weight_decay=0.01),
+    dict(lr=0.0, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01),
+    dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=0.0, weight_decay=0.0),
+    dict(lr=0.5, beta1=0.5, beta2=0.75, eps=1e-3, weight_decay=0.5),
+], ids=["beta1=0", "beta2=0", "lr=0", "eps=0-no-decay", "large"])
+def test_hyperparameter_edges(tb, synth, hp):
+    """The ends of the accepted ranges (beta = 0 makes m or v the last gradient alone,
+    lr = 0 leaves theta exactly as it was, eps = 0 divides by sqrt(v_hat) alone) and
+    large values, against the oracle on every element over 5 steps."""
+    st = synth.make_adamw_state([("a", (4096,)), ("b", (1000,)), ("c", (7,))], seed=81,
+                                device="cuda")
+    theta0 = st.theta.clone()
+    err = _run(tb, synth, st, 5, _all_live(st), hp=hp)
+    _assert_within_targets(err)
+    if hp["lr"] == 0.0:
+        assert torch.equal(st.theta, theta0)
