@@ -162,3 +162,21 @@ def test_norm_llama7b_table_against_float64_reduction(tb, synth):
     torch.cuda.empty_cache()
     assert abs(out[0] - ref) <= 1e-5 * ref
     assert abs(out[1] - min(1.0, 1.0 / ref)) <= 1e-5 and out[2] == 0.0
+
+
+def test_norm_special_cases(tb, synth):
+    """All-zero gradients: norm 0, factor 1, no flag.  A max_norm that is negative or
+    equal to the norm leaves the factor at exactly 1."""
+    st = synth.make_adamw_state([("a", (4096,)), ("b", (77,))], seed=9, device="cuda")
+    plan = _plan(tb, st)
+    st.grad.zero_()
+    out = _norm(tb, plan, 1 / 65536.0, 1.0).cpu().numpy()
+    assert out[0] == 0.0 and out[1] == 1.0 and out[2] == 0.0
+    # gradients whose unscaled norm is exactly 2: four elements of 1 (bf16 65536 * 1/65536)
+    st.tensor("grad", 0)[:4] = 65536.0
+    for max_norm in (-1.0, 2.0, 3.0):
+        out = _norm(tb, plan, 1 / 65536.0, max_norm).cpu().numpy()
+        assert out[0] == 2.0 and out[1] == 1.0 and out[2] == 0.0, max_norm
+    out = _norm(tb, plan, 1 / 65536.0, 0.5).cpu().numpy()
+    assert out[0] == 2.0 and out[1] == 0.25
+    plan.close()
