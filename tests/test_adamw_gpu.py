@@ -367,3 +367,48 @@ def test_hyperparameter_edges(tb, synth, hp):
     _assert_within_targets(err)
     if hp["lr"] == 0.0:
         assert torch.equal(st.theta, theta0)
+
+
+def test_tile_counter_over_a_long_mix_of_calls(tb, synth):
+    """200 calls on one plan, cycling through plain, clipped and device-counter steps and
+    replays of a captured graph; after every call each gradient element is +0 (every tile
+    was visited, so the counter started each launch at zero)."""
+    st = synth.make_adamw_state(synth.gpt2_small_shapes()[:8], seed=73, device="cuda")
+    plan = _plan(tb, st)
+    k = len(st.sizes)
+    inv = 1 / 65536.0
+    clip = torch.zeros(3, device="cuda")
+    ws = torch.empty(tb.tb_adamw_grad_norm_workspace_size(plan), dtype=torch.uint8, device="cuda")
+    step = torch.zeros(1, dtype=torch.int64, device="cuda")
+
+    def device_step():
+        step.add_(1)
+        tb.tb_adamw_grad_norm(plan, inv, 1.0, clip, ws)
+        tb.tb_adamw_step_device(plan, step, inv_loss_scale=inv, clip=clip, **HP)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        device_step()                       # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        device_step()
+    ity = torch.int16
+    for i in range(200):
+        synth.fill_grads(st, i + 2)
+        kind = i % 4
+        if kind == 0:
+            tb.tb_adamw_step(plan, i + 1, inv_loss_scale=inv, **HP)
+        elif kind == 1:
+            tb.tb_adamw_grad_norm(plan, inv, 1.0, clip, ws)
+            tb.tb_adamw_step_clipped(plan, i + 1, inv_loss_scale=inv, clip=clip, **HP)
+        elif kind == 2:
+            device_step()
+        else:
+            graph.replay()
+        torch.cuda.synchronize()
+        assert all(bool((st.tensor("grad", j).view(ity) == 0).all()) for j in range(k)), (i, kind)
+    assert tb.tb_device_error(reset=True) == 0
+    plan.close()
