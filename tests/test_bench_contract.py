@@ -1,0 +1,44 @@
+"""bench.py's output line, checked on the CPU through the reference arm (the CPU oracle,
+which needs no GPU): one JSON line with every key of the benchmark contract, for the
+same metric and workload as the GPU arm, and consistent numbers."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args):
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stdout + p.stderr
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line_has_every_contract_key():
+    line = _run("--impl", "reference", "--steps", "3", "--warmup", "3")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference"
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["n_gpus"] == 1
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["scaling"] == "weak" and line["vs_baseline"] is None
+    assert line["value"] > 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == line["value"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    # the same workload and metric as the GPU arm
+    import bench
+    assert line["metric"] == bench.METRIC
+    assert line["config"]["workload"] == bench.WORKLOAD_TEXT["full"]
+    assert line["config"]["bytes_per_step"] == bench.FULL_STEP_BYTES
+    # value and ms_per_step describe the same step
+    assert abs(line["value"] - bench.FULL_STEP_BYTES / (line["ms_per_step"] / 1e3) / 1e9) \
+        <= 1e-3 * line["value"] + 1e-4
