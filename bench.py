@@ -360,7 +360,8 @@ def run_ours(args):
             "kernels": kernels,
             "extras": extras,
             "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": round(ad_gbs / peak, 4), "traffic": ADAMW_TRAFFIC_PER_LAUNCH,
+                         "frac": round(ad_gbs / peak, 4),
+                         "traffic": ADAMW_TRAFFIC_PER_LAUNCH if args.workload == "full" else None,
                          "kernel": "adamw_multi_tensor_kernel", "peak_source": peak_kind},
             "clocks": clk,
             "gpu_launches": hp_path.launches_per_step * K,

@@ -42,3 +42,29 @@ def test_reference_arm_line_has_every_contract_key():
     # value and ms_per_step describe the same step
     assert abs(line["value"] - bench.FULL_STEP_BYTES / (line["ms_per_step"] / 1e3) / 1e9) \
         <= 1e-3 * line["value"] + 1e-4
+
+
+import pytest  # noqa: E402
+
+
+@pytest.mark.gpu
+def test_gpu_arm_line_has_every_contract_key():
+    """The GPU arm on the small workload (the same code path as the full one): roofline,
+    clocks, launch count and the end-to-end figure with its copied bytes."""
+    line = _run("--workload", "small", "--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "clocks", "gpu_launches", "e2e"):
+        assert key in line, key
+    assert line["value"] > 0 and line["n_gpus"] == 1 and line["steps"] == 3
+    rf = line["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) <= 1e-3
+    assert 0.3 < rf["frac"] < 1.2
+    assert rf["traffic"] is None        # the stored DRAM traffic is the full workload's
+    ck = line["clocks"]
+    assert ck["sm_mhz"] > 0 and ck["sm_max_mhz"] > 0 and isinstance(ck["reasons"], list)
+    assert line["gpu_launches"] == 5 * line["steps"]     # AdamW, 2 softmax, LayerNorm rows + columns
+    e2e = line["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
