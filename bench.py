@@ -12,8 +12,15 @@ AdamW, 12 or 6 B/element for softmax, 6 B/element + stats for LayerNorm)
 divided by the device time of the step, summed over ranks for N > 1 (each rank
 runs an independent replica: weak scaling).
 
+Timing: CUDA events bracket the timed steps and, inside each step, the AdamW
+launch (its mean duration is the roofline's `achieved`).  No event sits between
+the backward kernels, which run back to back as in a training step; their total
+per step is `backward_in_step`, and each one's own duration comes from a loop of
+back-to-back calls of it after the timed region (`kernels`).
+
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-With --impl reference the CPU oracle is timed on the host instead (rank 0 only).
+With --impl reference the CPU oracle is timed on the host's cores instead (rank 0
+only), one proportional sample of the workload per step.
 """
 from __future__ import annotations
 
@@ -234,6 +241,7 @@ class HotPath:
         self.clip = torch.zeros(3, device=device)
         self.nws = torch.empty(tb.tb_adamw_grad_norm_workspace_size(self.plan), dtype=torch.uint8,
                                device=device)
+        self._bwd = list(self.backward().values())
 
     def extras(self):
         """name -> (callable, algorithmic bytes) for the kernels outside the step."""
@@ -265,20 +273,32 @@ class HotPath:
         tb.tb_adamw_step(self.plan32, self.t + 1, inv_loss_scale=1.0, **HP)
         tb.tb_cast_from_f32(self.st.theta, self.st.copy)
 
+    def backward(self):
+        """name -> callable of the backward kernels of the step, in step order."""
+        tb = self.tb
+        return {
+            "softmax_f32": lambda: tb.tb_softmax_bwd(self.dY32, self.P32, self.dX32),
+            "softmax_bf16": lambda: tb.tb_softmax_bwd(self.dY16, self.P16, self.dX16),
+            "layernorm_bf16": lambda: tb.tb_layernorm_bwd(self.ldY, self.x, self.mean, self.rstd,
+                                                          self.gamma, self.ldX, self.dg, self.db,
+                                                          self.ws),
+        }
+
     def step(self, events=None):
+        """One step.  `events` (two CUDA events, or None) bracket the AdamW launch only:
+        an event recorded between two kernels makes the second wait for the first to
+        complete and flush before it is even placed, so the backward kernels run back
+        to back, as in a training step, and each overlaps its set-up with the drain of
+        the one before it (programmatic dependent launch)."""
         tb = self.tb
         self.t += 1
-        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
-        rec(0)
+        if events is not None:
+            events[0].record()
         tb.tb_adamw_step(self.plan, self.t, inv_loss_scale=1.0 / LOSS_SCALE, **HP)
-        rec(1)
-        tb.tb_softmax_bwd(self.dY32, self.P32, self.dX32)
-        rec(2)
-        tb.tb_softmax_bwd(self.dY16, self.P16, self.dX16)
-        rec(3)
-        tb.tb_layernorm_bwd(self.ldY, self.x, self.mean, self.rstd, self.gamma, self.ldX,
-                            self.dg, self.db, self.ws)
-        rec(4)
+        if events is not None:
+            events[1].record()
+        for fn in self._bwd:
+            fn()
 
 
 def run_ours(args):
@@ -299,7 +319,7 @@ def run_ours(args):
     if hp_path.tb.tb_device_error(reset=True) != 0:
         raise RuntimeError("a kernel's bounded wait gave up during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier()
@@ -316,10 +336,14 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    per = {n: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)] for i, n in enumerate(names)}
-    mean_ms = {n: statistics.fmean(v) for n, v in per.items()}
-    red = reduce_over_ranks([total_ms] + [mean_ms[n] for n in names], "max")
-    total_ms, mean_ms = red[0], dict(zip(names, red[1:]))
+    adamw_ms = statistics.fmean(evs[k][0].elapsed_time(evs[k][1]) for k in range(K))
+    # the backward kernels of step k run from AdamW's end to the start of step k+1
+    bwd_ms = statistics.fmean(evs[k][1].elapsed_time(evs[k + 1][0] if k + 1 < K else end)
+                              for k in range(K))
+    total_ms, adamw_ms, bwd_ms = reduce_over_ranks([total_ms, adamw_ms, bwd_ms], "max")
+    # each backward kernel on its own: a loop of back-to-back calls after the timed region
+    iso = {n: time_loop(fn, reps=max(K, 20)) for n, fn in hp_path.backward().items()}
+    mean_ms = dict(adamw=adamw_ms, **iso)
 
     step_bytes = sum(hp_path.bytes.values())
     value = job_gbs(world, step_bytes, K, total_ms)
@@ -328,8 +352,15 @@ def run_ours(args):
     for n in names:
         gbs = hp_path.bytes[n] / (mean_ms[n] / 1e3) / 1e9
         kernels[n] = {"ms": round(mean_ms[n], 4), "GB_s": round(gbs, 1),
-                      "frac_of_peak": round(gbs / peak, 4), "bytes": hp_path.bytes[n]}
+                      "frac_of_peak": round(gbs / peak, 4), "bytes": hp_path.bytes[n],
+                      "timing": "in step" if n == "adamw" else "back-to-back calls"}
     kernels["adamw"]["gparams_s"] = round(hp_path.n_params / (mean_ms["adamw"] / 1e3) / 1e9, 2)
+    bwd_bytes = step_bytes - hp_path.bytes["adamw"]
+    backward_in_step = {"ms": round(bwd_ms, 4),
+                        "GB_s": round(bwd_bytes / (bwd_ms / 1e3) / 1e9, 1),
+                        "frac_of_peak": round(bwd_bytes / (bwd_ms / 1e3) / 1e9 / peak, 4),
+                        "bytes": bwd_bytes,
+                        "sum_of_back_to_back_ms": round(sum(iso.values()), 4)}
     ad_gbs = kernels["adamw"]["GB_s"]
 
     extras = (None if args.no_extras
@@ -349,15 +380,10 @@ def run_ours(args):
             "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(total_ms / K, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {
-                "workload": WORKLOAD_TEXT[args.workload],
-                "bytes_per_step": step_bytes,
-                "adamw_gparams_per_s": kernels["adamw"]["gparams_s"],
-                "l2": "no flush: every launch streams far more than the 129 MB L2",
-                "parallelism": f"replicas x{world}",
-                "wall_s_timed_region": round(wall, 3),
-            },
+            "config": config_block(args.workload, world, step_bytes),
+            "wall_s_timed_region": round(wall, 3),
             "kernels": kernels,
+            "backward_in_step": backward_in_step,
             "extras": extras,
             "roofline": {"bound": "hbm", "achieved": ad_gbs, "peak": peak, "unit": "GB/s",
                          "frac": round(ad_gbs / peak, 4),
@@ -374,29 +400,44 @@ def run_ours(args):
 
 
 # Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, from
-# one single-pass ncu capture of the full step (94.343 GB read + 107.754 GB written;
-# profiles/dram_traffic_full_step_llama7b.md).  Must go back to None whenever the
-# kernel changes until it is captured again.
+# one single-pass ncu capture of the full step (94.343 GB read + 107.754 GB written).
+# Must go back to None whenever the kernel changes until it is captured again.
 ADAMW_TRAFFIC_PER_LAUNCH = 202.097223168e9
+
+
+def config_block(workload, world, step_bytes):
+    """The `config` object of both arms: the workload only, no measured values."""
+    return {"workload": WORKLOAD_TEXT[workload],
+            "bytes_per_step": step_bytes,
+            "l2": "no flush: every launch streams far more than the 129 MB L2",
+            "parallelism": f"replicas x{world}"}
+
+
+def time_loop(fn, reps, name=None):
+    """Mean ms per call of `fn` in a loop of `reps` back-to-back calls (CUDA events
+    on the current stream, after 3 untimed calls), max over ranks."""
+    import torch
+    if name:
+        torch.cuda.nvtx.range_push(name)     # lets a profiler pick this kernel's launches
+    for _ in range(3):
+        fn()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    if name:
+        torch.cuda.nvtx.range_pop()
+    return reduce_over_ranks([s.elapsed_time(e) / reps], "max")[0]
 
 
 def time_extras(hp_path, reps, peak):
     """Per-kernel CUDA-event timing of the kernels that are not part of the step."""
-    import torch
     out = {}
     for name, (fn, nbytes) in hp_path.extras().items():
-        torch.cuda.nvtx.range_push(name)     # lets a profiler pick this kernel's launches
-        for _ in range(3):
-            fn()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        s.record()
-        for _ in range(reps):
-            fn()
-        e.record()
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-        ms = reduce_over_ranks([s.elapsed_time(e) / reps], "max")[0]
+        ms = time_loop(fn, reps, name)
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"ms": round(ms, 4), "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                      "bytes": nbytes}
@@ -510,98 +551,159 @@ def run_e2e(hp_path, K):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def _oracle_rates(adamw_n, sm_rows, ln_rows, reps=1):
-    """Seconds per unit of the CPU oracle on bounded samples (inputs prepared outside)."""
-    import numpy as np
-    import oracle
-    rng = np.random.default_rng(0)
-    th = rng.standard_normal(adamw_n) * 0.02
-    m = np.zeros(adamw_n)
-    v = np.zeros(adamw_n)
-    g = oracle.encode16(rng.standard_normal(adamw_n) * 1e-4 * LOSS_SCALE, "bf16")
-    oracle.adamw_step_f64(th[:4096], m[:4096], v[:4096], g[:4096], "bf16", 1 / LOSS_SCALE, 1, **HP)
-    P = rng.random((sm_rows, SM_COLS))
-    P /= P.sum(axis=1, keepdims=True)
-    dY = rng.standard_normal((sm_rows, SM_COLS))
-    x = rng.standard_normal((ln_rows, LN_D))
-    ldY = rng.standard_normal((ln_rows, LN_D)) * 1e-2
-    mu = x.mean(axis=1)
-    rs = 1.0 / np.sqrt(x.var(axis=1) + 1e-5)
-    gam = np.ones(LN_D)
-    oracle.softmax_bwd_f64(dY[:8], P[:8])
-    oracle.layernorm_bwd_f64(ldY[:8], x[:8], mu[:8], rs[:8], gam)
-    t_a = t_s = t_l = 0.0
-    for r in range(reps):
-        t0 = time.perf_counter()
-        oracle.adamw_step_f64(th, m, v, g, "bf16", 1 / LOSS_SCALE, r + 1, **HP)
-        t1 = time.perf_counter()
-        oracle.softmax_bwd_f64(dY, P)
-        t2 = time.perf_counter()
-        oracle.layernorm_bwd_f64(ldY, x, mu, rs, gam)
-        t3 = time.perf_counter()
-        t_a += t1 - t0
-        t_s += t2 - t1
-        t_l += t3 - t2
-    return (t_a / (reps * adamw_n), t_s / (reps * sm_rows * SM_COLS),
-            t_l / (reps * ln_rows * LN_D), t_a + t_s + t_l)
-
-
 LLAMA7B_PARAMS = 6_738_415_616
 FULL_STEP_BYTES = (adamw_bytes(LLAMA7B_PARAMS) + softmax_bytes(SM_ROWS, SM_COLS, 4)
                    + softmax_bytes(SM_ROWS, SM_COLS, 2) + layernorm_bytes(LN_ROWS, LN_D, 2))
+# The CPU oracle runs on a proportional sample of the full step: 1/64 of the AdamW
+# parameters, of the softmax rows (fp32 and bf16 instances) and of the LayerNorm rows.
+# Every term of the step's byte count divides by 64, so a sample step stands for
+# exactly FULL_STEP_BYTES / 64 algorithmic bytes.
+SAMPLE_DIV = 64
+SAMPLE_BYTES = FULL_STEP_BYTES // SAMPLE_DIV
+assert SAMPLE_BYTES * SAMPLE_DIV == FULL_STEP_BYTES
 
 
-def _full_step_equivalent(per_param, per_sm, per_ln):
-    """GB/s of the full workload at the oracle's per-unit speeds (single thread)."""
-    t = (LLAMA7B_PARAMS * per_param + 2 * SM_ROWS * SM_COLS * per_sm + LN_ROWS * LN_D * per_ln)
-    return FULL_STEP_BYTES / t / 1e9, t
+def host_cpu():
+    """Core count and CPU model of this host (lscpu where available)."""
+    info = {"cpu_count": os.cpu_count()}
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            k, v = k.strip(), v.strip()
+            if k in ("Model name", "Socket(s)", "Architecture", "Thread(s) per core"):
+                info[k.lower().replace("(s)", "s").replace(" ", "_")] = v
+    except Exception:
+        pass
+    return info
+
+
+class OracleSample:
+    """Inputs of one sample step of the CPU oracle, cut into `threads` disjoint slices
+    (contiguous parameter ranges and row blocks).  A sample step calls the float64 C
+    oracle on every slice, one Python thread per slice (ctypes releases the GIL, so
+    the slices run on separate cores), and stands for SAMPLE_BYTES of the workload."""
+
+    def __init__(self, threads):
+        import numpy as np
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.threads = threads
+        rng = np.random.default_rng(0)
+        n = LLAMA7B_PARAMS // SAMPLE_DIV
+        self.th = rng.standard_normal(n) * 0.02
+        self.m = np.zeros(n)
+        self.v = np.zeros(n)
+        self.g = oracle.encode16(rng.standard_normal(n) * 1e-4 * LOSS_SCALE, "bf16")
+        sm_rows = 2 * SM_ROWS // SAMPLE_DIV          # the fp32 and the bf16 instance
+        self.P = rng.random((sm_rows, SM_COLS))
+        self.P /= self.P.sum(axis=1, keepdims=True)
+        self.sdY = rng.standard_normal((sm_rows, SM_COLS))
+        ln_rows = LN_ROWS // SAMPLE_DIV
+        self.x = rng.standard_normal((ln_rows, LN_D))
+        self.ldY = rng.standard_normal((ln_rows, LN_D)) * 1e-2
+        self.mu = self.x.mean(axis=1)
+        self.rs = 1.0 / np.sqrt(self.x.var(axis=1) + 1e-5)
+        self.gam = 1.0 + 0.1 * rng.standard_normal(LN_D)
+        cut = lambda total: [total * i // threads for i in range(threads + 1)]
+        self.pa, self.ps, self.pl = cut(n), cut(sm_rows), cut(ln_rows)
+        self.t = 0
+        self._pool = None
+        if threads > 1:
+            import concurrent.futures as cf
+            self._pool = cf.ThreadPoolExecutor(max_workers=threads)
+
+    def _slice(self, i, t):
+        o = self.oracle
+        a0, a1 = self.pa[i], self.pa[i + 1]
+        o.adamw_step_f64(self.th[a0:a1], self.m[a0:a1], self.v[a0:a1], self.g[a0:a1], "bf16",
+                         1.0 / LOSS_SCALE, t, **HP)
+        s0, s1 = self.ps[i], self.ps[i + 1]
+        if s1 > s0:
+            o.softmax_bwd_f64(self.sdY[s0:s1], self.P[s0:s1])
+        l0, l1 = self.pl[i], self.pl[i + 1]
+        if l1 > l0:
+            o.layernorm_bwd_f64(self.ldY[l0:l1], self.x[l0:l1], self.mu[l0:l1], self.rs[l0:l1],
+                                self.gam)
+
+    def step(self):
+        """One sample step; returns its wall time in seconds."""
+        self.t += 1
+        t0 = time.perf_counter()
+        if self._pool is None:
+            self._slice(0, self.t)
+        else:
+            list(self._pool.map(lambda i: self._slice(i, self.t), range(self.threads)))
+        return time.perf_counter() - t0
+
+    def close(self):
+        if self._pool is not None:
+            self._pool.shutdown()
 
 
 def cpu_baseline(seconds_budget=15.0):
-    adamw_n = 1 << 26
-    per_p, per_s, per_l, spent = _oracle_rates(adamw_n, 8192, 4096, reps=1)
-    reps = max(1, min(4, int(seconds_budget / max(spent, 1e-3))))
-    if reps > 1:
-        per_p, per_s, per_l, spent2 = _oracle_rates(adamw_n, 8192, 4096, reps=reps - 1)
-        spent += spent2
-    gbs, t_full = _full_step_equivalent(per_p, per_s, per_l)
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"float64 C oracle, single thread, on a 2^26-param AdamW slice, "
-                       f"8192x1024 softmax rows and 4096x4096 LayerNorm rows ({spent:.1f} s of "
-                       f"CPU work); per-unit times scaled to the full step "
-                       f"({t_full:.0f} s per step)"),
-            "adamw_ns_per_param": round(per_p * 1e9, 2)}
+    """The oracle on this host's cores: sample steps on every core, then one on a
+    single core.  GB/s = SAMPLE_BYTES per sample step over its wall time."""
+    host = host_cpu()
+    threads = max(1, host["cpu_count"] or 1)
+    smp = OracleSample(threads)
+    smp.step()                                   # untimed: first touch of every page
+    times = []
+    t_end = time.perf_counter() + 0.6 * seconds_budget
+    while len(times) < 3 or (time.perf_counter() < t_end and len(times) < 20):
+        times.append(smp.step())
+    smp.close()
+    ms = statistics.fmean(times) * 1e3
+    one = OracleSample(1)
+    one_ms = one.step() * 1e3
+    gbs = SAMPLE_BYTES / (ms / 1e3) / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": (f"float64 C oracle on 1/{SAMPLE_DIV} of the step ({LLAMA7B_PARAMS // SAMPLE_DIV:,} "
+                       f"AdamW params, {2 * SM_ROWS // SAMPLE_DIV} softmax rows of {SM_COLS}, "
+                       f"{LN_ROWS // SAMPLE_DIV} LayerNorm rows of {LN_D}) cut into {threads} "
+                       f"disjoint slices, one thread each; {len(times)} sample steps of "
+                       f"{ms:.0f} ms"),
+            "ms_per_sample_step": round(ms, 1),
+            "full_step_s_extrapolated": round(ms * SAMPLE_DIV / 1e3, 1),
+            "single_thread": {"value": round(SAMPLE_BYTES / (one_ms / 1e3) / 1e9, 4), "cores": 1,
+                              "ms_per_sample_step": round(one_ms, 1)},
+            "host": host}
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle (float64 C, plain loops) on this host's cores,
+    one sample step (1/SAMPLE_DIV of the workload) per step."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    import oracle
-    oracle.build()
-    adamw_n, sm_rows, ln_rows = 1 << 22, 2048, 1024
+    host = host_cpu()
+    threads = max(1, host["cpu_count"] or 1)
+    smp = OracleSample(threads)
     for _ in range(args.warmup):
-        _oracle_rates(adamw_n, sm_rows, ln_rows)
-    per = [0.0, 0.0, 0.0]
+        smp.step()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        p, s, l, _spent = _oracle_rates(adamw_n, sm_rows, ln_rows)
-        per = [per[0] + p, per[1] + s, per[2] + l]
+    times = [smp.step() for _ in range(args.steps)]
     wall = time.perf_counter() - t0
-    per = [x / args.steps for x in per]
-    gbs, t_full = _full_step_equivalent(*per)
+    smp.close()
+    ms = statistics.fmean(times) * 1e3
+    gbs = SAMPLE_BYTES / (ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_full * 1e3, 1),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": WORKLOAD_TEXT["full"],
-                   "bytes_per_step": FULL_STEP_BYTES,
-                   "parallelism": f"replicas x{world}",
-                   "sampling": "per-unit oracle times on bounded samples, scaled to the full step"},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": (f"each step: 2^22-param AdamW slice, {sm_rows}x1024 softmax, "
-                                    f"{ln_rows}x4096 LayerNorm; {wall:.1f} s wall for the timed steps")},
+        "config": config_block("full", world, FULL_STEP_BYTES),
+        "sample_bytes_per_step": SAMPLE_BYTES,
+        "wall_s_timed_region": round(wall, 3),
+        "full_step_s_extrapolated": round(ms * SAMPLE_DIV / 1e3, 1),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": (f"each step: float64 C oracle on 1/{SAMPLE_DIV} of the full step "
+                                    f"({LLAMA7B_PARAMS // SAMPLE_DIV:,} AdamW params, "
+                                    f"{2 * SM_ROWS // SAMPLE_DIV} softmax rows, "
+                                    f"{LN_ROWS // SAMPLE_DIV} LayerNorm rows) in {threads} "
+                                    f"disjoint slices, one thread each"),
+                         "host": host},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

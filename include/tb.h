@@ -21,6 +21,11 @@
  *     fault inside a kernel surfaces at the caller's next synchronisation.
  *   - Argument errors are reported synchronously, before anything is enqueued,
  *     as a tb_status.  A failed launch reports TB_ERR_CUDA.
+ *   - The softmax, LayerNorm and RMSNorm kernels are launched as programmatic
+ *     dependents of the work before them on `stream`: their blocks may start
+ *     while the previous kernel drains and set up shared memory, but they read
+ *     and write no global memory before every earlier kernel on the stream has
+ *     completed and its writes are visible.  Stream order is kept exactly.
  *   - fp32 pointers must be 4-byte aligned and 16-bit pointers 2-byte aligned
  *     (TB_ERR_MISALIGNED otherwise).  Any larger alignment is optional: 16-byte
  *     aligned buffers take the vectorised path, others a scalar one.
@@ -161,10 +166,12 @@ tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_tensors,
  *   inv_loss_scale  1/loss_scale (exact for a power-of-two scale); > 0
  *   stream          cudaStream_t or NULL
  * The kernel's CTAs claim tiles of the flat parameter space from a counter kept
- * in the plan's device memory (so CTAs on faster SMs take more tiles); the
- * last CTA to finish resets it.  Steps of one plan (plain, clipped or device)
- * must therefore run one after another: on one stream, or ordered by events.
- * They update the same tensors, so they must be ordered in any case.
+ * in the plan's device memory (so CTAs on faster SMs take more tiles).  Each call
+ * enqueues a 16-byte cudaMemsetAsync of that counter on `stream` before the
+ * launch, so every launch starts from zero whatever an earlier launch left
+ * there.  Steps of one plan (plain, clipped or device) must run one after
+ * another: on one stream, or ordered by events.  They update the same tensors
+ * and share the counter, so they must be ordered in any case.
  * Errors: TB_ERR_INVALID_VALUE (plan/hp NULL, step < 1, beta outside [0,1),
  * eps, lr or weight_decay negative or not finite, inv_loss_scale <= 0),
  * TB_ERR_DEVICE (another device is current), TB_ERR_CUDA.
@@ -226,6 +233,17 @@ tb_status tb_adamw_step_clipped(const tb_adamw_plan* plan, int64_t step,
 tb_status tb_adamw_step_device(const tb_adamw_plan* plan, const int64_t* step,
                                const tb_adamw_hparams* hp, float inv_loss_scale,
                                const float* clip, void* stream);
+
+/*
+ * tb_adamw_selftest_stale_counter -- test hook for the tile counter above.  It
+ * waits for `stream`, then writes `next` into the plan's tile counter (and a
+ * nonzero value into the counter's second word) with a synchronous cudaMemcpy,
+ * as a launch that stopped part-way would leave them.  The next step of the
+ * plan must still update and zero every element.  Not for use in training.
+ * Errors: TB_ERR_INVALID_VALUE (not a live plan), TB_ERR_DEVICE, TB_ERR_CUDA.
+ */
+tb_status tb_adamw_selftest_stale_counter(const tb_adamw_plan* plan, uint64_t next,
+                                          void* stream);
 
 /* Free a plan (NULL is accepted; a pointer that is not a live plan, e.g. one
  * destroyed already, returns TB_ERR_INVALID_VALUE).  Synchronises nothing: the

@@ -30,7 +30,7 @@ EXPORTS = ("tb_status_string", "tb_version", "tb_device_error", "tb_adamw_plan_c
            "tb_softmax_bwd_causal", "tb_rmsnorm_bwd_workspace_size", "tb_rmsnorm_bwd",
            "tb_adamw_grad_norm_workspace_size", "tb_adamw_grad_norm", "tb_adamw_step_clipped",
            "tb_cast_to_f32", "tb_cast_from_f32", "tb_layernorm_bwd_selftest_timeout",
-           "tb_adamw_step_device")
+           "tb_adamw_step_device", "tb_adamw_selftest_stale_counter")
 
 
 class TbError(RuntimeError):
@@ -97,6 +97,8 @@ def _load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.tb_adamw_step_device.restype = i32
     lib.tb_layernorm_bwd_selftest_timeout.argtypes = [i64, vp]
     lib.tb_layernorm_bwd_selftest_timeout.restype = i32
+    lib.tb_adamw_selftest_stale_counter.argtypes = [vp, ctypes.c_uint64, vp]
+    lib.tb_adamw_selftest_stale_counter.restype = i32
     return lib
 
 
@@ -245,6 +247,12 @@ def tb_adamw_step_device(plan: AdamWPlan, step: torch.Tensor, lr: float, beta1: 
 
 def tb_adamw_plan_destroy(plan: AdamWPlan) -> None:
     plan.close()
+
+
+def tb_adamw_selftest_stale_counter(plan: AdamWPlan, next_tile: int, stream=None) -> None:
+    """Test hook: leaves a stale value in the plan's tile counter (synchronises)."""
+    _check("tb_adamw_selftest_stale_counter",
+           lib.tb_adamw_selftest_stale_counter(plan.handle, int(next_tile), _stream(stream)))
 
 
 def tb_adamw_grad_norm_workspace_size(plan: AdamWPlan) -> int:

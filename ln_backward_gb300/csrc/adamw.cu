@@ -60,13 +60,14 @@ struct alignas(16) TensorEntry {
 };
 static_assert(sizeof(TensorEntry) == 64, "table entry is one 64-byte line");
 
-// Tile counter of a plan's step kernel, in device memory after the table.  It is
-// zero when a launch starts; the last CTA to finish sets it back to zero, so
-// launches of one plan must be stream-ordered (they update the same tensors).
+// Tile counter of a plan's step kernel, in device memory after the table.  The
+// host clears it with a 16-byte memset enqueued on the launch's stream right
+// before every launch, so it is zero when a launch starts whatever an earlier
+// launch left in it.  Launches of one plan must be stream-ordered (they update
+// the same tensors and share this counter).
 struct alignas(16) TileQueue {
     unsigned long long next;   // tiles claimed so far beyond the first one of each CTA
-    unsigned int done;         // CTAs finished
-    unsigned int pad;
+    unsigned long long pad;
 };
 
 // Per-step scalars, hoisted on the host.
@@ -292,12 +293,6 @@ adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t
         }
         __syncthreads();
         tile = s_tile[(it + 1) & 1];
-    }
-    // Every CTA's last claim came back past the end; the last CTA out resets the
-    // counter for the next launch.
-    if (threadIdx.x == 0 && atomicAdd(&q->done, 1u) == gridDim.x - 1) {
-        q->next = 0ull;
-        q->done = 0u;
     }
 }
 
@@ -633,6 +628,11 @@ extern "C" tb_status tb_adamw_plan_create(const tb_tensor_desc* tensors, int n_t
 
 namespace tb {
 namespace {
+// The step kernel's tile counter: the slot after the plan's device table.
+TileQueue* tile_queue(const tb_adamw_plan* plan) {
+    return reinterpret_cast<TileQueue*>(plan->d_table + plan->n_tensors);
+}
+
 // step_dev non-null: the step is read on the device when the kernel runs and
 // `step` is ignored.
 tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adamw_hparams* hp,
@@ -674,10 +674,14 @@ tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adam
     const TensorEntry* tab = plan->d_table;
     int nt = plan->n_tensors;
     int64_t tu = plan->total_units;
-    TileQueue* q = reinterpret_cast<TileQueue*>(plan->d_table + plan->n_tensors);
+    TileQueue* q = tile_queue(plan);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The counter starts every launch at zero, even after a launch that did not run
+    // to its end.
+    if (cudaMemsetAsync(q, 0, sizeof(TileQueue), st) != cudaSuccess) return TB_ERR_CUDA;
     void* args[] = {&tab, &nt, &tu, &n_tiles, &s, &clip, &step_dev, &err, &q};
     if (cudaLaunchKernel(step_kernel(plan->grad_dtype, plan->copy_dtype, plan->has_copy), dim3(grid),
-                         dim3(kThreads), args, 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                         dim3(kThreads), args, 0, st) != cudaSuccess)
         return TB_ERR_CUDA;
     return TB_OK;
 }
@@ -749,6 +753,21 @@ extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_los
                                                             plan->total_units > 0 ? grid : 0,
                                                             max_norm, out);
     return launch_status();
+}
+
+extern "C" tb_status tb_adamw_selftest_stale_counter(const tb_adamw_plan* plan,
+                                                     uint64_t next, void* stream) {
+    using namespace tb;
+    if (!plan_live(plan)) return TB_ERR_INVALID_VALUE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TB_ERR_CUDA;
+    if (dev != plan->device) return TB_ERR_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TB_ERR_CUDA;
+    const TileQueue stale = {static_cast<unsigned long long>(next), ~0ull};
+    if (cudaMemcpy(tile_queue(plan), &stale, sizeof(stale), cudaMemcpyHostToDevice) != cudaSuccess)
+        return TB_ERR_CUDA;
+    return TB_OK;
 }
 
 extern "C" tb_status tb_adamw_plan_destroy(tb_adamw_plan* plan) {

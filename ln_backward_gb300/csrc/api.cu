@@ -1,5 +1,7 @@
-// api.cu -- status strings, version, per-device property cache and the
-// device-side error word.
+// api.cu -- status strings, version, per-device property cache, the identity of
+// the current CUDA context and the device-side error word.
+#include <cuda.h>
+
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -13,8 +15,51 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 bool g_have[kMaxDevices] = {};
 DeviceInfo g_info[kMaxDevices];
-int* g_err_ptr[kMaxDevices] = {};
+CachedAddress g_err_addr[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+std::once_flag g_ctx_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
 }  // namespace
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, [] {
+        auto resolve = [](const char* name) -> void* {
+            void* f = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess) {
+                cudaGetLastError();   // clear this call's own error only
+                return nullptr;
+            }
+            return q == cudaDriverEntryPointSuccess ? f : nullptr;
+        };
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(resolve("cuCtxGetCurrent"));
+        g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(resolve("cuCtxGetId"));
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+void* CachedAddress::get(const void* symbol) {
+    const unsigned long long id = current_context_id();
+    if (id != 0 && id == ctx_id) return ptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    // The lookup creates the context if there was none yet: key on the id it has now.
+    ctx_id = current_context_id();
+    ptr = ctx_id != 0 ? p : nullptr;
+    return p;
+}
 
 // Set by kernels whose bounded waits give up; read by tb_device_error.
 __device__ int g_device_error = 0;
@@ -42,30 +87,30 @@ int* device_error_word() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_err_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        g_err_ptr[dev] = static_cast<int*>(p);
-    }
-    return g_err_ptr[dev];
+    return static_cast<int*>(g_err_addr[dev].get(&g_device_error));
 }
 
 namespace {
 std::mutex g_occ_mu;
-std::map<std::tuple<int, const void*, int, size_t>, int> g_occ;   // -> CTAs per SM
-std::map<std::pair<int, const void*>, size_t> g_smem_limit;        // -> limit set so far
+// Keyed on the context id as well: a kernel's raised shared-memory limit belongs
+// to the context it was set in.
+std::map<std::tuple<int, unsigned long long, const void*, int, size_t>, int> g_occ;  // -> CTAs per SM
+std::map<std::tuple<int, unsigned long long, const void*>, size_t> g_smem_limit;     // -> limit set
 }  // namespace
 
 int resident_ctas_per_sm(const void* kernel, int threads, size_t dyn_smem) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_occ_mu);
     try {
-        const auto key = std::make_tuple(dev, kernel, threads, dyn_smem);
+        const auto key = std::make_tuple(dev, ctx, kernel, threads, dyn_smem);
         const auto it = g_occ.find(key);
-        if (it != g_occ.end()) return it->second;
+        if (it != g_occ.end() && ctx != 0) return it->second;
         if (dyn_smem > 48 * 1024) {
-            size_t& lim = g_smem_limit[std::make_pair(dev, kernel)];
+            // without a context id nothing is cached: the limit is set every time
+            size_t unused = 0;
+            size_t& lim = ctx != 0 ? g_smem_limit[std::make_tuple(dev, ctx, kernel)] : unused;
             if (lim < dyn_smem) {
                 if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)dyn_smem) != cudaSuccess)
@@ -77,7 +122,7 @@ int resident_ctas_per_sm(const void* kernel, int threads, size_t dyn_smem) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) !=
             cudaSuccess)
             return 0;
-        g_occ.emplace(key, per_sm);
+        if (ctx != 0) g_occ.emplace(key, per_sm);
         return per_sm;
     } catch (...) {
         return 0;

@@ -114,15 +114,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-// Programmatic dependent launch: the primary grid allows its dependent to be
-// scheduled; the dependent waits until the primary has completed and flushed.
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -295,8 +286,12 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&bars[s]), 1);
         mbar_init_fence();
         pol = evict_first_policy();
-        for (; issued < ngroups && issued < stages; ++issued) issue(issued, (int)issued);
     }
+    // Up to here only shared memory was touched: the previous kernel may still be
+    // running (programmatic launch).  Every global access comes after this wait.
+    pdl_wait();
+    if (tid == 0)
+        for (; issued < ngroups && issued < stages; ++issued) issue(issued, (int)issued);
 
     constexpr int NP = Pairs<Fmt>::kN;
     float2 g[NV][NP], acc_g[NV][NP], acc_b[NV][NP];
@@ -444,7 +439,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         return;
     }
     // Let the column reduction launch; it waits for this grid to finish before reading.
-    griddep_launch_dependents();
+    pdl_trigger();
 
     float* pg = partials + (size_t)blockIdx.x * (kRms ? 1 : 2) * D;
     float* pb = pg + D;
@@ -472,6 +467,7 @@ ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename 
                          const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
                          float* __restrict__ partials, int64_t rows, int64_t D, int64_t rows_per_cta) {
     __shared__ float red[2][2][kMaxWarps];
+    pdl_wait();   // the previous kernel has completed (programmatic launch)
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     float* pg = partials + (size_t)blockIdx.x * (kRms ? 1 : 2) * D;
@@ -519,7 +515,7 @@ ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename 
             if (!kRms) pb[j] += dyv;
         }
     }
-    griddep_launch_dependents();
+    pdl_trigger();
 }
 
 // ------------------------------------------------------------------ column reduction
@@ -536,7 +532,8 @@ __global__ void __launch_bounds__(kColThreads, 2)
 ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t W, int64_t D,
                      float* __restrict__ dgamma, float* __restrict__ dbeta) {
     __shared__ float sm[kColGroups][33];
-    griddep_wait();   // the row kernel (if any) has completed and flushed its partials
+    pdl_trigger();   // the next kernel may be placed now; it waits for this one to complete
+    pdl_wait();      // the row kernel (if any) has completed and flushed its partials
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t c = (int64_t)blockIdx.x * 32 + lane;
     float acc = 0.f;
@@ -568,17 +565,8 @@ ln_bwd_colsum_kernel(const float* __restrict__ partials, int G, int64_t W, int64
 // drains (programmatic dependent launch); it waits inside for the row kernel.
 cudaError_t launch_colsum(const float* ws, int G, int64_t W, int64_t D, float* dgamma,
                           float* dbeta, cudaStream_t st) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((W + 31) / 32));
-    cfg.blockDim = dim3(kColThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ln_bwd_colsum_kernel, ws, G, W, D, dgamma, dbeta);
+    return launch_pdl(ln_bwd_colsum_kernel, dim3((unsigned)((W + 31) / 32)), dim3(kColThreads), 0,
+                      st, ws, G, W, D, dgamma, dbeta);
 }
 
 // ------------------------------------------------------------------ launch planning
@@ -719,9 +707,9 @@ struct RingLaunchOps {
         static int run(const LnPlan& p, const T* dy, const T* x, const float* mean,
                        const float* inv_std, const float* gamma, T* dx, float* ws, int64_t rows,
                        int D, int* err, cudaStream_t st) {
-            ln_bwd_rows_ring_kernel<Fmt, NV, R, kRms><<<p.grid, p.threads, p.smem, st>>>(
-                dy, x, mean, inv_std, gamma, dx, ws, rows, D, p.stages, p.rows_per_cta, err,
-                p.wait_limit_ns, p.withhold_copies);
+            launch_pdl(ln_bwd_rows_ring_kernel<Fmt, NV, R, kRms>, dim3((unsigned)p.grid),
+                       dim3((unsigned)p.threads), p.smem, st, dy, x, mean, inv_std, gamma, dx, ws,
+                       rows, D, p.stages, p.rows_per_cta, err, p.wait_limit_ns, p.withhold_copies);
             return 0;
         }
     };
@@ -743,11 +731,11 @@ void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* me
             with_ring_variant<Fmt, RingLaunchOps<false>::template Launch>(
                 p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
     } else if (rms) {
-        ln_bwd_rows_plain_kernel<Fmt, true><<<p.grid, p.threads, 0, st>>>(
-            dy, xx, mean, inv_std, gamma, dx, ws, rows, D, p.rows_per_cta);
+        launch_pdl(ln_bwd_rows_plain_kernel<Fmt, true>, dim3((unsigned)p.grid), dim3((unsigned)p.threads),
+                   0, st, dy, xx, mean, inv_std, gamma, dx, ws, rows, D, p.rows_per_cta);
     } else {
-        ln_bwd_rows_plain_kernel<Fmt, false><<<p.grid, p.threads, 0, st>>>(
-            dy, xx, mean, inv_std, gamma, dx, ws, rows, D, p.rows_per_cta);
+        launch_pdl(ln_bwd_rows_plain_kernel<Fmt, false>, dim3((unsigned)p.grid), dim3((unsigned)p.threads),
+                   0, st, dy, xx, mean, inv_std, gamma, dx, ws, rows, D, p.rows_per_cta);
     }
 }
 
@@ -842,18 +830,15 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) float g_ln_scratch[kNoAllocScratchFloats];
 
 std::mutex g_scratch_mu;
-float* g_scratch_ptr[kNoAllocMaxDevices] = {};
+CachedAddress g_scratch_addr[kNoAllocMaxDevices];
 
 // Device address of g_ln_scratch on `dev` (which must be current); nullptr on error.
+// Looked up once per device with cudaGetSymbolAddress, and again only if the
+// device's context has changed since (after a device reset).
 float* noalloc_scratch(int dev) {
     if (dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_ln_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = static_cast<float*>(p);
-    }
-    return g_scratch_ptr[dev];
+    return static_cast<float*>(g_scratch_addr[dev].get(&g_ln_scratch));
 }
 }  // namespace
 }  // namespace tb

@@ -95,6 +95,8 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
     // fp16 at up to 4); the scalar form elsewhere.
     constexpr bool kPacked = std::is_same<Fmt, BF16>::value ? VPL >= 8
                            : std::is_same<Fmt, F16>::value ? VPL <= 4 : false;
+    pdl_wait();      // the previous kernel has completed (programmatic launch)
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int sub = lane / G;        // row slot inside the warp
     const int gl = lane % G;         // lane inside the group
@@ -180,6 +182,8 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
     constexpr int E = Vec<Fmt>::kElems;
     constexpr int kWarps = kCtaThreads / 32;
     __shared__ float red[2][kWarps];
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int parity = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
@@ -236,6 +240,8 @@ softmax_bwd_twopass_kernel(const typename Fmt::T* __restrict__ dY,
                            int64_t period, int64_t offset) {
     constexpr int kWarps = kTwoPassThreads / 32;
     __shared__ float red[2][kWarps];
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int parity = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
@@ -272,8 +278,10 @@ tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, in
     if (per_sm == 0) return TB_ERR_CUDA;
     const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * per_sm));
-    softmax_bwd_group_kernel<Fmt, G, VPL><<<(unsigned)grid, 256, 0, st>>>(
-        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv, period, offset);
+    if (launch_pdl(softmax_bwd_group_kernel<Fmt, G, VPL>, dim3((unsigned)grid), dim3(256), 0, st,
+                   static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
+                   static_cast<uint4*>(dX), rows, nv, period, offset) != cudaSuccess)
+        return TB_ERR_CUDA;
     return launch_status();
 }
 
@@ -284,9 +292,10 @@ tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int 
         reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, VPL>), kCtaThreads, 0);
     if (per_sm == 0) return TB_ERR_CUDA;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * per_sm));
-    softmax_bwd_cta_kernel<Fmt, VPL><<<(unsigned)grid, kCtaThreads, 0, st>>>(
-        static_cast<const uint4*>(dY), static_cast<const uint4*>(P), static_cast<uint4*>(dX), rows, nv,
-        period, offset);
+    if (launch_pdl(softmax_bwd_cta_kernel<Fmt, VPL>, dim3((unsigned)grid), dim3(kCtaThreads), 0, st,
+                   static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
+                   static_cast<uint4*>(dX), rows, nv, period, offset) != cudaSuccess)
+        return TB_ERR_CUDA;
     return launch_status();
 }
 
@@ -312,9 +321,10 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
         reinterpret_cast<const void*>(&softmax_bwd_twopass_kernel<Fmt>), kTwoPassThreads, 0);
     if (per_sm == 0) return TB_ERR_CUDA;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * per_sm));
-    softmax_bwd_twopass_kernel<Fmt><<<(unsigned)grid, kTwoPassThreads, 0, st>>>(
-        static_cast<const T*>(dY), static_cast<const T*>(P), static_cast<T*>(dX), rows, cols, period,
-        offset);
+    if (launch_pdl(softmax_bwd_twopass_kernel<Fmt>, dim3((unsigned)grid), dim3(kTwoPassThreads), 0,
+                   st, static_cast<const T*>(dY), static_cast<const T*>(P), static_cast<T*>(dX),
+                   rows, cols, period, offset) != cudaSuccess)
+        return TB_ERR_CUDA;
     return launch_status();
 }
 

@@ -45,6 +45,20 @@ struct DeviceInfo {
 // Fills `info` for the current device; returns false on a CUDA error.
 bool current_device_info(int* device, DeviceInfo* info);
 
+// Unique id of the CUDA context current on this thread (0 when there is none or it
+// cannot be read).  Ids are never reused within a process.
+unsigned long long current_context_id();
+
+// Device address of a __device__ variable in the current context, looked up with
+// cudaGetSymbolAddress and cached against the context's id: a device reset ends
+// the context, and the next context may load the module at other addresses, so a
+// new id means a new lookup.  Not thread-safe by itself (callers hold a lock).
+struct CachedAddress {
+    unsigned long long ctx_id = 0;
+    void* ptr = nullptr;
+    void* get(const void* symbol);   // nullptr on a CUDA error
+};
+
 // Address of the device-side error word on the current device (nullptr on error).
 int* device_error_word();
 
@@ -56,6 +70,38 @@ int resident_ctas_per_sm(const void* kernel, int threads, size_t dyn_smem);
 
 inline tb_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels of this library are launched as programmatic dependents of the work
+// before them in the stream: their CTAs may be placed on the SMs while the
+// previous kernel drains, do their set-up (shared memory, barriers), and then
+// wait in pdl_wait() until every prerequisite grid has completed and its memory
+// is visible.  No global memory is read or written before that wait.  Launched
+// without the attribute (or after work that is not a kernel), the wait returns
+// at once.  pdl_trigger() lets the next programmatic dependent be scheduled
+// early; that kernel still waits for this one to complete before it touches
+// memory, so the trigger may be placed anywhere.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kernel` on `st` with the programmatic-stream-serialization attribute.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 // ---------------------------------------------------------------- device helpers

@@ -128,6 +128,8 @@ def test_pointers_that_are_not_live_plans_are_never_dereferenced(tb):
     assert lib.tb_adamw_grad_norm(bogus, 1.0, 1.0, 0x2000, 0x3000, 64, None) == INVALID
     assert lib.tb_adamw_step_device(bogus, 0x2000, ctypes.byref(hp), 1.0, None, None) == INVALID
     assert lib.tb_adamw_step_device(None, None, ctypes.byref(hp), 1.0, None, None) == INVALID
+    assert lib.tb_adamw_selftest_stale_counter(bogus, 5, None) == INVALID
+    assert lib.tb_adamw_selftest_stale_counter(None, 5, None) == INVALID
     assert lib.tb_adamw_plan_destroy(bogus) == INVALID
 
 

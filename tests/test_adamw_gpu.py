@@ -100,11 +100,16 @@ def _run(tb, synth, st, steps, idx, first_step=1, hp=None):
     # (b) within one 16-bit ulp of the oracle's master rounded to nearest even, or --
     #     where theta has decayed far below its starting scale -- the rounding of a
     #     value within the theta tolerance (1e-5, floored at rms) of the oracle
-    tol = 1e-5 * np.maximum(np.abs(th), np.sqrt(np.mean(th * th)))
+    rms = np.sqrt(np.mean(th * th))
+    tol = 1e-5 * np.maximum(np.abs(th), rms)
     ok, n_tol, dmax = lowp_check(got_c, th, ckind, err=tol)
+    ok_1ulp, _, _ = lowp_check(got_c, th, ckind)
+    widened = ok & ~ok_1ulp          # pass only under the widened rule
     return dict(theta=floored_rel(got_th, th), m=floored_rel(got_m, m), v=floored_rel(got_v, v),
                 copy_exact=copy_exact, copy_ok=bool(ok.all()), copy_max_ulps=dmax,
-                copy_beyond_1ulp=n_tol)
+                copy_beyond_1ulp=n_tol,
+                copy_widened_max_theta_over_rms=float(np.max(np.abs(th[widened])) / rms)
+                if widened.any() else 0.0)
 
 
 def _assert_within_targets(err):
@@ -113,6 +118,11 @@ def _assert_within_targets(err):
     assert err["v"] <= 1e-5, err
     assert err["copy_exact"], err
     assert err["copy_ok"], err
+    # The widened copy rule covers only parameters that have decayed below the rms
+    # of their tensor set: a copy more than 1 ulp off anywhere else fails.
+    assert err["copy_widened_max_theta_over_rms"] < 1.0, err
+    print(f"copies beyond 1 ulp (widened rule): {err['copy_beyond_1ulp']}, "
+          f"largest |theta|/rms among them: {err['copy_widened_max_theta_over_rms']:.3g}")
 
 
 # ----------------------------------------------------------------------------- tiny config

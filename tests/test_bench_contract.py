@@ -34,14 +34,18 @@ def test_reference_arm_line_has_every_contract_key():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
-    # the same workload and metric as the GPU arm
+    # the same workload, metric and config object as the GPU arm
     import bench
     assert line["metric"] == bench.METRIC
-    assert line["config"]["workload"] == bench.WORKLOAD_TEXT["full"]
+    assert line["config"] == bench.config_block("full", 1, bench.FULL_STEP_BYTES)
     assert line["config"]["bytes_per_step"] == bench.FULL_STEP_BYTES
-    # value and ms_per_step describe the same step
-    assert abs(line["value"] - bench.FULL_STEP_BYTES / (line["ms_per_step"] / 1e3) / 1e9) \
+    # a step is one sample step, actually timed: value and ms_per_step describe it, and
+    # the timed steps fit in the measured wall time of the timed region
+    assert line["sample_bytes_per_step"] * bench.SAMPLE_DIV == bench.FULL_STEP_BYTES
+    assert abs(line["value"] - line["sample_bytes_per_step"] / (line["ms_per_step"] / 1e3) / 1e9) \
         <= 1e-3 * line["value"] + 1e-4
+    assert line["steps"] * line["ms_per_step"] / 1e3 <= line["wall_s_timed_region"] * 1.01
+    assert cb["cores"] == cb["host"]["cpu_count"]
 
 
 import pytest  # noqa: E402
@@ -65,6 +69,13 @@ def test_gpu_arm_line_has_every_contract_key():
     ck = line["clocks"]
     assert ck["sm_mhz"] > 0 and ck["sm_max_mhz"] > 0 and isinstance(ck["reasons"], list)
     assert line["gpu_launches"] == 5 * line["steps"]     # AdamW, 2 softmax, LayerNorm rows + columns
+    ks = line["kernels"]
+    assert set(ks) == {"adamw", "softmax_f32", "softmax_bf16", "layernorm_bf16"}
+    assert ks["adamw"]["timing"] == "in step"
+    bw = line["backward_in_step"]
+    assert bw["ms"] > 0 and bw["bytes"] == sum(ks[n]["bytes"] for n in ks if n != "adamw")
+    # the backward kernels timed alone add up to about their share of the step
+    assert 0.7 < bw["sum_of_back_to_back_ms"] / bw["ms"] < 1.3
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0

@@ -6,6 +6,9 @@
   word and returns, and the context stays usable for the next call.
 * A destroyed AdamW plan is rejected by every call that takes a plan, without
   being dereferenced.
+* A stale value in an AdamW plan's tile counter (what a launch that stopped
+  part-way would leave) is planted from the host; the next step still updates and
+  zeroes every element, bit for bit as a plan whose counter was never touched.
 """
 import ctypes
 
@@ -86,3 +89,29 @@ def test_destroyed_plan_is_rejected(tb, synth):
     # a pointer that was never a plan
     assert lib.tb_adamw_step(ctypes.c_void_p(0x1000), 1, ctypes.byref(hp), 1.0,
                              None) == TB_ERR_INVALID_VALUE
+
+
+def test_stale_tile_counter_is_cleared_before_the_next_step(tb, synth):
+    # 3 tensors, 8.4 M params: about 520 tiles of 16,384 elements, more than the
+    # persistent grid, so CTAs claim tiles from the counter
+    shapes = [("a", (4096, 1024)), ("b", (4099,)), ("c", (1024, 4095))]
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    runs = []
+    for stale in (None, 1, 300, 2 ** 40):
+        st = synth.make_adamw_state(shapes, seed=33, device="cuda")
+        k = len(shapes)
+        plan = tb.tb_adamw_plan_create(*[[st.tensor(a, i) for i in range(k)]
+                                         for a in ("theta", "m", "v", "grad", "copy")])
+        for t in (1, 2):
+            synth.fill_grads(st, t)
+            if stale is not None:
+                tb.tb_adamw_selftest_stale_counter(plan, stale)
+            tb.tb_adamw_step(plan, t, inv_loss_scale=1.0 / 65536.0, **hp)
+            torch.cuda.synchronize()
+            for i in range(k):
+                assert int(torch.count_nonzero(st.tensor("grad", i))) == 0, (stale, t, i)
+        runs.append((st.theta.clone(), st.m.clone(), st.v.clone(), st.copy.clone()))
+        plan.close()
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            assert torch.equal(a, b)

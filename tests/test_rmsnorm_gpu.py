@@ -55,6 +55,9 @@ def _err_bound(x, dY, rs, gamma):
 
 
 def check(x, dY, rs, gamma, dX, dg):
+    """fp32 dX must meet the 1e-4 floored relative target.  Only for D <= 2 may it
+    instead sit within the derived fp32 error bound: at D = 1 the exact dX is
+    proportional to eps (x_hat is +-1 up to eps) and cancels far below its terms."""
     xn, dYn = x.double().cpu().numpy(), dY.double().cpu().numpy()
     rn, gn = rs.double().cpu().numpy(), gamma.double().cpu().numpy()
     rdx, rdg = oracle.rmsnorm_bwd_f64(dYn, xn, rn, gn)
@@ -62,7 +65,9 @@ def check(x, dY, rs, gamma, dX, dg):
     if dX.dtype == torch.float32:
         got = dX.double().cpu().numpy()
         e = floored_rel(got, rdx)
-        if e > 1e-4:
+        if x.shape[1] > 2:
+            assert e <= 1e-4, f"dX floored relative error {e}"
+        elif e > 1e-4:
             ok = within_bound(got, rdx, _err_bound(xn, dYn, rn, gn))
             assert ok.all(), f"dX floored relative error {e}, {(~ok).sum()} beyond the fp32 bound"
     else:
