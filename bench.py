@@ -399,10 +399,14 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-# Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, from
-# one single-pass ncu capture of the full step (94.343 GB read + 107.754 GB written).
-# Must go back to None whenever the kernel changes until it is captured again.
-ADAMW_TRAFFIC_PER_LAUNCH = 202.097223168e9
+# Per-launch DRAM bytes (read + write) of the AdamW kernel at the 7B workload, or None
+# while no capture of the current kernel exists.  Must go back to None whenever the
+# kernel changes until it is captured again.  From one ncu capture of the kernel on
+# the GPT-2-small table (124,439,808 params): 1,742,311,168 B read, 1,930,455,552 B
+# written.  Reads scale with the parameter count (14.0012 B/param); writes are
+# 16 B/param less a fixed 60,581,376 B still dirty in L2 when the kernel ends.  At
+# 6,738,415,616 params: 94.346 + 107.754 GB.
+ADAMW_TRAFFIC_PER_LAUNCH = 202.100218406e9
 
 
 def config_block(workload, world, step_bytes):

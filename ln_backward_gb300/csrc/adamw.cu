@@ -19,8 +19,11 @@
 // few per cent slower than others; with a fixed share per CTA the step would
 // end with them).  The update is elementwise, so which CTA takes which tile
 // changes no result bit.  Each CTA follows its tensor with a forward scan of
-// the table.  Every thread moves 2 units per step with 128-bit evict-first
-// loads and stores: 14 B read and 16 B written per element, one HBM pass.
+// the table.  A warp walks blocks of 256 elements, each lane taking two 4-element
+// chunks 128 elements apart, so every warp access covers whole 32-byte sectors:
+// 16-byte evict-first accesses for fp32, 8-byte ones for the 16-bit arrays, two
+// blocks in flight per warp.  14 B read and 16 B written per element, one HBM
+// pass.
 // Tensors whose five pointers are not all 16-byte aligned, and the last
 // partial unit of a tensor, take a scalar path.
 #include <algorithm>
@@ -40,7 +43,7 @@ namespace {
 
 constexpr int kUnit = 8;        // elements per unit
 constexpr int kThreads = 256;   // threads per CTA
-constexpr int kUnroll = 2;      // units in flight per thread
+constexpr int kUnroll = 2;      // 256-element blocks in flight per warp (16 elements per thread)
 constexpr int64_t kTileUnits = (int64_t)kThreads * kUnroll * 4;   // 16384 elements
 // The gradient-norm pass reads 2 bytes per element instead of 30: it takes 4x
 // longer tiles (65,536 elements) so a CTA spends less of its time between tiles.
@@ -138,7 +141,29 @@ __device__ __forceinline__ void zero_segment(const TensorEntry& t, int64_t a, in
     }
 }
 
-// Units [a, e) of one tensor (local unit indices).
+// 4 consecutive 16-bit values (8 bytes) as fp32, and back (round to nearest even),
+// with the streaming cache policy.
+template <class Fmt>
+__device__ __forceinline__ void ld4_16(const void* p, float (&f)[4]) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+    const typename Fmt::T* h = reinterpret_cast<const typename Fmt::T*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = Fmt::to_f32(h[i]);
+}
+template <class Fmt>
+__device__ __forceinline__ void st4_16(void* p, const float (&f)[4]) {
+    uint2 u;
+    typename Fmt::T* h = reinterpret_cast<typename Fmt::T*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = Fmt::from_f32(f[i]);
+    __stcs(reinterpret_cast<uint2*>(p), u);
+}
+
+// Units [a, e) of one tensor (local unit indices).  A warp walks blocks of 256
+// elements (32 units); lane l takes the 4-element chunks [4l, 4l+4) and
+// [128+4l, 128+4l+4) of a block.  So every fp32 access of a warp covers 512
+// contiguous bytes and every 16-bit access 256: each 32-byte sector a warp
+// instruction touches is used whole.  kUnroll blocks per warp are in flight.
 template <class G, class C>
 __device__ __forceinline__ void process_segment(const TensorEntry& t, int64_t a, int64_t e,
                                                 const Scalars& s) {
@@ -147,59 +172,53 @@ __device__ __forceinline__ void process_segment(const TensorEntry& t, int64_t a,
     const int64_t n = t.n;
     const int64_t full = n / kUnit;   // units holding 8 valid elements
     if (t.vec_ok) {
-        const int64_t fe = e < full ? e : full;
-        for (int64_t base = a + threadIdx.x; base < fe; base += (int64_t)kThreads * kUnroll) {
-            float th[kUnroll][8], mm[kUnroll][8], vv[kUnroll][8], gg[kUnroll][8];
-            bool act[kUnroll];
+        constexpr int kWarps = kThreads / 32;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        // elements [e0, e1): e0 and e1 are multiples of 8, every chunk start a multiple
+        // of 4, so a chunk that starts below e1 ends at or below it
+        const int64_t e0 = a * kUnit, e1 = (e < full ? e : full) * kUnit;
+        for (int64_t blk = e0 + (int64_t)warp * 256 * kUnroll; blk < e1;
+             blk += (int64_t)kWarps * 256 * kUnroll) {
+            float th[kUnroll][2][4], mm[kUnroll][2][4], vv[kUnroll][2][4], gg[kUnroll][2][4];
+            bool act[kUnroll][2];
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
-                const int64_t uu = base + (int64_t)j * kThreads;
-                act[j] = uu < fe;
-                if (act[j]) {
-                    const int64_t i0 = uu * kUnit;
-                    float4 a0 = ld_stream_f4(t.p + i0), a1 = ld_stream_f4(t.p + i0 + 4);
-                    float4 b0 = ld_stream_f4(t.m + i0), b1 = ld_stream_f4(t.m + i0 + 4);
-                    float4 c0 = ld_stream_f4(t.v + i0), c1 = ld_stream_f4(t.v + i0 + 4);
-                    uint4 gr;
-                    float4 gf0, gf1;
-                    if constexpr (kF32Grad<G>) {
-                        gf0 = ld_stream_f4(static_cast<const float*>(t.g) + i0);
-                        gf1 = ld_stream_f4(static_cast<const float*>(t.g) + i0 + 4);
-                    } else {
-                        gr = ld_stream_u4(static_cast<const GT*>(t.g) + i0);
-                    }
-                    th[j][0] = a0.x; th[j][1] = a0.y; th[j][2] = a0.z; th[j][3] = a0.w;
-                    th[j][4] = a1.x; th[j][5] = a1.y; th[j][6] = a1.z; th[j][7] = a1.w;
-                    mm[j][0] = b0.x; mm[j][1] = b0.y; mm[j][2] = b0.z; mm[j][3] = b0.w;
-                    mm[j][4] = b1.x; mm[j][5] = b1.y; mm[j][6] = b1.z; mm[j][7] = b1.w;
-                    vv[j][0] = c0.x; vv[j][1] = c0.y; vv[j][2] = c0.z; vv[j][3] = c0.w;
-                    vv[j][4] = c1.x; vv[j][5] = c1.y; vv[j][6] = c1.z; vv[j][7] = c1.w;
-                    if constexpr (kF32Grad<G>) {
-                        gg[j][0] = gf0.x; gg[j][1] = gf0.y; gg[j][2] = gf0.z; gg[j][3] = gf0.w;
-                        gg[j][4] = gf1.x; gg[j][5] = gf1.y; gg[j][6] = gf1.z; gg[j][7] = gf1.w;
-                    } else {
-                        unpack8<G>(gr, gg[j]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t i0 = blk + j * 256 + h * 128 + 4 * lane;
+                    act[j][h] = i0 < e1;
+                    if (act[j][h]) {
+                        const float4 a0 = ld_stream_f4(t.p + i0), b0 = ld_stream_f4(t.m + i0),
+                                     c0 = ld_stream_f4(t.v + i0);
+                        th[j][h][0] = a0.x; th[j][h][1] = a0.y; th[j][h][2] = a0.z; th[j][h][3] = a0.w;
+                        mm[j][h][0] = b0.x; mm[j][h][1] = b0.y; mm[j][h][2] = b0.z; mm[j][h][3] = b0.w;
+                        vv[j][h][0] = c0.x; vv[j][h][1] = c0.y; vv[j][h][2] = c0.z; vv[j][h][3] = c0.w;
+                        if constexpr (kF32Grad<G>) {
+                            const float4 g0 = ld_stream_f4(static_cast<const float*>(t.g) + i0);
+                            gg[j][h][0] = g0.x; gg[j][h][1] = g0.y; gg[j][h][2] = g0.z; gg[j][h][3] = g0.w;
+                        } else {
+                            ld4_16<G>(static_cast<const GT*>(t.g) + i0, gg[j][h]);
+                        }
                     }
                 }
             }
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
-                if (!act[j]) continue;
-                const int64_t i0 = (base + (int64_t)j * kThreads) * kUnit;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) adamw_update(th[j][q], mm[j][q], vv[j][q], gg[j][q], s);
-                st_stream_f4(t.p + i0, make_float4(th[j][0], th[j][1], th[j][2], th[j][3]));
-                st_stream_f4(t.p + i0 + 4, make_float4(th[j][4], th[j][5], th[j][6], th[j][7]));
-                st_stream_f4(t.m + i0, make_float4(mm[j][0], mm[j][1], mm[j][2], mm[j][3]));
-                st_stream_f4(t.m + i0 + 4, make_float4(mm[j][4], mm[j][5], mm[j][6], mm[j][7]));
-                st_stream_f4(t.v + i0, make_float4(vv[j][0], vv[j][1], vv[j][2], vv[j][3]));
-                st_stream_f4(t.v + i0 + 4, make_float4(vv[j][4], vv[j][5], vv[j][6], vv[j][7]));
-                if constexpr (kHasCopy<C>) st_stream_u4(static_cast<CT*>(t.c) + i0, pack8<C>(th[j]));
-                if constexpr (kF32Grad<G>) {
-                    st_stream_f4(static_cast<float*>(t.g) + i0, make_float4(0.f, 0.f, 0.f, 0.f));
-                    st_stream_f4(static_cast<float*>(t.g) + i0 + 4, make_float4(0.f, 0.f, 0.f, 0.f));
-                } else {
-                    st_stream_u4(static_cast<GT*>(t.g) + i0, make_uint4(0u, 0u, 0u, 0u));
+                for (int h = 0; h < 2; ++h) {
+                    if (!act[j][h]) continue;
+                    const int64_t i0 = blk + j * 256 + h * 128 + 4 * lane;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        adamw_update(th[j][h][q], mm[j][h][q], vv[j][h][q], gg[j][h][q], s);
+                    st_stream_f4(t.p + i0, make_float4(th[j][h][0], th[j][h][1], th[j][h][2], th[j][h][3]));
+                    st_stream_f4(t.m + i0, make_float4(mm[j][h][0], mm[j][h][1], mm[j][h][2], mm[j][h][3]));
+                    st_stream_f4(t.v + i0, make_float4(vv[j][h][0], vv[j][h][1], vv[j][h][2], vv[j][h][3]));
+                    if constexpr (kHasCopy<C>) st4_16<C>(static_cast<CT*>(t.c) + i0, th[j][h]);
+                    if constexpr (kF32Grad<G>)
+                        st_stream_f4(static_cast<float*>(t.g) + i0, make_float4(0.f, 0.f, 0.f, 0.f));
+                    else
+                        __stcs(reinterpret_cast<uint2*>(static_cast<GT*>(t.g) + i0), make_uint2(0u, 0u));
                 }
             }
         }
