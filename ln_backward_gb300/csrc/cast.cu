@@ -11,12 +11,13 @@
 //   tb_cast_to_f32   : dst = float(src) * scale   (one fp32 rounding of the product)
 //   tb_cast_from_f32 : dst = round-to-nearest-even(src) in a 16-bit format
 //
-// Grid-stride over 8-element units with 16-byte vector accesses when both
-// pointers are 16-byte aligned; a scalar loop otherwise and for the ragged tail.
-// Widening to fp32 writes twice the bytes it reads: with a 32-byte aligned
-// destination each unit is one 16-byte load and one 32-byte store (sm_100's
-// 256-bit st.global), four units in flight per thread, which measured 20% faster
-// than two 16-byte stores per unit.
+// Vector paths grid-stride over 4-element chunks, one chunk per lane per access:
+// the fp32 side moves 16 bytes per lane and the 16-bit side 8, so every warp
+// access covers whole 32-byte sectors; four chunks are in flight per thread.
+// Widening a 16-bit source into a 32-byte aligned destination uses 8-element
+// units instead: one 16-byte load and one 32-byte store (sm_100's 256-bit
+// st.global) per lane, which measured 20% faster than two 16-byte stores per
+// unit.  A scalar loop covers misaligned buffers and the ragged tail.
 #include <algorithm>
 
 #include "tb_common.cuh"
@@ -26,17 +27,24 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Eight source elements as fp32 (16-bit formats: one 16-byte vector; fp32: two).
+// Eight 16-bit source elements (one 16-byte vector) as fp32.
 template <class S>
 __device__ __forceinline__ void load8(const void* p, int64_t i0, float (&f)[8]) {
     unpack8<S>(ld_stream_u4(static_cast<const typename S::T*>(p) + i0), f);
 }
+
+// Four source elements as fp32 (16-bit formats: one 8-byte access; fp32: 16 bytes).
+template <class S>
+__device__ __forceinline__ void load4(const void* p, int64_t i0, float (&f)[4]) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const typename S::T*>(p) + i0));
+    const typename S::T* h = reinterpret_cast<const typename S::T*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = S::to_f32(h[i]);
+}
 template <>
-__device__ __forceinline__ void load8<F32>(const void* p, int64_t i0, float (&f)[8]) {
-    const float* q = static_cast<const float*>(p) + i0;
-    const float4 a = ld_stream_f4(q), b = ld_stream_f4(q + 4);
+__device__ __forceinline__ void load4<F32>(const void* p, int64_t i0, float (&f)[4]) {
+    const float4 a = ld_stream_f4(static_cast<const float*>(p) + i0);
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
 __device__ __forceinline__ void st_stream_v8(float* p, const float (&f)[8]) {
@@ -52,36 +60,45 @@ cast_to_f32_kernel(const void* __restrict__ src, float* __restrict__ dst, int64_
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     int64_t done = 0;
-    if (vec == 2 && sizeof(typename S::T) == 2) {
-        // 32-byte aligned destination: one 16-byte load and one 32-byte store per
-        // unit, four units in flight per thread
-        const int64_t units = n / 8;
-        for (int64_t u = tid; u < units; u += 4 * stride) {
-            float f[4][8];
+    bool wide = false;
+    if constexpr (sizeof(typename S::T) == 2) {
+        if (vec == 2) {
+            // 32-byte aligned destination: one 16-byte load and one 32-byte store per
+            // unit, four units in flight per thread
+            wide = true;
+            const int64_t units = n / 8;
+            for (int64_t u = tid; u < units; u += 4 * stride) {
+                float f[4][8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (u + j * stride < units) load8<S>(src, (u + j * stride) * 8, f[j]);
+                for (int j = 0; j < 4; ++j)
+                    if (u + j * stride < units) load8<S>(src, (u + j * stride) * 8, f[j]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (u + j * stride < units) {
+                for (int j = 0; j < 4; ++j) {
+                    if (u + j * stride < units) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) f[j][q] *= scale;
-                    st_stream_v8(dst + (u + j * stride) * 8, f[j]);
+                        for (int q = 0; q < 8; ++q) f[j][q] *= scale;
+                        st_stream_v8(dst + (u + j * stride) * 8, f[j]);
+                    }
                 }
             }
+            done = units * 8;
         }
-        done = units * 8;
-    } else if (vec) {
-        const int64_t units = n / 8;
-        for (int64_t u = tid; u < units; u += stride) {
-            float f[8];
-            load8<S>(src, u * 8, f);
+    }
+    if (!wide && vec) {
+        const int64_t chunks = n / 4;
+        for (int64_t c = tid; c < chunks; c += 4 * stride) {
+            float f[4][4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) f[q] *= scale;
-            st_stream_f4(dst + u * 8, make_float4(f[0], f[1], f[2], f[3]));
-            st_stream_f4(dst + u * 8 + 4, make_float4(f[4], f[5], f[6], f[7]));
+            for (int j = 0; j < 4; ++j)
+                if (c + j * stride < chunks) load4<S>(src, (c + j * stride) * 4, f[j]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (c + j * stride < chunks)
+                    st_stream_f4(dst + (c + j * stride) * 4, make_float4(f[j][0] * scale, f[j][1] * scale,
+                                                                         f[j][2] * scale, f[j][3] * scale));
+            }
         }
-        done = units * 8;
+        done = chunks * 4;
     }
     const typename S::T* s = static_cast<const typename S::T*>(src);
     for (int64_t i = done + tid; i < n; i += stride) dst[i] = S::to_f32(s[i]) * scale;
@@ -95,13 +112,26 @@ cast_from_f32_kernel(const float* __restrict__ src, void* __restrict__ dst, int6
     typename D::T* d = static_cast<typename D::T*>(dst);
     int64_t done = 0;
     if (vec) {
-        const int64_t units = n / 8;
-        for (int64_t u = tid; u < units; u += stride) {
-            float f[8];
-            load8<F32>(src, u * 8, f);
-            st_stream_u4(d + u * 8, pack8<D>(f));
+        const int64_t chunks = n / 4;
+        for (int64_t c = tid; c < chunks; c += 4 * stride) {
+            float4 f[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (c + j * stride < chunks) f[j] = ld_stream_f4(src + (c + j * stride) * 4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (c + j * stride < chunks) {
+                    uint2 u;
+                    typename D::T* h = reinterpret_cast<typename D::T*>(&u);
+                    h[0] = D::from_f32(f[j].x);
+                    h[1] = D::from_f32(f[j].y);
+                    h[2] = D::from_f32(f[j].z);
+                    h[3] = D::from_f32(f[j].w);
+                    __stcs(reinterpret_cast<uint2*>(d + (c + j * stride) * 4), u);
+                }
+            }
         }
-        done = units * 8;
+        done = chunks * 4;
     }
     for (int64_t i = done + tid; i < n; i += stride) d[i] = D::from_f32(src[i]);
 }
@@ -130,7 +160,9 @@ extern "C" tb_status tb_cast_to_f32(const void* src, tb_dtype src_dtype, float s
     int dev = 0;
     DeviceInfo info{};
     if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
-    int vec = aligned_to(src, 16) && aligned_to(dst, 16) ? (aligned_to(dst, 32) ? 2 : 1) : 0;
+    // 2: 8-element units with 32-byte stores (16-bit source); 1: 4-element chunks
+    int vec = es == 2 && aligned_to(src, 16) && aligned_to(dst, 32) ? 2
+                  : aligned_to(src, 4 * es) && aligned_to(dst, 16) ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const void* k = src_dtype == TB_BF16 ? reinterpret_cast<const void*>(&cast_to_f32_kernel<BF16>)
                   : src_dtype == TB_F16  ? reinterpret_cast<const void*>(&cast_to_f32_kernel<F16>)
@@ -154,7 +186,7 @@ extern "C" tb_status tb_cast_from_f32(const float* src, void* dst, tb_dtype dst_
     int dev = 0;
     DeviceInfo info{};
     if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
-    int vec = aligned_to(src, 16) && aligned_to(dst, 16);
+    int vec = aligned_to(src, 16) && aligned_to(dst, 8);   // 4-element chunks
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const void* k = dst_dtype == TB_BF16 ? reinterpret_cast<const void*>(&cast_from_f32_kernel<BF16>)
                                          : reinterpret_cast<const void*>(&cast_from_f32_kernel<F16>);

@@ -42,9 +42,11 @@ def _src(n, dtype, offset=0, seed=0):
                          ids=["f16", "bf16", "f32"])
 @pytest.mark.parametrize("n", [1, 7, 8, 9, 1000, (1 << 20) + 3])
 # (source offset, destination offset) in elements: both aligned for the 32-byte store
-# path; a 16- but not 32-byte aligned destination for the 16-byte path (the bf16/fp16
-# source offset of 8 keeps it 16-byte aligned); both misaligned for the scalar path
-@pytest.mark.parametrize("offsets", [(0, 0), (8, 4), (1, 1)], ids=["v32", "v16", "scalar"])
+# path; a 16- but not 32-byte aligned destination for the 4-element chunk path (a source
+# offset of 8 keeps it 16-byte aligned, one of 4 leaves a 16-bit source only 8-byte
+# aligned, which that path still takes); both misaligned for the scalar path
+@pytest.mark.parametrize("offsets", [(0, 0), (8, 4), (4, 8), (1, 1)],
+                         ids=["v32", "v16", "chunk-src8", "scalar"])
 def test_cast_to_f32_bit_exact(tb, dtype, n, offsets):
     so, do = offsets
     src = _src(n, dtype, so, seed=n)
@@ -58,10 +60,14 @@ def test_cast_to_f32_bit_exact(tb, dtype, n, offsets):
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("n", [1, 7, 8, 9, 1000, (1 << 20) + 3])
-@pytest.mark.parametrize("offset", [0, 1])
-def test_cast_from_f32_bit_exact(tb, dtype, n, offset):
-    src = _src(n, torch.float32, offset, seed=n + 1)
-    dst = torch.empty(n + offset, dtype=dtype, device="cuda")[offset:]
+# (source offset, destination offset) in elements: the chunk path needs a 16-byte aligned
+# source and an 8-byte aligned destination; the others take the scalar loop
+@pytest.mark.parametrize("offsets", [(0, 0), (0, 4), (4, 0), (1, 1), (0, 1)],
+                         ids=["chunk", "chunk-dst8", "chunk-src16", "scalar", "scalar-dst"])
+def test_cast_from_f32_bit_exact(tb, dtype, n, offsets):
+    so, do = offsets
+    src = _src(n, torch.float32, so, seed=n + 1)
+    dst = torch.empty(n + do, dtype=dtype, device="cuda")[do:]
     tb.tb_cast_from_f32(src, dst)
     ref = oracle.cast_from_f32(src.cpu().numpy(), KIND[dtype])
     assert np.array_equal(to_bits(dst), ref)
