@@ -23,9 +23,10 @@
  *     as a tb_status.  A failed launch reports TB_ERR_CUDA.
  *   - The softmax, LayerNorm and RMSNorm kernels are launched as programmatic
  *     dependents of the work before them on `stream`: their blocks may start
- *     while the previous kernel drains and set up shared memory, but they read
- *     and write no global memory before every earlier kernel on the stream has
- *     completed and its writes are visible.  Stream order is kept exactly.
+ *     while the previous kernel drains, set up shared memory and (LayerNorm,
+ *     RMSNorm) prefetch their first rows into L2, but they load and store no
+ *     global memory before every earlier kernel on the stream has completed and
+ *     its writes are visible.  Stream order is kept exactly.
  *   - fp32 pointers must be 4-byte aligned and 16-bit pointers 2-byte aligned
  *     (TB_ERR_MISALIGNED otherwise).  Any larger alignment is optional: 16-byte
  *     aligned buffers take the vectorised path, others a scalar one.

@@ -12,7 +12,9 @@
 //    One elected thread streams the x and dY rows into a ring of shared-memory
 //    stages with 1-D bulk async copies (cp.async.bulk, completion counted on an
 //    mbarrier), several rows ahead, so HBM stays busy without holding the rows
-//    in registers.  Each thread owns a fixed set of 16-byte column vectors:
+//    in registers.  It is launched as a programmatic dependent: its CTAs set up
+//    their barriers and prefetch their first stage into L2 while the previous
+//    kernel drains, and copy nothing before that kernel has completed.  Each thread owns a fixed set of 16-byte column vectors:
 //    it keeps gamma and its dgamma/dbeta partial sums for those columns in
 //    registers across all rows of the CTA.  Phase 1 reads the staged row and
 //    forms the two row sums (dxhat, dxhat*xhat) with a warp butterfly plus one
@@ -112,6 +114,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
+}
+
+// Asynchronous prefetch of global memory into L2 (no data reaches the SM).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -286,9 +293,19 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&bars[s]), 1);
         mbar_init_fence();
         pol = evict_first_policy();
+        // Start pulling the first stage's rows from HBM into L2 while the previous
+        // kernel may still be draining.  A prefetch returns nothing to the kernel and
+        // L2 is coherent, so the copies issued after the wait still see every write of
+        // the previous kernel; the prefetch only shortens their trip.
+        if (ngroups > 0 && !withhold_copies) {
+            const uint32_t b0 = (uint32_t)(nrows < R ? nrows : R) * row_bytes;
+            bulk_prefetch_l2(x + r0 * D, b0);
+            bulk_prefetch_l2(dY + r0 * D, b0);
+        }
     }
-    // Up to here only shared memory was touched: the previous kernel may still be
-    // running (programmatic launch).  Every global access comes after this wait.
+    // Up to here the kernel has touched only shared memory (and issued the L2
+    // prefetch): the previous kernel may still be running (programmatic launch).
+    // Every load and store of global memory comes after this wait.
     pdl_wait();
     if (tid == 0)
         for (; issued < ngroups && issued < stages; ++issued) issue(issued, (int)issued);

@@ -77,7 +77,8 @@ inline tb_status launch_status() {
 // before them in the stream: their CTAs may be placed on the SMs while the
 // previous kernel drains, do their set-up (shared memory, barriers), and then
 // wait in pdl_wait() until every prerequisite grid has completed and its memory
-// is visible.  No global memory is read or written before that wait.  Launched
+// is visible.  No global memory is loaded or stored before that wait (an L2
+// prefetch, which returns nothing to the kernel, may be issued).  Launched
 // without the attribute (or after work that is not a kernel), the wait returns
 // at once.  pdl_trigger() lets the next programmatic dependent be scheduled
 // early; that kernel still waits for this one to complete before it touches

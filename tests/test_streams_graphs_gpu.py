@@ -2,6 +2,12 @@
 without interfering, and the softmax / LayerNorm / RMSNorm calls can be captured
 into a CUDA graph and replayed on new data with results bitwise equal to eager
 calls (every call is stream-ordered, allocates nothing and does not synchronise).
+
+The softmax, LayerNorm and RMSNorm kernels are launched as programmatic
+dependents of the work before them; the stream-order tests below check, with no
+synchronisation between the calls, that they still read what the previous kernel
+wrote and write nothing that the previous kernel was still reading -- against
+torch kernels and against their own earlier calls sharing one workspace.
 """
 import pytest
 import torch
@@ -205,3 +211,91 @@ def test_device_step_below_one_updates_nothing(tb, synth):
     assert tb.tb_device_error(reset=True) == 1        # TB_ERR_INVALID_VALUE
     assert tb.tb_device_error(reset=True) == 0
     plan.close()
+
+
+def test_programmatic_launch_keeps_stream_order_softmax(tb, synth):
+    rows, cols = 8192, 1024
+    P1, dY1 = synth.softmax_inputs(rows, cols, torch.bfloat16, seed=51, device="cuda")
+    P2, dY2 = synth.softmax_inputs(rows, cols, torch.bfloat16, seed=52, device="cuda")
+    ref1, ref2 = torch.empty_like(P1), torch.empty_like(P1)
+    tb.tb_softmax_bwd(dY1, P1, ref1)
+    tb.tb_softmax_bwd(dY2, P2, ref2)
+    torch.cuda.synchronize()
+    assert not torch.equal(ref1, ref2)
+    P, dY, dX = P1.clone(), dY1.clone(), torch.empty_like(P1)
+    snaps = []
+    for _ in range(4):
+        tb.tb_softmax_bwd(dY, P, dX)
+        snaps.append(dX.clone())          # a torch kernel reads dX ...
+        P.copy_(P2)                       # ... and torch kernels rewrite the inputs
+        dY.copy_(dY2)
+        tb.tb_softmax_bwd(dY, P, dX)      # must read the new inputs, and write dX only
+        snaps.append(dX.clone())          # after the clone above has read it
+        P.copy_(P1)
+        dY.copy_(dY1)
+    torch.cuda.synchronize()
+    for i, snap in enumerate(snaps):
+        assert torch.equal(snap, ref1 if i % 2 == 0 else ref2), i
+
+
+@pytest.mark.parametrize("op", ["layernorm", "rmsnorm"])
+def test_programmatic_launch_keeps_stream_order_norms(tb, synth, op):
+    """Back-to-back calls on different inputs share one workspace: a call's row kernel
+    must not overwrite the column partials before the previous call's column reduction
+    has read them, and must read inputs a torch kernel has just rewritten."""
+    rows, D = 4096, 4096
+    if op == "layernorm":
+        a = synth.layernorm_inputs(rows, D, torch.bfloat16, seed=53, device="cuda", dy_std=1e-2)
+        b = synth.layernorm_inputs(rows, D, torch.bfloat16, seed=54, device="cuda", dy_std=1e-2)
+        ws = torch.empty(tb.tb_layernorm_bwd_workspace_size(rows, D, torch.bfloat16),
+                         dtype=torch.uint8, device="cuda")
+
+        def call(inp, outs):
+            x, dY, mu, rs, g = inp
+            tb.tb_layernorm_bwd(dY, x, mu, rs, g, *outs, ws)
+
+        def outs_new():
+            return (torch.empty(rows, D, dtype=torch.bfloat16, device="cuda"),
+                    torch.empty(D, device="cuda"), torch.empty(D, device="cuda"))
+    else:
+        a = synth.rmsnorm_inputs(rows, D, torch.bfloat16, seed=55, device="cuda", dy_std=1e-2)
+        b = synth.rmsnorm_inputs(rows, D, torch.bfloat16, seed=56, device="cuda", dy_std=1e-2)
+        ws = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(rows, D, torch.bfloat16),
+                         dtype=torch.uint8, device="cuda")
+
+        def call(inp, outs):
+            x, dY, inv, g = inp
+            tb.tb_rmsnorm_bwd(dY, x, inv, g, *outs, ws)
+
+        def outs_new():
+            return (torch.empty(rows, D, dtype=torch.bfloat16, device="cuda"),
+                    torch.empty(D, device="cuda"))
+    ref_a, ref_b = outs_new(), outs_new()
+    call(a, ref_a)
+    torch.cuda.synchronize()
+    call(b, ref_b)
+    torch.cuda.synchronize()
+    assert not torch.equal(ref_a[1], ref_b[1])
+    # alternate the two problems with no synchronisation: each call's own outputs, and
+    # one input tensor set that torch kernels rewrite between the calls
+    own = [(outs_new(), outs_new()) for _ in range(3)]
+    shared = [(outs_new(), outs_new()) for _ in range(3)]
+    cur = tuple(t.clone() for t in a)
+    torch.cuda.synchronize()
+    for oa, ob in own:
+        call(a, oa)
+        call(b, ob)
+    for oa, ob in shared:
+        call(cur, oa)
+        for t, src in zip(cur, b):
+            t.copy_(src)
+        call(cur, ob)
+        for t, src in zip(cur, a):
+            t.copy_(src)
+    torch.cuda.synchronize()
+    for oa, ob in own + shared:
+        for u, w in zip(oa, ref_a):
+            assert torch.equal(u, w)
+        for u, w in zip(ob, ref_b):
+            assert torch.equal(u, w)
+    assert tb.tb_device_error(reset=True) == 0
