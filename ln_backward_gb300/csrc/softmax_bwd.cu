@@ -14,6 +14,8 @@
 //   group : rows of <= 256 vectors (1024 fp32 / 2048 16-bit), G lanes per row
 //   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
+// The group and CTA paths launch one CTA per row group when a CTA carries enough
+// traffic (the hardware scheduler then balances the SMs), else a persistent grid.
 //
 // Causal variant (tb_softmax_bwd_causal): row r of an attention block can only be
 // nonzero on its first min(cols, r mod period + 1 + offset) columns (the forward
@@ -269,6 +271,39 @@ softmax_bwd_twopass_kernel(const typename Fmt::T* __restrict__ dY,
 }
 
 // ------------------------------------------------------------------ dispatch
+// Grid shape.  A persistent grid (SM count x resident CTAs, grid-striding over the
+// rows) gives every warp a fixed share of the rows, and the SMs of a GB300 do not
+// stream at one rate: the CTAs of a persistent fp32 softmax at 98,304 x 1,024 end
+// over a window of 70 us of a 185 us launch.  One CTA per row group instead lets the
+// hardware scheduler hand the next group to whichever SM has room, so a faster SM
+// simply runs more of them (185 -> 170 us there; every row is independent, so the
+// results are the same bit for bit).  That pays only while a CTA carries enough
+// traffic to cover its own launch: below about 40 KB per CTA (bf16 causal rows of
+// 1,024 columns, half of them masked) the persistent grid measured faster.
+constexpr double kOneShotCtaBytes = 40.0 * 1024;
+
+// Mean number of open (readable) columns per row: all of them for a dense matrix;
+// under the causal mask the mean over one period of min(cols, q + 1 + offset).
+double mean_open_cols(int64_t cols, int64_t period, int64_t offset) {
+    if (period <= 0) return (double)cols;
+    // q + 1 + offset reaches cols at q = cols - 1 - offset
+    const int64_t ramp = std::max<int64_t>(0, std::min<int64_t>(period, cols - 1 - offset));
+    // q in [0, ramp): q + 1 + offset; q in [ramp, period): cols
+    const double sum_ramp = (double)ramp * (double)(1 + offset) + (double)ramp * (double)(ramp - 1) / 2.0;
+    return (sum_ramp + (double)(period - ramp) * (double)cols) / (double)period;
+}
+
+// CTAs for `want` row groups of `rows_per_cta` rows each: one per group when a CTA's
+// estimated traffic (reads of the open columns of P and dY, writes of all of dX)
+// reaches kOneShotCtaBytes, else a persistent grid.
+int64_t grid_for(int64_t want, int64_t rows_per_cta, int64_t cols, int64_t period, int64_t offset,
+                 size_t es, int sms, int per_sm) {
+    const double cta_bytes = (double)rows_per_cta * (double)es *
+                             (2.0 * mean_open_cols(cols, period, offset) + (double)cols);
+    if (cta_bytes >= kOneShotCtaBytes) return std::max<int64_t>(1, want);
+    return std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * per_sm));
+}
+
 template <class Fmt, int G, int VPL>
 tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, int nv,
                        int64_t period, int64_t offset, int sms, cudaStream_t st) {
@@ -277,7 +312,8 @@ tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, in
         reinterpret_cast<const void*>(&softmax_bwd_group_kernel<Fmt, G, VPL>), 256, 0);
     if (per_sm == 0) return TB_ERR_CUDA;
     const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * per_sm));
+    const int64_t grid = grid_for(want, kRowsPerCta, (int64_t)nv * Vec<Fmt>::kElems, period, offset,
+                                  sizeof(typename Fmt::T), sms, per_sm);
     if (launch_pdl(softmax_bwd_group_kernel<Fmt, G, VPL>, dim3((unsigned)grid), dim3(256), 0, st,
                    static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
                    static_cast<uint4*>(dX), rows, nv, period, offset) != cudaSuccess)
@@ -291,7 +327,8 @@ tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int 
     const int per_sm = resident_ctas_per_sm(
         reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, VPL>), kCtaThreads, 0);
     if (per_sm == 0) return TB_ERR_CUDA;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)sms * per_sm));
+    const int64_t grid = grid_for(rows, 1, (int64_t)nv * Vec<Fmt>::kElems, period, offset,
+                                  sizeof(typename Fmt::T), sms, per_sm);
     if (launch_pdl(softmax_bwd_cta_kernel<Fmt, VPL>, dim3((unsigned)grid), dim3(kCtaThreads), 0, st,
                    static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
                    static_cast<uint4*>(dX), rows, nv, period, offset) != cudaSuccess)

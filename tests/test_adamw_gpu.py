@@ -285,8 +285,8 @@ def test_plan_of_empty_tensors_is_a_no_op(tb):
 
 
 def test_tile_counter_is_reset_on_every_path(tb, synth):
-    """The step kernel's CTAs claim tiles from a counter in the plan that the last CTA
-    out resets.  After every kind of call (a device step that returns early for t < 1,
+    """The step kernel's CTAs claim tiles from a counter in the plan that each call
+    clears before its launch.  After every kind of call (a device step that returns early for t < 1,
     a step skipped for a non-finite gradient, plain, clipped and device steps) the next
     step must still visit every element: each step leaves every gradient element +0.
     Two tables: one with many more tiles than CTAs, one with a single tile."""

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from tolerance import floored_rel, lowp_check, to_bits, within_bound
+from tolerance import floored_rel, layernorm_dx_err_bound, lowp_check, to_bits, within_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -46,19 +46,7 @@ def run(tb, x, dY, mean, rstd, gamma, ws_bytes=None):
 
 
 def _dx_err_bound(x, dY, mean, rstd, gamma):
-    """Bound on |dX_fp32 - dX_exact|: xhat and dxhat carry a few fp32 roundings,
-    the two row sums at most D/32 + 64 rounded additions each."""
-    D = x.shape[1]
-    xh = (x - mean[:, None]) * rstd[:, None]
-    dxh = dY * gamma[None, :]
-    sa = np.sum(np.abs(dxh), axis=1, keepdims=True) / D
-    sb = np.sum(np.abs(dxh * xh), axis=1, keepdims=True) / D
-    mb = np.abs(np.sum(dxh * xh, axis=1, keepdims=True)) / D
-    ma = np.abs(np.sum(dxh, axis=1, keepdims=True)) / D
-    k = D / 32 + 64
-    u = 2.0 ** -24
-    return rstd[:, None] * (4 * u * (np.abs(dxh) + ma + np.abs(xh) * mb) +
-                            k * u * (sa + np.abs(xh) * sb))
+    return layernorm_dx_err_bound(x, dY, mean, rstd, gamma)
 
 
 def check(tb, x, dY, mean, rstd, gamma, dX, dg, db, strict_fp32=True):

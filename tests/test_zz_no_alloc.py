@@ -7,13 +7,15 @@ the device.  They have no workspace to pass, so this entry point keeps its
 scratch in a fixed array inside the library.  These checks call it through the
 C ABI and compare it with the workspace entry point, twice in a row (the second
 call finds the previous call's partial sums still in the shared array), within
-the tolerances the other LayerNorm tests use.  This file is collected last.
+the tolerances the other LayerNorm tests use, and then the second call's output
+with the CPU oracle under the same rules.  This file is collected last.
 """
 import numpy as np
 import pytest
 import torch
 
-from tolerance import floored_rel, lowp_check, to_bits
+import oracle
+from tolerance import floored_rel, layernorm_dx_err_bound, lowp_check, to_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -78,6 +80,19 @@ def test_matches_workspace_entry_point_twice(tb, synth, rows, D, dtype):
     if (rows, D) == (16384, 4096):
         for u, w in zip(got, ref):
             assert torch.equal(u, w)
+    # and against the oracle directly (float64 LayerNorm backward on the same inputs)
+    x, dY, mean, rstd, gamma = (t.double().cpu().numpy() for t in args)
+    rdx, rdg, rdb = oracle.layernorm_bwd_f64(dY, x, mean, rstd, gamma)
+    dX, dg, db = got
+    assert floored_rel(dg.double().cpu().numpy(), rdg) <= 1e-3
+    assert floored_rel(db.double().cpu().numpy(), rdb) <= 1e-3
+    if dX.dtype == torch.float32:
+        assert floored_rel(dX.double().cpu().numpy(), rdx) <= 1e-4
+    else:
+        kind = "bf16" if dX.dtype == torch.bfloat16 else "f16"
+        ok, _, _ = lowp_check(to_bits(dX), rdx, kind,
+                              layernorm_dx_err_bound(x, dY, mean, rstd, gamma))
+        assert ok.all()
     assert tb.tb_device_error(reset=True) == 0
 
 

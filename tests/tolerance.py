@@ -79,3 +79,20 @@ def within_bound(got, ref, err) -> np.ndarray:
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     return np.abs(got - ref) <= np.broadcast_to(np.asarray(err, np.float64), ref.shape)
+
+
+def layernorm_dx_err_bound(x, dY, mean, rstd, gamma):
+    """Bound on |dX_fp32 - dX_exact| of the LayerNorm backward (numpy float64 inputs):
+    xhat and dxhat carry a few fp32 roundings, the two row sums at most D/32 + 64
+    rounded additions each."""
+    D = x.shape[1]
+    xh = (x - mean[:, None]) * rstd[:, None]
+    dxh = dY * gamma[None, :]
+    sa = np.sum(np.abs(dxh), axis=1, keepdims=True) / D
+    sb = np.sum(np.abs(dxh * xh), axis=1, keepdims=True) / D
+    mb = np.abs(np.sum(dxh * xh, axis=1, keepdims=True)) / D
+    ma = np.abs(np.sum(dxh, axis=1, keepdims=True)) / D
+    k = D / 32 + 64
+    u = 2.0 ** -24
+    return rstd[:, None] * (4 * u * (np.abs(dxh) + ma + np.abs(xh) * mb) +
+                            k * u * (sa + np.abs(xh) * sb))
