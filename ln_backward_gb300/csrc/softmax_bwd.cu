@@ -300,7 +300,8 @@ int64_t grid_for(int64_t want, int64_t rows_per_cta, int64_t cols, int64_t perio
                  size_t es, int sms, int per_sm) {
     const double cta_bytes = (double)rows_per_cta * (double)es *
                              (2.0 * mean_open_cols(cols, period, offset) + (double)cols);
-    if (cta_bytes >= kOneShotCtaBytes) return std::max<int64_t>(1, want);
+    // (the kernels grid-stride, so a grid capped at the launch limit still covers every row)
+    if (cta_bytes >= kOneShotCtaBytes) return std::max<int64_t>(1, std::min<int64_t>(want, INT32_MAX));
     return std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sms * per_sm));
 }
 
