@@ -14,9 +14,10 @@
 //    mbarrier), several rows ahead, so HBM stays busy without holding the rows
 //    in registers.  It is launched as a programmatic dependent: its CTAs set up
 //    their barriers and prefetch their first stage into L2 while the previous
-//    kernel drains, and copy nothing before that kernel has completed.  Each thread owns a fixed set of 16-byte column vectors:
-//    it keeps gamma and its dgamma/dbeta partial sums for those columns in
-//    registers across all rows of the CTA.  Phase 1 reads the staged row and
+//    kernel drains, and copy nothing before that kernel has completed.  Each
+//    thread owns a fixed set of 16-byte column vectors: it keeps gamma and its
+//    dgamma/dbeta partial sums for those columns in registers across all rows
+//    of the CTA.  Phase 1 reads the staged row and
 //    forms the two row sums (dxhat, dxhat*xhat) with a warp butterfly plus one
 //    shared-memory exchange and one barrier per row; phase 2 re-reads the
 //    staged row (shared memory, not HBM), writes dX and accumulates the column
