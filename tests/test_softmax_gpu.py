@@ -79,6 +79,30 @@ def test_row_length_sweep(tb, synth, cols, dtype):
     check(dX, P, dY)
 
 
+# Shapes with more row groups than a persistent grid has CTAs (152 SMs x 3), in both grid
+# regimes: one CTA per row group when a CTA carries at least 40 KB of traffic, else the
+# persistent grid striding over the groups.
+@pytest.mark.parametrize("rows, cols, dtype, period", [
+    (4000, 1024, torch.float32, 0),        # warp per row, 96 KB per CTA: one CTA per group
+    (4000, 128, torch.float32, 0),         # warp per row, 12 KB per CTA: persistent
+    (4000, 1024, torch.bfloat16, 1024),    # causal, about 33 KB per CTA: persistent
+    (4000, 1024, torch.float32, 1024),     # causal, about 66 KB per CTA: one CTA per group
+    (2000, 4096, torch.float32, 0),        # CTA per row, 48 KB: one CTA per row
+    (2000, 2048, torch.float32, 0),        # CTA per row, 24 KB: persistent
+    (2000, 4096, torch.bfloat16, 4096),    # CTA per row, causal, about 16 KB: persistent
+], ids=["group-oneshot", "group-persistent", "causal-bf16-persistent", "causal-f32-oneshot",
+        "cta-oneshot", "cta-persistent", "cta-causal-persistent"])
+def test_both_grid_regimes(tb, synth, rows, cols, dtype, period):
+    P, dY = synth.softmax_inputs(rows, cols, dtype, seed=rows + cols, device="cuda",
+                                 causal_period=period or None)
+    dX = torch.full_like(P, float("nan"))
+    if period:
+        tb.tb_softmax_bwd_causal(dY, P, dX, period=period)
+    else:
+        tb.tb_softmax_bwd(dY, P, dX)
+    check(dX, P, dY)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_unaligned_buffers_take_two_pass_path(tb, synth, dtype):
     rows, cols = 19, 1024
