@@ -48,6 +48,12 @@ constexpr int64_t kTileUnits = (int64_t)kThreads * kUnroll * 4;   // 16384 eleme
 // The gradient-norm pass reads 2 bytes per element instead of 30: it takes 4x
 // longer tiles (65,536 elements) so a CTA spends less of its time between tiles.
 constexpr int64_t kNormTileUnits = 4 * kTileUnits;
+// Each CTA of the gradient-norm pass owns a fixed chunk of this many consecutive
+// tiles (262,144 elements) and writes the chunk's partial sum at the chunk's index:
+// the grid has one CTA per chunk, the block scheduler hands chunks to whichever SM
+// has room (a fixed share per CTA of a persistent grid ends with the slowest SMs),
+// and the partials still do not depend on timing.
+constexpr int64_t kNormChunkTiles = 4;
 constexpr uint64_t kPlanMagic = 0x7462616461707731ull;
 
 struct alignas(16) TensorEntry {
@@ -319,8 +325,8 @@ adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t
 // Sum of squares of the unscaled gradient over every tensor (reading only the
 // gradient), plus a non-finite flag.  Each thread adds its squares in fp32 in
 // rounds of at most 32, the round sums of a tile in fp32 and the tile sums in
-// fp64; each CTA writes one fp64 partial and one flag; the finalize kernel adds
-// the partials in order.
+// fp64; CTA b covers the tiles of chunk b and writes one fp64 partial and one flag
+// at index b; the finalize kernel adds the partials in index order.
 template <class G>
 __global__ void __launch_bounds__(kThreads)
 adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
@@ -330,7 +336,9 @@ adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t t
     double acc = 0.0;
     int bad = 0;
     int k = 0;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int64_t t0 = (int64_t)blockIdx.x * kNormChunkTiles;
+    const int64_t t1 = t0 + kNormChunkTiles < n_tiles ? t0 + kNormChunkTiles : n_tiles;
+    for (int64_t tile = t0; tile < t1; ++tile) {
         const int64_t u_lo = tile * kNormTileUnits;
         const int64_t u_hi = u_lo + kNormTileUnits < total_units ? u_lo + kNormTileUnits : total_units;
         k = tensor_of(tab, ntab, k, u_lo);
@@ -438,6 +446,7 @@ adamw_grad_norm_finalize_kernel(const double* __restrict__ part, const int* __re
     __shared__ double sh[kThreads];
     double acc = 0.0;
     int bad = 0;
+#pragma unroll 8
     for (int i = threadIdx.x; i < nparts; i += kThreads) {
         acc += part[i];
         bad |= flags[i];
@@ -493,7 +502,7 @@ struct tb_adamw_plan {
     tb::TensorEntry* d_table;
     int64_t total_units;
     int grid;        // CTAs of the step kernel
-    int norm_grid;   // CTAs of the gradient-norm kernel
+    int norm_parts;  // CTAs of the gradient-norm kernel = chunks of kNormChunkTiles tiles
     bool has_copy;   // the tensors have working copies (all of them, or none)
 };
 
@@ -593,10 +602,9 @@ static tb_status plan_create_impl(const tb_tensor_desc* tensors, int n_tensors,
                                                       kThreads, 0) != cudaSuccess)
         return TB_ERR_CUDA;
     per_sm = std::max(per_sm, 1);
-    int norm_per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&norm_per_sm, norm_kernel(grad_dtype), kThreads,
-                                                      0) != cudaSuccess)
-        return TB_ERR_CUDA;
+    const int64_t norm_tiles = (units + kNormTileUnits - 1) / kNormTileUnits;
+    const int64_t norm_parts = std::max<int64_t>(1, (norm_tiles + kNormChunkTiles - 1) / kNormChunkTiles);
+    if (norm_parts > INT32_MAX) return TB_ERR_INVALID_VALUE;   // beyond any device's memory
 
     tb_adamw_plan* plan = new (std::nothrow) tb_adamw_plan;
     if (!plan) return TB_ERR_OOM;
@@ -607,7 +615,7 @@ static tb_status plan_create_impl(const tb_tensor_desc* tensors, int n_tensors,
     plan->copy_dtype = copy_dtype;
     plan->total_units = units;
     plan->grid = info.sm_count * per_sm;
-    plan->norm_grid = info.sm_count * std::max(norm_per_sm, 1);
+    plan->norm_parts = (int)norm_parts;
     plan->has_copy = has_copy;
     plan->d_table = nullptr;
     // The table, then the step kernel's tile counter (zero), copied up together.
@@ -705,9 +713,9 @@ tb_status adamw_step_impl(const tb_adamw_plan* plan, int64_t step, const tb_adam
     return TB_OK;
 }
 
-// Partials of the gradient-norm kernel: one fp64 sum and one int flag per CTA.
+// Partials of the gradient-norm kernel: one fp64 sum and one int flag per chunk.
 size_t grad_norm_workspace(const tb_adamw_plan* plan) {
-    return (size_t)plan->norm_grid * (sizeof(double) + sizeof(int));
+    return (size_t)plan->norm_parts * (sizeof(double) + sizeof(int));
 }
 }  // namespace
 }  // namespace tb
@@ -754,9 +762,9 @@ extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_los
     if (dev != plan->device) return TB_ERR_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     double* part = static_cast<double*>(workspace);
-    int* flags = reinterpret_cast<int*>(part + plan->norm_grid);
+    int* flags = reinterpret_cast<int*>(part + plan->norm_parts);
     const int64_t n_tiles = (plan->total_units + kNormTileUnits - 1) / kNormTileUnits;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(plan->norm_grid, n_tiles));
+    const int grid = plan->norm_parts;   // one CTA per chunk of kNormChunkTiles tiles
     if (plan->total_units > 0) {
         const TensorEntry* tab = plan->d_table;
         int nt = plan->n_tensors;
