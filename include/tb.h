@@ -194,11 +194,12 @@ tb_status tb_adamw_step(const tb_adamw_plan* plan, int64_t step,
  *     out[1] = factor = max_norm / norm if max_norm > 0 and norm > max_norm, else 1
  *     out[2] = 1 if any gradient element is NaN or infinite, else 0
  * Each thread adds its squares in fp32 in rounds of at most 32, adds the round
- * sums of one tile (at most 256 squares) in fp32 and the tile sums in fp64; the
- * parameter space is cut into fixed chunks of 262,144 elements, one partial per
- * chunk, and the partials are added in chunk order, so the result is reproducible.
+ * sums of one tile (at most 256 squares) in fp32 and the tile sums in fp64; each
+ * CTA adds a fixed set of tiles (consecutive chunks of 262,144 elements on large
+ * tables, tiles dealt round-robin on small ones) into one partial, and the
+ * partials are added in a fixed order, so the result is reproducible.
  *   workspace  device scratch of tb_adamw_grad_norm_workspace_size() bytes,
- *              8-byte aligned (one fp64 partial and one flag per chunk)
+ *              8-byte aligned (one fp64 partial and one flag per CTA)
  * Errors: TB_ERR_INVALID_VALUE, TB_ERR_MISALIGNED, TB_ERR_WORKSPACE, TB_ERR_ALIAS,
  * TB_ERR_DEVICE, TB_ERR_CUDA.
  *

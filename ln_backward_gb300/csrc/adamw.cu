@@ -48,12 +48,20 @@ constexpr int64_t kTileUnits = (int64_t)kThreads * kUnroll * 4;   // 16384 eleme
 // The gradient-norm pass reads 2 bytes per element instead of 30: it takes 4x
 // longer tiles (65,536 elements) so a CTA spends less of its time between tiles.
 constexpr int64_t kNormTileUnits = 4 * kTileUnits;
-// Each CTA of the gradient-norm pass owns a fixed chunk of this many consecutive
-// tiles (262,144 elements) and writes the chunk's partial sum at the chunk's index:
-// the grid has one CTA per chunk, the block scheduler hands chunks to whichever SM
-// has room (a fixed share per CTA of a persistent grid ends with the slowest SMs),
-// and the partials still do not depend on timing.
+// Grid of the gradient-norm pass.  On a large table each CTA owns a fixed chunk of
+// kNormChunkTiles consecutive tiles (262,144 elements) and writes the chunk's
+// partial at the chunk's index: one CTA per chunk, so the block scheduler hands
+// chunks to whichever SM has room (a fixed share per CTA of a persistent grid ends
+// with the slowest SMs; 7B table: 1.80 against 1.88 ms), and the partials still do
+// not depend on timing.  Below four chunks per resident CTA slot the CTAs would be
+// too short-lived to pay for their own start, and a persistent grid dealing tiles
+// round-robin is kept (GPT-2-small table: 49.7 against 53.2 us).  Returns the
+// chunk length in tiles, 0 for the round-robin grid.
 constexpr int64_t kNormChunkTiles = 4;
+
+int64_t norm_chunk_tiles(int64_t n_tiles, int64_t slots) {
+    return n_tiles >= 4 * kNormChunkTiles * std::max<int64_t>(slots, 1) ? kNormChunkTiles : 0;
+}
 constexpr uint64_t kPlanMagic = 0x7462616461707731ull;
 
 struct alignas(16) TensorEntry {
@@ -325,20 +333,23 @@ adamw_multi_tensor_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t
 // Sum of squares of the unscaled gradient over every tensor (reading only the
 // gradient), plus a non-finite flag.  Each thread adds its squares in fp32 in
 // rounds of at most 32, the round sums of a tile in fp32 and the tile sums in
-// fp64; CTA b covers the tiles of chunk b and writes one fp64 partial and one flag
-// at index b; the finalize kernel adds the partials in index order.
+// fp64; CTA b covers the tiles of chunk b (or tiles b, b + grid, ...) and writes
+// one fp64 partial and one flag at index b; the finalize kernel adds the partials
+// in index order.
 template <class G>
 __global__ void __launch_bounds__(kThreads)
 adamw_grad_sumsq_kernel(const TensorEntry* __restrict__ tab, int ntab, int64_t total_units,
-                        int64_t n_tiles, float inv_s, double* __restrict__ part,
+                        int64_t n_tiles, int64_t chunk, float inv_s, double* __restrict__ part,
                         int* __restrict__ flags) {
     using GT = typename G::T;
     double acc = 0.0;
     int bad = 0;
     int k = 0;
-    const int64_t t0 = (int64_t)blockIdx.x * kNormChunkTiles;
-    const int64_t t1 = t0 + kNormChunkTiles < n_tiles ? t0 + kNormChunkTiles : n_tiles;
-    for (int64_t tile = t0; tile < t1; ++tile) {
+    // chunk > 0: tiles [b*chunk, (b+1)*chunk); chunk == 0: tiles b, b + grid, ...
+    const int64_t t0 = chunk ? (int64_t)blockIdx.x * chunk : (int64_t)blockIdx.x;
+    const int64_t t1 = chunk ? (t0 + chunk < n_tiles ? t0 + chunk : n_tiles) : n_tiles;
+    const int64_t tstep = chunk ? 1 : (int64_t)gridDim.x;
+    for (int64_t tile = t0; tile < t1; tile += tstep) {
         const int64_t u_lo = tile * kNormTileUnits;
         const int64_t u_hi = u_lo + kNormTileUnits < total_units ? u_lo + kNormTileUnits : total_units;
         k = tensor_of(tab, ntab, k, u_lo);
@@ -502,7 +513,8 @@ struct tb_adamw_plan {
     tb::TensorEntry* d_table;
     int64_t total_units;
     int grid;        // CTAs of the step kernel
-    int norm_parts;  // CTAs of the gradient-norm kernel = chunks of kNormChunkTiles tiles
+    int64_t norm_chunk;   // tiles per chunk of the gradient-norm kernel (0: round-robin)
+    int norm_parts;       // CTAs of the gradient-norm kernel = chunks
     bool has_copy;   // the tensors have working copies (all of them, or none)
 };
 
@@ -602,8 +614,16 @@ static tb_status plan_create_impl(const tb_tensor_desc* tensors, int n_tensors,
                                                       kThreads, 0) != cudaSuccess)
         return TB_ERR_CUDA;
     per_sm = std::max(per_sm, 1);
+    int norm_per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&norm_per_sm, norm_kernel(grad_dtype), kThreads,
+                                                      0) != cudaSuccess)
+        return TB_ERR_CUDA;
     const int64_t norm_tiles = (units + kNormTileUnits - 1) / kNormTileUnits;
-    const int64_t norm_parts = std::max<int64_t>(1, (norm_tiles + kNormChunkTiles - 1) / kNormChunkTiles);
+    const int64_t slots = (int64_t)info.sm_count * std::max(norm_per_sm, 1);
+    const int64_t norm_chunk = norm_chunk_tiles(norm_tiles, slots);
+    const int64_t norm_parts =
+        std::max<int64_t>(1, norm_chunk ? (norm_tiles + norm_chunk - 1) / norm_chunk
+                                        : std::min<int64_t>(slots, norm_tiles));
     if (norm_parts > INT32_MAX) return TB_ERR_INVALID_VALUE;   // beyond any device's memory
 
     tb_adamw_plan* plan = new (std::nothrow) tb_adamw_plan;
@@ -615,6 +635,7 @@ static tb_status plan_create_impl(const tb_tensor_desc* tensors, int n_tensors,
     plan->copy_dtype = copy_dtype;
     plan->total_units = units;
     plan->grid = info.sm_count * per_sm;
+    plan->norm_chunk = norm_chunk;
     plan->norm_parts = (int)norm_parts;
     plan->has_copy = has_copy;
     plan->d_table = nullptr;
@@ -764,14 +785,15 @@ extern "C" tb_status tb_adamw_grad_norm(const tb_adamw_plan* plan, float inv_los
     double* part = static_cast<double*>(workspace);
     int* flags = reinterpret_cast<int*>(part + plan->norm_parts);
     const int64_t n_tiles = (plan->total_units + kNormTileUnits - 1) / kNormTileUnits;
-    const int grid = plan->norm_parts;   // one CTA per chunk of kNormChunkTiles tiles
+    const int grid = plan->norm_parts;   // one CTA per chunk, or the round-robin grid
     if (plan->total_units > 0) {
         const TensorEntry* tab = plan->d_table;
         int nt = plan->n_tensors;
         int64_t tu = plan->total_units;
         int64_t nti = n_tiles;
+        int64_t chunk = plan->norm_chunk;
         float inv = inv_loss_scale;
-        void* args[] = {&tab, &nt, &tu, &nti, &inv, &part, &flags};
+        void* args[] = {&tab, &nt, &tu, &nti, &chunk, &inv, &part, &flags};
         if (cudaLaunchKernel(norm_kernel(plan->grad_dtype), dim3(grid), dim3(kThreads), args, 0, st) !=
             cudaSuccess)
             return TB_ERR_CUDA;
