@@ -150,7 +150,9 @@ def test_norm_llama7b_table_against_float64_reduction(tb, synth):
     same gradients (computed with torch on the device, chunk by chunk)."""
     st = synth.make_adamw_state(synth.llama7b_shapes(), seed=5, device="cuda", grad_std=1e-4)
     plan = _plan(tb, st)
-    out = _norm(tb, plan, 1 / 65536.0, 1.0).double().cpu().numpy()
+    out_t = _norm(tb, plan, 1 / 65536.0, 1.0)
+    out = out_t.double().cpu().numpy()
+    assert torch.equal(_norm(tb, plan, 1 / 65536.0, 1.0), out_t)   # reproducible bit for bit
     total = 0.0
     for i in range(len(st.sizes)):
         g = st.tensor("grad", i)
@@ -158,10 +160,21 @@ def test_norm_llama7b_table_against_float64_reduction(tb, synth):
             c = g[s0:s0 + (1 << 28)].double() / 65536.0
             total += float(torch.dot(c, c))
     ref = np.sqrt(total)
-    del st
+    # a non-finite element in one chunk of this table raises the flag (this table is large
+    # enough for the one-CTA-per-chunk grid); an Inf in another chunk as well
+    last = st.tensor("grad", len(st.sizes) - 1)
+    emb = st.tensor("grad", 0)
+    last[-3] = float("nan")
+    flagged_nan = _norm(tb, plan, 1 / 65536.0, 1.0).cpu().numpy()[2]
+    last[-3] = 0.0
+    emb[123457] = float("inf")
+    flagged_inf = _norm(tb, plan, 1 / 65536.0, 1.0).cpu().numpy()[2]
+    plan.close()
+    del st, last, emb
     torch.cuda.empty_cache()
     assert abs(out[0] - ref) <= 1e-5 * ref
     assert abs(out[1] - min(1.0, 1.0 / ref)) <= 1e-5 and out[2] == 0.0
+    assert flagged_nan == 1.0 and flagged_inf == 1.0
 
 
 def test_norm_special_cases(tb, synth):
