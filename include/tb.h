@@ -84,13 +84,15 @@ tb_status tb_device_error(int* code, int reset);
 
 /*
  * tb_layernorm_bwd_selftest_timeout -- exercises that failure path without a
- * GPU fault.  It runs the LayerNorm backward's bulk-copy ring kernel on a small
- * internal problem (4 x 256 bf16, zeroed buffers the call allocates and frees)
- * with its copies withheld, so that every wait on them runs out after
- * wait_limit_ns nanoseconds; the kernel then sets the device error word to
+ * GPU fault.  It runs the LayerNorm backward's two bulk-copy ring kernels on
+ * small internal problems (4 x 256 bf16 on one CTA per row block, then 4 x
+ * 8,192 bf16 split over a two-CTA cluster; zeroed buffers the call allocates and
+ * frees) with their copies withheld, so that every wait on them runs out after
+ * wait_limit_ns nanoseconds; each kernel then sets the device error word to
  * TB_ERR_TIMEOUT, waits (bounded as well) for the copies it would have issued,
- * and returns.  Nothing is in flight when it returns, so the context stays
- * usable.  The call synchronises `stream`; afterwards tb_device_error reports
+ * and returns -- the CTAs of a cluster together, after telling each other of the
+ * failure.  Nothing is in flight when it returns, so the context stays usable.
+ * The call synchronises `stream`; afterwards tb_device_error reports
  * TB_ERR_TIMEOUT.
  *   wait_limit_ns  1,000 .. 1,000,000,000
  * Returns TB_OK once the kernel has finished, TB_ERR_INVALID_VALUE (limit out of
@@ -329,7 +331,11 @@ tb_status tb_softmax_bwd_causal(const void* dY, const void* P, void* dX, int64_t
  * dgamma and dbeta are OVERWRITTEN (not accumulated).  They are reduced in two
  * stages -- per-CTA partial sums into the workspace, then a second kernel that
  * adds them in a fixed order -- so results are bitwise reproducible run to run
- * on the same device model.
+ * on the same device model.  Rows of more than 4,096 columns (16-byte aligned
+ * buffers, D a multiple of 2..8 times the 16-byte vector) are split by columns
+ * over the CTAs of a thread-block cluster, which exchange their shares of the
+ * row sums through distributed shared memory and write one partial row per
+ * cluster; all CTAs of a cluster use bitwise the same row sums.
  */
 
 /*

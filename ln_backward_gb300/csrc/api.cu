@@ -129,6 +129,41 @@ int resident_ctas_per_sm(const void* kernel, int threads, size_t dyn_smem) {
     }
 }
 
+int resident_clusters(const void* kernel, int threads, size_t dyn_smem, int cluster) {
+    if (cluster < 1 || resident_ctas_per_sm(kernel, threads, dyn_smem) == 0) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const unsigned long long ctx = current_context_id();
+    static std::mutex mu;
+    static std::map<std::tuple<int, unsigned long long, const void*, int, size_t, int>, int> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    try {
+        const auto key = std::make_tuple(dev, ctx, kernel, threads, dyn_smem, cluster);
+        const auto it = cache.find(key);
+        if (it != cache.end() && ctx != 0) return it->second;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)cluster);
+        cfg.blockDim = dim3((unsigned)threads);
+        cfg.dynamicSmemBytes = dyn_smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        if (ctx != 0) cache.emplace(key, n);
+        return n;
+    } catch (...) {
+        return 0;
+    }
+}
+
 }  // namespace tb
 
 extern "C" const char* tb_status_string(tb_status s) {

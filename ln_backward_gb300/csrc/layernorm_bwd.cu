@@ -23,11 +23,17 @@
 //    staged row (shared memory, not HBM), writes dX and accumulates the column
 //    partials.  A stage is refilled one row later, once every thread is past
 //    it.  At the end each CTA stores its column partials to the workspace.
-//  * Kernel 2 (columns): adds the per-CTA partials in a fixed order -> dgamma,
-//    dbeta, bitwise reproducible run to run.
+//  * Kernel 1' (rows wider than 4096 columns): the same ring, with each row
+//    split by columns over the 2..8 CTAs of a thread-block cluster.  Every CTA
+//    keeps the gamma and partials of its column slice in registers (so two CTAs
+//    still fit per SM) and the CTAs exchange their shares of the two row sums
+//    through distributed shared memory (st.async into the peers' exchange
+//    slots, counted on an mbarrier there) -- one exchange per row group.
+//  * Kernel 2 (columns): adds the per-CTA (per-cluster) partials in a fixed
+//    order -> dgamma, dbeta, bitwise reproducible run to run.
 //  * Rows whose byte length is not a multiple of 16, unaligned buffers, or D
-//    beyond the register budget use a plain-load fallback of the same
-//    structure (two passes over the row, partials kept in the workspace).
+//    that neither ring covers use a plain-load fallback of the same structure
+//    (two passes over the row, partials kept in the workspace).
 //
 // RMSNorm backward (tb_rmsnorm_bwd) runs the same kernels with kRms set:
 //   xhat = x * inv_rms, dX = inv_rms * (dxhat - xhat * mean_D(dxhat * xhat)),
@@ -52,6 +58,9 @@ constexpr int kRingBudget = 96 * 1024;         // bytes of ring per CTA we aim f
 constexpr int kStageTargetBytes = 32 * 1024;   // x + dY bytes per ring stage we aim for
 constexpr int kBarRegion = 128;                // bytes reserved for the mbarriers
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr int kMaxCluster = 8;                 // CTAs a row may be split over (portable size)
+constexpr int64_t kSplitFromD = 4096;          // wider rows are split over a cluster
+constexpr int64_t kSplitSliceTarget = 4096;    // columns per CTA we aim for when splitting
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -124,6 +133,70 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Thread-block cluster: this CTA's rank, the cluster's CTA count, the cluster's index.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Store 4 bytes into another CTA's shared memory (remote_addr), counted as 4
+// transaction bytes on that CTA's mbarrier (remote_bar).
+__device__ __forceinline__ void st_async_remote(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(
+                     remote_addr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
+
+// Every thread of every CTA of the cluster arrives and waits (the non-.aligned
+// form: the threads of a warp need not arrive converged).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// As mbar_try_wait, acquiring what other CTAs of the cluster released into the phase.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
+                                                          unsigned long long limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1; it < (1u << 30); ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+    return false;
 }
 
 // Read one 16-byte vector from shared memory as fp32 values.
@@ -243,6 +316,130 @@ __device__ __forceinline__ void stg_pairs<F16>(void* p, const float2 (&f)[4]) {
     st_stream_u4(p, make_uint4(w[0], w[1], w[2], w[3]));
 }
 
+// ------------------------------------------------------------------ per-row math (both ring kernels)
+// A thread owns the 16-byte column vectors vi = tid + k*nthreads (k < NV, vi <
+// nvec) of the columns a CTA covers; g holds gamma for them, acc_g / acc_b the
+// CTA's dgamma / dbeta partial sums.  xr and dyr point at the staged row (the
+// CTA's columns of it) in shared memory.
+
+// Phase 1: this thread's shares of sum(dxhat) (sa) and sum(dxhat*xhat) (sb).
+template <class Fmt, int NV, bool kRms>
+__device__ __forceinline__ void row_shares(const unsigned char* xr, const unsigned char* dyr,
+                                           const float2 (&g)[NV][Pairs<Fmt>::kN], float mu,
+                                           float rs, int tid, int nthreads, int nvec, float& sa,
+                                           float& sb) {
+    constexpr int NP = Pairs<Fmt>::kN;
+    float2 sa2 = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+    const float2 nmu = make_float2(-mu, -mu), rs2 = make_float2(rs, rs);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int vi = tid + k * nthreads;
+        if (vi < nvec) {
+            float2 xv[NP], dy[NP];
+            lds_pairs<Fmt>(xr + (size_t)vi * 16, xv);
+            lds_pairs<Fmt>(dyr + (size_t)vi * 16, dy);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float2 xh = kRms ? __fmul2_rn(xv[q], rs2)
+                                       : __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
+                const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
+                if (!kRms) sa2 = __fadd2_rn(sa2, dxh);
+                sb2 = __ffma2_rn(dxh, xh, sb2);
+            }
+        }
+    }
+    sa = sa2.x + sa2.y;
+    sb = sb2.x + sb2.y;
+}
+
+// Phase 2: dX of the row (dxr: the CTA's first column of it in global memory)
+// and the column partials, from the row means mean_a = mean(dxhat) and
+// mean_b = mean(dxhat*xhat):
+//   dX = rs*dxhat - rs*mean_a - rs*mean_b*xhat  (two packed FMAs per pair)
+template <class Fmt, int NV, bool kRms>
+__device__ __forceinline__ void row_dx(const unsigned char* xr, const unsigned char* dyr,
+                                       typename Fmt::T* dxr, const float2 (&g)[NV][Pairs<Fmt>::kN],
+                                       float2 (&acc_g)[NV][Pairs<Fmt>::kN],
+                                       float2 (&acc_b)[NV][Pairs<Fmt>::kN], float mu, float rs,
+                                       float mean_a, float mean_b, int tid, int nthreads,
+                                       int nvec) {
+    constexpr int NP = Pairs<Fmt>::kN;
+    constexpr int E = Vec<Fmt>::kElems;
+    const float2 nmu = make_float2(-mu, -mu), rs2 = make_float2(rs, rs);
+    const float c0 = -(rs * mean_a), c1 = -(rs * mean_b);
+    const float2 nc0 = make_float2(c0, c0), nc1 = make_float2(c1, c1);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int vi = tid + k * nthreads;
+        if (vi < nvec) {
+            float2 xv[NP], dy[NP], out[NP];
+            lds_pairs<Fmt>(xr + (size_t)vi * 16, xv);
+            lds_pairs<Fmt>(dyr + (size_t)vi * 16, dy);
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float2 xh = kRms ? __fmul2_rn(xv[q], rs2)
+                                       : __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
+                const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
+                out[q] = __ffma2_rn(dxh, rs2, __ffma2_rn(xh, nc1, nc0));
+                acc_g[k][q] = __ffma2_rn(dy[q], xh, acc_g[k][q]);
+                if (!kRms) acc_b[k][q] = __fadd2_rn(acc_b[k][q], dy[q]);
+            }
+            stg_pairs<Fmt>(dxr + (size_t)vi * E, out);
+        }
+    }
+}
+
+// Sum of the kMaxWarps per-warp values at p, in a fixed order.
+__device__ __forceinline__ float cta_total(const float* p) {
+    const float4 a0 = *reinterpret_cast<const float4*>(p);
+    const float4 a1 = *reinterpret_cast<const float4*>(p + 4);
+    return ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
+}
+
+// gamma of the thread's columns (zero past nvec); the partial sums start at zero.
+template <class Fmt, int NV>
+__device__ __forceinline__ void load_gamma(const float* __restrict__ gamma, float2 (&g)[NV][Pairs<Fmt>::kN],
+                                           float2 (&acc_g)[NV][Pairs<Fmt>::kN],
+                                           float2 (&acc_b)[NV][Pairs<Fmt>::kN], int tid,
+                                           int nthreads, int nvec) {
+    constexpr int E = Vec<Fmt>::kElems;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int vi = tid + k * nthreads;
+#pragma unroll
+        for (int q = 0; q < Pairs<Fmt>::kN; ++q) {
+            g[k][q] = vi < nvec ? make_float2(gamma[vi * E + 2 * q], gamma[vi * E + 2 * q + 1])
+                                : make_float2(0.f, 0.f);
+            acc_g[k][q] = make_float2(0.f, 0.f);
+            acc_b[k][q] = make_float2(0.f, 0.f);
+        }
+    }
+}
+
+// Store the thread's column partials (pg: dgamma partials of the CTA's first
+// column; pb: dbeta partials, LayerNorm only).
+template <class Fmt, int NV, bool kRms>
+__device__ __forceinline__ void store_partials(float* pg, float* pb,
+                                               const float2 (&acc_g)[NV][Pairs<Fmt>::kN],
+                                               const float2 (&acc_b)[NV][Pairs<Fmt>::kN], int tid,
+                                               int nthreads, int nvec) {
+    constexpr int E = Vec<Fmt>::kElems;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int vi = tid + k * nthreads;
+        if (vi < nvec) {
+#pragma unroll
+            for (int q = 0; q < Pairs<Fmt>::kN; q += 2) {
+                *reinterpret_cast<float4*>(pg + vi * E + 2 * q) =
+                    make_float4(acc_g[k][q].x, acc_g[k][q].y, acc_g[k][q + 1].x, acc_g[k][q + 1].y);
+                if (!kRms)
+                    *reinterpret_cast<float4*>(pb + vi * E + 2 * q) =
+                        make_float4(acc_b[k][q].x, acc_b[k][q].y, acc_b[k][q + 1].x, acc_b[k][q + 1].y);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ row kernel (bulk-copy ring)
 // A ring stage holds a group of R consecutive rows: [R rows of x | R rows of dY].
 // Columns per thread NV*E up to 16 fit two CTAs per SM; 32 need the full budget.
@@ -313,17 +510,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
 
     constexpr int NP = Pairs<Fmt>::kN;
     float2 g[NV][NP], acc_g[NV][NP], acc_b[NV][NP];
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = tid + k * nthreads;
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-            g[k][q] = vi < nvec ? make_float2(gamma[vi * E + 2 * q], gamma[vi * E + 2 * q + 1])
-                                : make_float2(0.f, 0.f);
-            acc_g[k][q] = make_float2(0.f, 0.f);
-            acc_b[k][q] = make_float2(0.f, 0.f);
-        }
-    }
+    load_gamma<Fmt, NV>(gamma, g, acc_g, acc_b, tid, nthreads, nvec);
     float mu[R], rs[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
@@ -355,29 +542,12 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         float sa[R], sb[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-            float2 sa2 = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
-            if (ok && i < nr) {
-                const float2 nmu = make_float2(-mu[i], -mu[i]), rs2 = make_float2(rs[i], rs[i]);
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int vi = tid + k * nthreads;
-                    if (vi < nvec) {
-                        float2 xv[NP], dy[NP];
-                        lds_pairs<Fmt>(st + (size_t)i * row_bytes + (size_t)vi * 16, xv);
-                        lds_pairs<Fmt>(st + grp_bytes + (size_t)i * row_bytes + (size_t)vi * 16, dy);
-#pragma unroll
-                        for (int q = 0; q < NP; ++q) {
-                            const float2 xh = kRms ? __fmul2_rn(xv[q], rs2)
-                                                   : __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
-                            const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
-                            if (!kRms) sa2 = __fadd2_rn(sa2, dxh);
-                            sb2 = __ffma2_rn(dxh, xh, sb2);
-                        }
-                    }
-                }
-            }
-            sa[i] = sa2.x + sa2.y;
-            sb[i] = sb2.x + sb2.y;
+            sa[i] = 0.f;
+            sb[i] = 0.f;
+            if (ok && i < nr)
+                row_shares<Fmt, NV, kRms>(st + (size_t)i * row_bytes,
+                                          st + grp_bytes + (size_t)i * row_bytes, g, mu[i], rs[i],
+                                          tid, nthreads, nvec, sa[i], sb[i]);
         }
         float sums[2 * R];
 #pragma unroll
@@ -401,40 +571,16 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         }
 
         // Phase 2: dX and the column partials, re-reading the staged rows.
-        //   dX = rs*dxhat - rs*mean_a - rs*mean_b*xhat  (two packed FMAs per pair)
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             if (i < nr) {
-                const float4 a0 = *reinterpret_cast<const float4*>(&red[buf][2 * i][0]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&red[buf][2 * i][4]);
-                const float4 b0 = *reinterpret_cast<const float4*>(&red[buf][2 * i + 1][0]);
-                const float4 b1 = *reinterpret_cast<const float4*>(&red[buf][2 * i + 1][4]);
-                const float a = ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
-                const float b = ((b0.x + b0.y) + (b0.z + b0.w)) + ((b1.x + b1.y) + (b1.z + b1.w));
+                const float a = cta_total(&red[buf][2 * i][0]);
+                const float b = cta_total(&red[buf][2 * i + 1][0]);
                 const float mean_a = kRms ? 0.f : a * inv_D, mean_b = b * inv_D;
-                const float2 nmu = make_float2(-mu[i], -mu[i]), rs2 = make_float2(rs[i], rs[i]);
-                const float c0 = -(rs[i] * mean_a), c1 = -(rs[i] * mean_b);
-                const float2 nc0 = make_float2(c0, c0), nc1 = make_float2(c1, c1);
-                T* dxr = dX + (first + i) * D;
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    const int vi = tid + k * nthreads;
-                    if (vi < nvec) {
-                        float2 xv[NP], dy[NP], out[NP];
-                        lds_pairs<Fmt>(st + (size_t)i * row_bytes + (size_t)vi * 16, xv);
-                        lds_pairs<Fmt>(st + grp_bytes + (size_t)i * row_bytes + (size_t)vi * 16, dy);
-#pragma unroll
-                        for (int q = 0; q < NP; ++q) {
-                            const float2 xh = kRms ? __fmul2_rn(xv[q], rs2)
-                                                   : __fmul2_rn(__fadd2_rn(xv[q], nmu), rs2);
-                            const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
-                            out[q] = __ffma2_rn(dxh, rs2, __ffma2_rn(xh, nc1, nc0));
-                            acc_g[k][q] = __ffma2_rn(dy[q], xh, acc_g[k][q]);
-                            if (!kRms) acc_b[k][q] = __fadd2_rn(acc_b[k][q], dy[q]);
-                        }
-                        stg_pairs<Fmt>(dxr + (size_t)vi * E, out);
-                    }
-                }
+                row_dx<Fmt, NV, kRms>(st + (size_t)i * row_bytes,
+                                      st + grp_bytes + (size_t)i * row_bytes, dX + (first + i) * D,
+                                      g, acc_g, acc_b, mu[i], rs[i], mean_a, mean_b, tid, nthreads,
+                                      nvec);
             }
         }
 #pragma unroll
@@ -460,21 +606,225 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
     pdl_trigger();
 
     float* pg = partials + (size_t)blockIdx.x * (kRms ? 1 : 2) * D;
-    float* pb = pg + D;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = tid + k * nthreads;
-        if (vi < nvec) {
-#pragma unroll
-            for (int q = 0; q < NP; q += 2) {
-                *reinterpret_cast<float4*>(pg + vi * E + 2 * q) =
-                    make_float4(acc_g[k][q].x, acc_g[k][q].y, acc_g[k][q + 1].x, acc_g[k][q + 1].y);
-                if (!kRms)
-                    *reinterpret_cast<float4*>(pb + vi * E + 2 * q) =
-                        make_float4(acc_b[k][q].x, acc_b[k][q].y, acc_b[k][q + 1].x, acc_b[k][q + 1].y);
+    store_partials<Fmt, NV, kRms>(pg, pg + D, acc_g, acc_b, tid, nthreads, nvec);
+}
+
+// ------------------------------------------------------------------ row kernel (split over a cluster)
+// Rows wider than one CTA's register budget are split by columns over the C
+// CTAs of a thread-block cluster (2 <= C <= 8).  CTA k of a cluster owns the
+// column slice [k*D/C, (k+1)*D/C): for every row of the cluster's row block it
+// streams that slice of x and dY into its own ring (one bulk copy per row and
+// tensor), keeps gamma and the column partials of the slice in registers, and
+// forms the slice's share of the two row sums.  The shares travel through
+// distributed shared memory: each CTA stores its 2R sums and a failure flag
+// into the exchange slot of every other CTA with st.async, counted as
+// transaction bytes on that CTA's exchange mbarrier (two slots, alternating by
+// group).  Every CTA adds the C shares in rank order, so all of them use
+// bitwise the same row sums.  A cluster owns one partial row of the workspace;
+// its CTAs fill disjoint column ranges of it.
+//
+// Only the 2R+1 exchanging threads wait for the peers; the rest of the CTA meets
+// them at the barrier that publishes the row sums (through shared memory).
+// Slot reuse is safe without further handshakes: a CTA sends group g+2 into a
+// slot only after it has received every share of group g+1, and each CTA sends
+// its share of g+1 only after its threads have read the slot's group-g shares
+// and after it has armed the slot's barrier for g+2 (expected bytes), so a
+// phase is always armed before any peer's bytes for it arrive.
+//
+// The kernel is launched without the programmatic-dependent attribute: launched
+// early, while the previous kernel still held SMs, clusters of three or more CTAs
+// were placed so that part of the grid ran as a second wave (twice the time).
+// A CTA whose ring wait gives up still sends its shares (with the flag set), so
+// the whole cluster leaves the loop at the same group; every CTA then waits
+// (bounded) for its own copies in flight, and the cluster synchronises once more
+// before any CTA exits, so no CTA's shared memory goes away while a peer may
+// still store into it.
+template <class Fmt, int NV, int R, bool kRms>
+__global__ void __launch_bounds__(kRowThreads, (NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
+ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
+                         const float* __restrict__ mean, const float* __restrict__ inv_std,
+                         const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
+                         float* __restrict__ partials, int64_t rows, int D, int stages,
+                         int64_t rows_per_cluster, int* err, unsigned long long wait_limit_ns,
+                         int withhold_copies) {
+    using T = typename Fmt::T;
+    constexpr int E = Vec<Fmt>::kElems;
+    constexpr int kWords = 2 * R + 1;   // shares: 2R row sums, then the failure flag
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(16) float red[2][2 * R][kMaxWarps];
+    __shared__ float xs[2][kMaxCluster][kWords];
+    __shared__ float rsum[2 * R];   // the group's row sums, published for phase 2
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nthreads = blockDim.x;
+    const uint32_t rank = cluster_ctarank(), csize = cluster_nctarank();
+    // Launched with 2..kMaxCluster CTAs per cluster only (with one, a CTA could
+    // complete an exchange phase on its own ahead of its slower threads).
+    if (csize < 2 || csize > (uint32_t)kMaxCluster) {   // uniform over the grid
+        if (tid == 0) atomicExch(err, (int)TB_ERR_INVALID_VALUE);
+        return;
+    }
+    const int Dc = D / (int)csize;
+    const int col0 = (int)rank * Dc;
+    const int nvec = Dc / E;
+    const uint32_t slice_bytes = (uint32_t)Dc * (uint32_t)sizeof(T);
+    const uint32_t half_bytes = (uint32_t)R * slice_bytes;   // x part of a stage; dY follows
+    for (int i = tid; i < 2 * 2 * R * kMaxWarps; i += nthreads) (&red[0][0][0])[i] = 0.f;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);   // ring stages
+    uint64_t* xbar = bars + kMaxStages;                   // exchange slots 0 and 1
+    unsigned char* ring = smem + kBarRegion;              // stage s at ring + s * 2 * half_bytes
+
+    const int64_t r0 = (int64_t)cluster_index() * rows_per_cluster;
+    const int64_t r1 = r0 + rows_per_cluster < rows ? r0 + rows_per_cluster : rows;
+    const int64_t nrows = r1 > r0 ? r1 - r0 : 0;
+    const int64_t ngroups = (nrows + R - 1) / R;
+
+    uint64_t pol = 0;
+    int64_t issued = 0;   // groups issued so far (thread 0 only)
+    auto issue = [&](int64_t grp, int s) {
+        const int64_t first = r0 + grp * R;
+        const int nr = (int)(nrows - grp * R < R ? nrows - grp * R : R);
+        const uint32_t bar = smem_addr(&bars[s]);
+        unsigned char* st = ring + (size_t)s * 2 * half_bytes;
+        mbar_arrive_expect_tx(bar, 2u * (uint32_t)nr * slice_bytes);
+        if (withhold_copies) return;   // self-test: the stage's barrier never completes
+        for (int i = 0; i < nr; ++i) {
+            const int64_t off = (first + i) * D + col0;
+            bulk_g2s(smem_addr(st + (size_t)i * slice_bytes), x + off, slice_bytes, bar, pol);
+            bulk_g2s(smem_addr(st + half_bytes + (size_t)i * slice_bytes), dY + off, slice_bytes,
+                     bar, pol);
+        }
+    };
+    const uint32_t xs_bytes = (csize - 1) * (uint32_t)kWords * 4u;   // a slot phase's bytes
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        // groups 0 and 1 armed now; group g+2 once group g's phase has completed
+        mbar_arrive_expect_tx(smem_addr(&xbar[0]), xs_bytes);
+        mbar_arrive_expect_tx(smem_addr(&xbar[1]), xs_bytes);
+        mbar_init_fence();
+        pol = evict_first_policy();
+        if (ngroups > 0 && !withhold_copies) {
+            const int nr0 = (int)(nrows < R ? nrows : R);
+            for (int i = 0; i < nr0; ++i) {
+                bulk_prefetch_l2(x + (r0 + i) * D + col0, slice_bytes);
+                bulk_prefetch_l2(dY + (r0 + i) * D + col0, slice_bytes);
             }
         }
     }
+    // Every CTA's barriers are initialised (and `red` zeroed) before any peer
+    // stores into them.  Only shared memory has been touched so far.
+    cluster_sync_all();
+    pdl_wait();
+    if (tid == 0)
+        for (; issued < ngroups && issued < stages; ++issued) issue(issued, (int)issued);
+
+    constexpr int NP = Pairs<Fmt>::kN;
+    float2 g[NV][NP], acc_g[NV][NP], acc_b[NV][NP];
+    load_gamma<Fmt, NV>(gamma + col0, g, acc_g, acc_b, tid, nthreads, nvec);
+    float mu[R], rs[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        mu[i] = (!kRms && i < nrows) ? mean[r0 + i] : 0.f;
+        rs[i] = i < nrows ? inv_std[r0 + i] : 0.f;
+    }
+
+    const float inv_D = 1.0f / (float)D;
+    int64_t fail_at = -1;
+    for (int64_t grp = 0; grp < ngroups; ++grp) {
+        const int s = (int)(grp % stages);
+        const uint32_t parity = (uint32_t)((grp / stages) & 1);
+        const int64_t first = r0 + grp * R;
+        const int nr = (int)(nrows - grp * R < R ? nrows - grp * R : R);
+        float mu_n[R], rs_n[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int64_t rn = first + R + i;
+            const bool has = rn < r1;
+            mu_n[i] = (!kRms && has) ? mean[rn] : 0.f;
+            rs_n[i] = has ? inv_std[rn] : 0.f;
+        }
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity, wait_limit_ns);
+        const unsigned char* st = ring + (size_t)s * 2 * half_bytes;
+
+        // Phase 1: this CTA's shares of the row sums of the group.
+        float sums[2 * R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            sums[2 * i] = 0.f;
+            sums[2 * i + 1] = 0.f;
+            if (ok && i < nr)
+                row_shares<Fmt, NV, kRms>(st + (size_t)i * slice_bytes,
+                                          st + half_bytes + (size_t)i * slice_bytes, g, mu[i],
+                                          rs[i], tid, nthreads, nvec, sums[2 * i], sums[2 * i + 1]);
+        }
+        const float wsum = warp_sum_multi<2 * R>(sums, lane);
+        const int buf = (int)(grp & 1);
+        if (multi_writer<2 * R>(lane)) red[buf][multi_index<2 * R>(lane)][wid] = wsum;
+        // Past this barrier every thread has finished the previous group entirely.
+        const bool failed_here = __syncthreads_or(!ok);
+        if (tid == 0 && !failed_here && grp >= 1 && issued < ngroups) {
+            fence_proxy_async_smem();
+            issue(issued, (int)((grp - 1) % stages));
+            ++issued;
+        }
+        // Thread j < 2R owns row sum j, thread 2R the failure flag: it sends this
+        // CTA's share to every other CTA of the cluster, waits for theirs, and adds
+        // the C shares in rank order (the flags add up to the number of failed CTAs).
+        bool xok = true, flagged = false;
+        if (tid < kWords) {
+            const uint32_t xbar_local = smem_addr(&xbar[buf]);
+            const float own = tid < 2 * R ? cta_total(&red[buf][tid][0]) : (failed_here ? 1.f : 0.f);
+            const uint32_t slot = smem_addr(&xs[buf][rank][tid]);
+            for (uint32_t p = 0; p < csize; ++p)
+                if (p != rank) st_async_remote(map_to_rank(slot, p), own, map_to_rank(xbar_local, p));
+            xok = mbar_wait_cluster_bounded(xbar_local, (uint32_t)((grp >> 1) & 1), wait_limit_ns);
+            if (tid == 0 && xok && grp + 2 < ngroups) mbar_arrive_expect_tx(xbar_local, xs_bytes);
+            float t = 0.f;
+            for (uint32_t c = 0; c < csize; ++c) t += c == rank ? own : xs[buf][c][tid];
+            if (tid < 2 * R) rsum[tid] = t;
+            else flagged = t != 0.f;
+        }
+        // One decision for the whole CTA; past it the row sums are visible to all.
+        if (__syncthreads_or(!xok || flagged)) {
+            fail_at = grp;
+            break;
+        }
+
+        // Phase 2: dX and the column partials of this CTA's slice.
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            if (i < nr) {
+                const float mean_a = kRms ? 0.f : rsum[2 * i] * inv_D, mean_b = rsum[2 * i + 1] * inv_D;
+                row_dx<Fmt, NV, kRms>(st + (size_t)i * slice_bytes,
+                                      st + half_bytes + (size_t)i * slice_bytes,
+                                      dX + (first + i) * D + col0, g, acc_g, acc_b, mu[i], rs[i],
+                                      mean_a, mean_b, tid, nthreads, nvec);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            mu[i] = mu_n[i];
+            rs[i] = rs_n[i];
+        }
+    }
+
+    if (fail_at >= 0) {
+        if (tid == 0) {
+            atomicExch(err, (int)TB_ERR_TIMEOUT);
+            for (int64_t q = fail_at; q < issued; ++q)
+                mbar_wait_bounded(smem_addr(&bars[q % stages]), (uint32_t)((q / stages) & 1),
+                                  wait_limit_ns);
+        }
+        __syncthreads();
+        cluster_sync_all();
+        return;
+    }
+    pdl_trigger();
+    float* pg = partials + (size_t)cluster_index() * (kRms ? 1 : 2) * D + col0;
+    store_partials<Fmt, NV, kRms>(pg, pg + D, acc_g, acc_b, tid, nthreads, nvec);
+    cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ row kernel (plain loads)
@@ -588,17 +938,19 @@ cudaError_t launch_colsum(const float* ws, int G, int64_t W, int64_t D, float* d
 }
 
 // ------------------------------------------------------------------ launch planning
-enum class Path { kRing, kPlain };
+enum class Path { kRing, kSplit, kPlain };
 
 struct LnPlan {
     Path path;
     int threads;
-    int nv;          // vectors per thread (ring path)
-    int r;           // rows per ring stage (ring path)
+    int nv;          // vectors per thread (ring and split paths)
+    int r;           // rows per ring stage (ring and split paths)
     int stages;      // ring stages
-    size_t smem;     // dynamic shared memory (ring path)
-    int grid;        // CTAs of the row kernel == partial rows in the workspace
-    int64_t rows_per_cta;
+    size_t smem;     // dynamic shared memory (ring and split paths)
+    int cluster = 1; // CTAs a row is split over (split path), else 1
+    int grid;        // CTAs of the row kernel
+    int parts;       // partial rows in the workspace: grid / cluster
+    int64_t rows_per_cta;   // rows per CTA (per cluster on the split path)
     unsigned long long wait_limit_ns = kWaitLimitNs;   // bound of every wait (ring path)
     int withhold_copies = 0;   // self-test only: issue no copies, so every wait runs out
 };
@@ -651,6 +1003,42 @@ const void* ring_kernel(tb_dtype dt, int nv, int r, bool rms) {
     }
 }
 
+// Op<Fmt, NV, R>::run(args...) for the split kernel's instantiated (nv, r) pairs:
+// 16 or 32 columns per thread.
+template <class Fmt, template <class, int, int> class Op, class... Args>
+auto with_split_variant(int nv, int r, Args&&... args) {
+    constexpr int nv16 = 16 / Vec<Fmt>::kElems;
+    if (nv <= nv16) {
+        if (nv16 == 2 && r >= 2) return Op<Fmt, nv16, (nv16 == 2 ? 2 : 1)>::run(args...);
+        return Op<Fmt, nv16, 1>::run(args...);
+    }
+    return Op<Fmt, 2 * nv16, 1>::run(args...);
+}
+
+template <bool kRms>
+struct SplitOps {
+    template <class Fmt, int NV, int R>
+    struct Ptr {
+        static const void* run() {
+            return reinterpret_cast<const void*>(&ln_bwd_rows_split_kernel<Fmt, NV, R, kRms>);
+        }
+    };
+};
+
+template <class Fmt>
+const void* split_kernel_for(int nv, int r, bool rms) {
+    return rms ? with_split_variant<Fmt, SplitOps<true>::template Ptr>(nv, r)
+               : with_split_variant<Fmt, SplitOps<false>::template Ptr>(nv, r);
+}
+
+const void* split_kernel(tb_dtype dt, int nv, int r, bool rms) {
+    switch (dt) {
+        case TB_F32: return split_kernel_for<F32>(nv, r, rms);
+        case TB_BF16: return split_kernel_for<BF16>(nv, r, rms);
+        default: return split_kernel_for<F16>(nv, r, rms);
+    }
+}
+
 template <class Fmt>
 const void* plain_kernel_for(bool rms) {
     return rms ? reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<Fmt, true>)
@@ -665,6 +1053,50 @@ const void* plain_kernel(tb_dtype dt, bool rms) {
     }
 }
 
+// Cluster size for splitting rows of D columns: the smallest C in [2, 8] that
+// cuts a row into slices of whole 16-byte vectors of at most `target` columns
+// (0 if there is none).
+int split_cluster_size(int64_t D, int64_t E, int64_t target) {
+    for (int64_t c = std::max<int64_t>(2, (D + target - 1) / target); c <= kMaxCluster; ++c)
+        if (D % (c * E) == 0) return (int)c;
+    return 0;
+}
+
+// Split path (rows of D > kSplitFromD columns): C CTAs per row, each with 16
+// columns per thread when the slice allows it, else 32.
+bool make_split_plan(int64_t rows, int64_t D, tb_dtype dt, LnPlan* p, bool rms) {
+    const int64_t es = (int64_t)dtype_size(dt);
+    const int64_t E = 16 / es;
+    int c = split_cluster_size(D, E, kSplitSliceTarget);
+    if (c == 0) c = split_cluster_size(D, E, (int64_t)kMaxElemsPerThread * kRowThreads);
+    if (c == 0) return false;
+    const int64_t Dc = D / c;
+    const int64_t nvec = Dc / E;
+    const int nv = (int)((Dc <= (int64_t)16 * kRowThreads ? 16 : 32) / E);
+    const int64_t need_threads = (nvec + nv - 1) / nv;   // nv vectors each, before rounding to warps
+    const int threads = (int)std::min<int64_t>(kRowThreads, (need_threads + 31) / 32 * 32);
+    const int64_t slice_bytes = Dc * es;
+    int r = 1;
+    while (r < max_r_for(nv) && (int64_t)(2 * r) * slice_bytes <= kStageTargetBytes / 2) r *= 2;
+    const int64_t stage_bytes = 2 * (int64_t)r * slice_bytes;
+    const int stages =
+        (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
+    const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
+    const int clusters = resident_clusters(split_kernel(dt, nv, r, rms), threads, smem, c);
+    if (clusters == 0) return false;
+    p->path = Path::kSplit;
+    p->threads = threads;
+    p->nv = nv;
+    p->r = r;
+    p->stages = stages;
+    p->smem = smem;
+    p->cluster = c;
+    p->parts = (int)std::min<int64_t>(clusters, rows);
+    p->grid = p->parts * c;
+    p->rows_per_cta = (rows + p->parts - 1) / p->parts;
+    return true;
+}
+
 // `aligned`: every row buffer 16-byte aligned (the caller checks pointers).
 bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceInfo& info,
                LnPlan* p, bool rms = false) {
@@ -673,6 +1105,10 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
     const int64_t row_bytes = D * es;
     const int64_t nvec = D / E;
     p->path = Path::kPlain;
+    p->cluster = 1;
+    if (aligned && row_bytes % 16 == 0 && D > kSplitFromD && rows > 0 &&
+        make_split_plan(rows, D, dt, p, rms))
+        return true;
     // Ring path: at most kMaxElemsPerThread columns per thread (gamma and the two
     // partial sums live in registers), i.e. D <= 8192.
     if (aligned && row_bytes % 16 == 0 && D <= (int64_t)kMaxElemsPerThread * kRowThreads) {
@@ -709,12 +1145,13 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
         p->grid = info.sm_count * std::min(per_sm, 2);
     }
     p->grid = (int)std::min<int64_t>(p->grid, rows);
+    p->parts = p->grid;
     p->rows_per_cta = p->grid > 0 ? (rows + p->grid - 1) / p->grid : 0;
     return true;
 }
 
 size_t workspace_bytes_for(const LnPlan& p, int64_t D, bool rms = false) {
-    return (size_t)p.grid * (rms ? 1 : 2) * (size_t)D * sizeof(float);
+    return (size_t)p.parts * (rms ? 1 : 2) * (size_t)D * sizeof(float);
 }
 
 template <bool kRms>
@@ -733,6 +1170,23 @@ struct RingLaunchOps {
     };
 };
 
+template <bool kRms>
+struct SplitLaunchOps {
+    template <class Fmt, int NV, int R>
+    struct Launch {
+        using T = typename Fmt::T;
+        static int run(const LnPlan& p, const T* dy, const T* x, const float* mean,
+                       const float* inv_std, const float* gamma, T* dx, float* ws, int64_t rows,
+                       int D, int* err, cudaStream_t st) {
+            launch_cluster(ln_bwd_rows_split_kernel<Fmt, NV, R, kRms>, dim3((unsigned)p.grid),
+                           dim3((unsigned)p.threads), p.smem, st, p.cluster, dy, x, mean, inv_std,
+                           gamma, dx, ws, rows, D, p.stages, p.rows_per_cta, err, p.wait_limit_ns,
+                           p.withhold_copies);
+            return 0;
+        }
+    };
+};
+
 template <class Fmt>
 void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* mean,
                  const float* inv_std, const float* gamma, void* dX, float* ws, int64_t rows,
@@ -741,7 +1195,14 @@ void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* me
     const T* dy = static_cast<const T*>(dY);
     const T* xx = static_cast<const T*>(x);
     T* dx = static_cast<T*>(dX);
-    if (p.path == Path::kRing) {
+    if (p.path == Path::kSplit) {
+        if (rms)
+            with_split_variant<Fmt, SplitLaunchOps<true>::template Launch>(
+                p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
+        else
+            with_split_variant<Fmt, SplitLaunchOps<false>::template Launch>(
+                p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
+    } else if (p.path == Path::kRing) {
         if (rms)
             with_ring_variant<Fmt, RingLaunchOps<true>::template Launch>(
                 p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
@@ -831,7 +1292,7 @@ extern "C" tb_status tb_layernorm_bwd(const void* dY, const void* x, const float
         default: launch_rows<F16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
     }
     if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
-    return launch_colsum(ws, p.grid, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+    return launch_colsum(ws, p.parts, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ entry point without allocation
@@ -903,11 +1364,12 @@ extern "C" tb_status tb_layernorm_bwd_noalloc(const void* dY, const void* x, con
                          aligned_to(gamma, 16);
     LnPlan p;
     if (!make_plan(rows, D, io_dtype, aligned, info, &p)) return TB_ERR_CUDA;
-    // Fewer CTAs when their partial sums would not fit in the scratch array.
-    const int64_t max_grid = kNoAllocScratchFloats / (2 * D);
-    if (p.grid > max_grid) {
-        p.grid = (int)max_grid;
-        p.rows_per_cta = (rows + p.grid - 1) / p.grid;
+    // Fewer CTAs (clusters) when their partial sums would not fit in the scratch array.
+    const int64_t max_parts = kNoAllocScratchFloats / (2 * D);
+    if (p.parts > max_parts) {
+        p.parts = (int)max_parts;
+        p.grid = p.parts * p.cluster;
+        p.rows_per_cta = (rows + p.parts - 1) / p.parts;
     }
     // Every CTA overwrites its whole partial row, so nothing needs clearing first.
     switch (io_dtype) {
@@ -916,7 +1378,7 @@ extern "C" tb_status tb_layernorm_bwd_noalloc(const void* dY, const void* x, con
         default: launch_rows<F16>(p, dY, x, mean, inv_std, gamma, dX, ws, rows, D, err, st); break;
     }
     if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
-    return launch_colsum(ws, p.grid, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+    return launch_colsum(ws, p.parts, 2 * D, D, dgamma, dbeta, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ RMSNorm backward
@@ -987,45 +1449,62 @@ extern "C" tb_status tb_rmsnorm_bwd(const void* dY, const void* x, const float* 
         default: launch_rows<F16>(p, dY, x, nullptr, inv_rms, gamma, dX, ws, rows, D, err, st, true); break;
     }
     if (cudaGetLastError() != cudaSuccess) return TB_ERR_CUDA;
-    return launch_colsum(ws, p.grid, D, D, dgamma, nullptr, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
+    return launch_colsum(ws, p.parts, D, D, dgamma, nullptr, st) == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ self-test of the bounded waits
-extern "C" tb_status tb_layernorm_bwd_selftest_timeout(int64_t wait_limit_ns, void* stream) {
-    using namespace tb;
-    if (wait_limit_ns < 1000 || wait_limit_ns > (int64_t)kWaitLimitNs) return TB_ERR_INVALID_VALUE;
-    int dev = 0;
-    DeviceInfo info{};
-    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
-    constexpr int64_t kRows = 4, kD = 256;
+namespace tb {
+namespace {
+// Runs the row kernel of a plan for rows x D bf16 with every copy withheld, so
+// every ring wait gives up after wait_limit_ns.
+tb_status run_withheld(int64_t rows, int64_t D, Path want, int64_t wait_limit_ns,
+                       const DeviceInfo& info, int* err, cudaStream_t st) {
     LnPlan p;
-    if (!make_plan(kRows, kD, TB_BF16, true, info, &p) || p.path != Path::kRing) return TB_ERR_CUDA;
+    if (!make_plan(rows, D, TB_BF16, true, info, &p) || p.path != want) return TB_ERR_CUDA;
     p.wait_limit_ns = (unsigned long long)wait_limit_ns;
     p.withhold_copies = 1;
-    int* err = device_error_word();
-    if (!err) return TB_ERR_CUDA;
     // One zeroed allocation holds x, dY, dX, mean, inv_std, gamma and the workspace,
     // each part starting on a 256-byte boundary.
-    const size_t mat = (size_t)kRows * kD * sizeof(uint16_t);
-    const size_t off_dy = mat, off_dx = 2 * mat, off_mu = 3 * mat, off_rs = off_mu + 256;
-    const size_t off_g = off_rs + 256, off_ws = off_g + (size_t)kD * sizeof(float);
-    const size_t total = off_ws + workspace_bytes_for(p, kD);
+    const size_t mat = ((size_t)rows * D * sizeof(uint16_t) + 255) / 256 * 256;
+    const size_t off_dy = mat, off_dx = 2 * mat, off_mu = 3 * mat;
+    const size_t off_rs = off_mu + ((size_t)rows * 4 + 255) / 256 * 256;
+    const size_t off_g = off_rs + ((size_t)rows * 4 + 255) / 256 * 256;
+    const size_t off_ws = off_g + ((size_t)D * sizeof(float) + 255) / 256 * 256;
+    const size_t total = off_ws + workspace_bytes_for(p, D);
     unsigned char* buf = nullptr;
     if (cudaMalloc(&buf, total) != cudaSuccess) {
         cudaGetLastError();
         return TB_ERR_OOM;
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     tb_status status = TB_OK;
     if (cudaMemsetAsync(buf, 0, total, st) != cudaSuccess) {
         status = TB_ERR_CUDA;
     } else {
         launch_rows<BF16>(p, buf + off_dy, buf, reinterpret_cast<float*>(buf + off_mu),
                           reinterpret_cast<float*>(buf + off_rs), reinterpret_cast<float*>(buf + off_g),
-                          buf + off_dx, reinterpret_cast<float*>(buf + off_ws), kRows, kD, err, st);
+                          buf + off_dx, reinterpret_cast<float*>(buf + off_ws), rows, D, err, st);
         if (cudaGetLastError() != cudaSuccess) status = TB_ERR_CUDA;
     }
     if (cudaStreamSynchronize(st) != cudaSuccess) status = TB_ERR_CUDA;
     if (cudaFree(buf) != cudaSuccess) status = TB_ERR_CUDA;
     return status;
+}
+}  // namespace
+}  // namespace tb
+
+extern "C" tb_status tb_layernorm_bwd_selftest_timeout(int64_t wait_limit_ns, void* stream) {
+    using namespace tb;
+    if (wait_limit_ns < 1000 || wait_limit_ns > (int64_t)kWaitLimitNs) return TB_ERR_INVALID_VALUE;
+    int dev = 0;
+    DeviceInfo info{};
+    if (!current_device_info(&dev, &info)) return TB_ERR_CUDA;
+    int* err = device_error_word();
+    if (!err) return TB_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The single-CTA ring (rows of 256 columns), then the cluster-split ring
+    // (rows of 8192 columns over two CTAs): every CTA of the cluster gives up at
+    // the same group and the cluster ends together.
+    const tb_status a = run_withheld(4, 256, Path::kRing, wait_limit_ns, info, err, st);
+    if (a != TB_OK) return a;
+    return run_withheld(4, 8192, Path::kSplit, wait_limit_ns, info, err, st);
 }

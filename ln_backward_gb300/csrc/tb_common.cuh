@@ -68,6 +68,12 @@ int* device_error_word();
 // is above the default; results are cached per (device, kernel, threads, smem).
 int resident_ctas_per_sm(const void* kernel, int threads, size_t dyn_smem);
 
+// Clusters of `cluster` CTAs of `kernel` that fit on the current device at once
+// with `threads` threads and `dyn_smem` bytes of dynamic shared memory per CTA
+// (0 on a CUDA error, or when such a cluster cannot be placed).  Raises the
+// kernel's dynamic shared-memory limit first, as resident_ctas_per_sm does.
+int resident_clusters(const void* kernel, int threads, size_t dyn_smem, int cluster);
+
 inline tb_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? TB_OK : TB_ERR_CUDA;
 }
@@ -100,6 +106,28 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Launches `kernel` on `st` in thread-block clusters of `cluster` CTAs along x
+// (grid.x a multiple of `cluster`), in plain stream order: it starts once the
+// previous work in the stream has completed, so every cluster finds its SMs free
+// (its pdl_wait() returns at once).
+template <class... KArgs, class... Args>
+inline cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t st, int cluster, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);

@@ -5,9 +5,9 @@ Targets: fp32 dX within 1e-4 floored relative error; 16-bit dX within one
 fp32 arithmetic's own error bound for outputs that cancel -- see
 tests/tolerance.py); dgamma and dbeta within 1e-3 floored relative error.
 Covers the tiny config (1024 x 256 fp32), the full config (16,384 x 4,096 bf16,
-every element), a sweep of D across the ring and plain paths with ragged row
-counts, unaligned buffers, zero rows, bitwise determinism and the workspace
-check.
+every element), a sweep of D across the ring, cluster-split and plain paths
+with ragged row counts, rows split over clusters of 2..8 CTAs, unaligned
+buffers, zero rows, bitwise determinism and the workspace check.
 """
 import numpy as np
 import pytest
@@ -137,6 +137,43 @@ def test_workspace_too_small_is_rejected(tb, synth):
     with pytest.raises(tb.TbError) as ei:
         run(tb, *args, ws_bytes=16)     # the query may return more than one path needs
     assert ei.value.code == 5
+
+
+# Rows split over a thread-block cluster: cluster sizes 2..8 (16 columns per
+# thread), 32 columns per thread (D = 65,536), slices that leave threads idle
+# (4,104 / 8,200), row counts that leave clusters empty or ragged.
+# D -> CTAs per cluster the plan picks for 16-bit rows: the smallest of 2..8
+# giving slices of whole 16-byte vectors of at most 4,096 columns, else of at
+# most 8,192 (fp32 rows of 4,104 take two CTAs of 2,052 columns).
+SPLIT = {4104: 3, 5120: 2, 8192: 2, 10240: 4, 12288: 3, 16384: 4, 18432: 6, 20480: 5,
+         25600: 8, 65536: 8}
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
+                         ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", list(SPLIT), ids=[f"D{d}-cluster{c}" for d, c in SPLIT.items()])
+def test_rows_split_over_a_cluster(tb, synth, D, dtype):
+    for rows in (1, 5, 211):
+        args = synth.layernorm_inputs(rows, D, dtype, seed=3 * D + rows, device="cuda")
+        check(tb, *args, *run(tb, *args))
+
+
+def test_split_rows_many_clusters_bf16(tb, synth):
+    """4,096 x 12,288 bf16 (GPT-3-class hidden size): every cluster holds many
+    row groups, every element compared."""
+    args = synth.layernorm_inputs(4096, 12288, torch.bfloat16, seed=12, device="cuda", dy_std=1e-2)
+    out = run(tb, *args)
+    torch.cuda.synchronize()
+    check(tb, *args, *out)
+
+
+def test_split_rows_deterministic_bitwise(tb, synth):
+    args = synth.layernorm_inputs(3000, 16384, torch.bfloat16, seed=13, device="cuda", dy_std=1e-2)
+    a = run(tb, *args)
+    b = run(tb, *args)
+    torch.cuda.synchronize()
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
 
 
 def test_no_kernel_gave_up_waiting(tb):

@@ -90,7 +90,8 @@ def test_llama_hidden_bf16(tb, synth):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
                          ids=["f32", "bf16", "f16"])
-@pytest.mark.parametrize("D", [1, 3, 8, 100, 256, 1000, 2048, 4096, 4104, 8192, 12288])
+@pytest.mark.parametrize("D", [1, 3, 8, 100, 256, 1000, 2048, 4096, 4104, 8192, 12288, 16384,
+                               25600, 65536])
 def test_feature_dim_sweep(tb, synth, D, dtype):
     for rows in (1, 7, 300):
         args = synth.rmsnorm_inputs(rows, D, dtype, seed=D + rows, device="cuda")
