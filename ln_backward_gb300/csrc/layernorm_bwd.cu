@@ -521,9 +521,12 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
 
     const float inv_D = 1.0f / (float)D;
     int64_t fail_at = -1;
+    // Stage of this group and of the previous one, and the phase parity: advanced
+    // by counting (a 64-bit division by the run-time stage count costs dozens of
+    // instructions per group).
+    int s = 0, prev_s = stages - 1;
+    uint32_t parity = 0;
     for (int64_t grp = 0; grp < ngroups; ++grp) {
-        const int s = (int)(grp % stages);
-        const uint32_t parity = (uint32_t)((grp / stages) & 1);
         const int64_t first = r0 + grp * R;
         const int nr = (int)(nrows - grp * R < R ? nrows - grp * R : R);
         // Prefetch the next group's statistics while this one is processed.
@@ -566,7 +569,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         }
         if (tid == 0 && grp >= 1 && issued < ngroups) {
             fence_proxy_async_smem();
-            issue(issued, (int)((grp - 1) % stages));
+            issue(issued, prev_s);
             ++issued;
         }
 
@@ -587,6 +590,11 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
         for (int i = 0; i < R; ++i) {
             mu[i] = mu_n[i];
             rs[i] = rs_n[i];
+        }
+        prev_s = s;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
         }
     }
 
@@ -732,9 +740,12 @@ ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename 
 
     const float inv_D = 1.0f / (float)D;
     int64_t fail_at = -1;
+    // Stage of this group and of the previous one, and the phase parity: advanced
+    // by counting (a 64-bit division by the run-time stage count costs dozens of
+    // instructions per group).
+    int s = 0, prev_s = stages - 1;
+    uint32_t parity = 0;
     for (int64_t grp = 0; grp < ngroups; ++grp) {
-        const int s = (int)(grp % stages);
-        const uint32_t parity = (uint32_t)((grp / stages) & 1);
         const int64_t first = r0 + grp * R;
         const int nr = (int)(nrows - grp * R < R ? nrows - grp * R : R);
         float mu_n[R], rs_n[R];
@@ -766,7 +777,7 @@ ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename 
         const bool failed_here = __syncthreads_or(!ok);
         if (tid == 0 && !failed_here && grp >= 1 && issued < ngroups) {
             fence_proxy_async_smem();
-            issue(issued, (int)((grp - 1) % stages));
+            issue(issued, prev_s);
             ++issued;
         }
         // Thread j < 2R owns row sum j, thread 2R the failure flag: it sends this
@@ -807,6 +818,11 @@ ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename 
         for (int i = 0; i < R; ++i) {
             mu[i] = mu_n[i];
             rs[i] = rs_n[i];
+        }
+        prev_s = s;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
         }
     }
 
