@@ -86,8 +86,8 @@ tb_status tb_device_error(int* code, int reset);
  * tb_layernorm_bwd_selftest_timeout -- exercises that failure path without a
  * GPU fault.  It runs the LayerNorm backward's two bulk-copy ring kernels on
  * small internal problems (4 x 256 bf16 on one CTA per row block, then 4 x
- * 8,192 bf16 split over a two-CTA cluster; zeroed buffers the call allocates and
- * frees) with their copies withheld, so that every wait on them runs out after
+ * 16,384 bf16 split over a four-CTA cluster; zeroed buffers the call allocates
+ * and frees) with their copies withheld, so that every wait on them runs out after
  * wait_limit_ns nanoseconds; each kernel then sets the device error word to
  * TB_ERR_TIMEOUT, waits (bounded as well) for the copies it would have issued,
  * and returns -- the CTAs of a cluster together, after telling each other of the
@@ -331,11 +331,12 @@ tb_status tb_softmax_bwd_causal(const void* dY, const void* P, void* dX, int64_t
  * dgamma and dbeta are OVERWRITTEN (not accumulated).  They are reduced in two
  * stages -- per-CTA partial sums into the workspace, then a second kernel that
  * adds them in a fixed order -- so results are bitwise reproducible run to run
- * on the same device model.  Rows of more than 4,096 columns (16-byte aligned
- * buffers, D a multiple of 2..8 times the 16-byte vector) are split by columns
- * over the CTAs of a thread-block cluster, which exchange their shares of the
- * row sums through distributed shared memory and write one partial row per
- * cluster; all CTAs of a cluster use bitwise the same row sums.
+ * on the same device model.  Rows longer than 16 KB (more than 8,192 16-bit or
+ * 4,096 fp32 columns; 16-byte aligned buffers, D a multiple of 2..8 times the
+ * 16-byte vector) are split by columns over the CTAs of a thread-block cluster,
+ * which exchange their shares of the row sums through distributed shared memory
+ * and write one partial row per cluster; all CTAs of a cluster use bitwise the
+ * same row sums.
  */
 
 /*

@@ -23,7 +23,7 @@
 //    staged row (shared memory, not HBM), writes dX and accumulates the column
 //    partials.  A stage is refilled one row later, once every thread is past
 //    it.  At the end each CTA stores its column partials to the workspace.
-//  * Kernel 1' (rows wider than 4096 columns): the same ring, with each row
+//  * Kernel 1' (rows longer than 16 KB): the same ring, with each row
 //    split by columns over the 2..8 CTAs of a thread-block cluster.  Every CTA
 //    keeps the gamma and partials of its column slice in registers (so two CTAs
 //    still fit per SM) and the CTAs exchange their shares of the two row sums
@@ -59,7 +59,7 @@ constexpr int kStageTargetBytes = 32 * 1024;   // x + dY bytes per ring stage we
 constexpr int kBarRegion = 128;                // bytes reserved for the mbarriers
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr int kMaxCluster = 8;                 // CTAs a row may be split over (portable size)
-constexpr int64_t kSplitFromD = 4096;          // wider rows are split over a cluster
+constexpr int64_t kSplitFromRowBytes = 16 * 1024;   // longer rows are split over a cluster
 constexpr int64_t kSplitSliceTarget = 4096;    // columns per CTA we aim for when splitting
 
 // ------------------------------------------------------------------ PTX helpers
@@ -1078,8 +1078,9 @@ int split_cluster_size(int64_t D, int64_t E, int64_t target) {
     return 0;
 }
 
-// Split path (rows of D > kSplitFromD columns): C CTAs per row, each with 16
-// columns per thread when the slice allows it, else 32.
+// Split path (rows longer than kSplitFromRowBytes): C CTAs per row, each with
+// 16 columns per thread when the slice allows it, else 32.  (Up to 16 KB rows --
+// 8192 16-bit or 4096 fp32 columns -- the single-CTA ring measured faster.)
 bool make_split_plan(int64_t rows, int64_t D, tb_dtype dt, LnPlan* p, bool rms) {
     const int64_t es = (int64_t)dtype_size(dt);
     const int64_t E = 16 / es;
@@ -1092,11 +1093,14 @@ bool make_split_plan(int64_t rows, int64_t D, tb_dtype dt, LnPlan* p, bool rms) 
     const int64_t need_threads = (nvec + nv - 1) / nv;   // nv vectors each, before rounding to warps
     const int threads = (int)std::min<int64_t>(kRowThreads, (need_threads + 31) / 32 * 32);
     const int64_t slice_bytes = Dc * es;
+    // ring bytes in proportion to the CTA's warps, as on the ring path
+    const int64_t budget = (int64_t)kRingBudget * (threads / 32) / kMaxWarps;
+    const int64_t stage_target = std::min<int64_t>(kStageTargetBytes, budget / 3);
     int r = 1;
-    while (r < max_r_for(nv) && (int64_t)(2 * r) * slice_bytes <= kStageTargetBytes / 2) r *= 2;
+    while (r < max_r_for(nv) && (int64_t)(2 * r) * slice_bytes <= stage_target / 2) r *= 2;
     const int64_t stage_bytes = 2 * (int64_t)r * slice_bytes;
     const int stages =
-        (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
+        (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, budget / stage_bytes));
     const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
     const int clusters = resident_clusters(split_kernel(dt, nv, r, rms), threads, smem, c);
     if (clusters == 0) return false;
@@ -1122,7 +1126,7 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
     const int64_t nvec = D / E;
     p->path = Path::kPlain;
     p->cluster = 1;
-    if (aligned && row_bytes % 16 == 0 && D > kSplitFromD && rows > 0 &&
+    if (aligned && row_bytes % 16 == 0 && row_bytes > kSplitFromRowBytes && rows > 0 &&
         make_split_plan(rows, D, dt, p, rms))
         return true;
     // Ring path: at most kMaxElemsPerThread columns per thread (gamma and the two
@@ -1131,12 +1135,16 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
         const int threads = (int)std::min<int64_t>(kRowThreads, (nvec + 31) / 32 * 32);
         int nv = (int)((nvec + threads - 1) / threads);
         nv = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : 8;
-        // Rows per stage: about 16 KB of x (and as much dY) per stage.
+        // Ring bytes in proportion to the CTA's warps (12 KB a warp, 96 KB for 8), so
+        // that CTAs of short rows -- one to seven warps -- fit more per SM; a stage
+        // holds about a third of the ring (at most 16 KB of x and as much dY).
+        const int64_t budget = (int64_t)kRingBudget * (threads / 32) / kMaxWarps;
+        const int64_t stage_target = std::min<int64_t>(kStageTargetBytes, budget / 3);
         int r = 1;
-        while (r < max_r_for(nv) && (int64_t)(2 * r) * row_bytes <= kStageTargetBytes / 2) r *= 2;
+        while (r < max_r_for(nv) && (int64_t)(2 * r) * row_bytes <= stage_target / 2) r *= 2;
         const int64_t stage_bytes = 2 * (int64_t)r * row_bytes;
         const int stages =
-            (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, kRingBudget / stage_bytes));
+            (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, budget / stage_bytes));
         const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
         if ((int64_t)smem <= info.max_smem_optin) {
             const int per_sm = resident_ctas_per_sm(ring_kernel(dt, nv, r, rms), threads, smem);
@@ -1518,9 +1526,9 @@ extern "C" tb_status tb_layernorm_bwd_selftest_timeout(int64_t wait_limit_ns, vo
     if (!err) return TB_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The single-CTA ring (rows of 256 columns), then the cluster-split ring
-    // (rows of 8192 columns over two CTAs): every CTA of the cluster gives up at
-    // the same group and the cluster ends together.
+    // (rows of 16384 columns over four CTAs): every CTA of the cluster gives up
+    // at the same group and the cluster ends together.
     const tb_status a = run_withheld(4, 256, Path::kRing, wait_limit_ns, info, err, st);
     if (a != TB_OK) return a;
-    return run_withheld(4, 8192, Path::kSplit, wait_limit_ns, info, err, st);
+    return run_withheld(4, 16384, Path::kSplit, wait_limit_ns, info, err, st);
 }

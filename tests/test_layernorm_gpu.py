@@ -139,19 +139,20 @@ def test_workspace_too_small_is_rejected(tb, synth):
     assert ei.value.code == 5
 
 
-# Rows split over a thread-block cluster: cluster sizes 2..8 (16 columns per
-# thread), 32 columns per thread (D = 65,536), slices that leave threads idle
-# (4,104 / 8,200), row counts that leave clusters empty or ragged.
-# D -> CTAs per cluster the plan picks for 16-bit rows: the smallest of 2..8
-# giving slices of whole 16-byte vectors of at most 4,096 columns, else of at
-# most 8,192 (fp32 rows of 4,104 take two CTAs of 2,052 columns).
-SPLIT = {4104: 3, 5120: 2, 8192: 2, 10240: 4, 12288: 3, 16384: 4, 18432: 6, 20480: 5,
-         25600: 8, 65536: 8}
+# Rows longer than 16 KB are split over a thread-block cluster: cluster sizes
+# 2..8 (16 columns per thread), 32 columns per thread (D = 65,536), slices that
+# leave threads idle (4,104 fp32 / 8,200), row counts that leave clusters empty
+# or ragged.  16-bit rows up to 8,192 columns take the single-CTA ring instead.
+# D -> CTAs per cluster for 16-bit rows (fp32 in brackets where it differs): the
+# smallest of 2..8 giving slices of whole 16-byte vectors of at most 4,096
+# columns, else of at most 8,192.
+SPLIT = {4104: "ring [2]", 5120: "ring [2]", 8192: "ring [2]", 8200: 5, 10240: 4,
+         12288: 3, 16384: 4, 18432: 6, 20480: 5, 25600: 8, 65536: 8}
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
                          ids=["f32", "bf16", "f16"])
-@pytest.mark.parametrize("D", list(SPLIT), ids=[f"D{d}-cluster{c}" for d, c in SPLIT.items()])
+@pytest.mark.parametrize("D", list(SPLIT), ids=[f"D{d}" for d in SPLIT])
 def test_rows_split_over_a_cluster(tb, synth, D, dtype):
     for rows in (1, 5, 211):
         args = synth.layernorm_inputs(rows, D, dtype, seed=3 * D + rows, device="cuda")
