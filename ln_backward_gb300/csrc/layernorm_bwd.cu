@@ -52,6 +52,7 @@ namespace {
 
 constexpr int kRowThreads = 256;               // max threads of the row kernels
 constexpr int kMaxWarps = kRowThreads / 32;
+constexpr int kWideWarps = 16;                 // warps of the wide ring variant (512 threads)
 constexpr int kMaxStages = 4;
 constexpr int kMaxElemsPerThread = 32;
 constexpr int kRingBudget = 96 * 1024;         // bytes of ring per CTA we aim for
@@ -389,11 +390,15 @@ __device__ __forceinline__ void row_dx(const unsigned char* xr, const unsigned c
     }
 }
 
-// Sum of the kMaxWarps per-warp values at p, in a fixed order.
+// Sum of the W (8 or 16) per-warp values at p, in a fixed order.
+template <int W = kMaxWarps>
 __device__ __forceinline__ float cta_total(const float* p) {
+    static_assert(W == 8 || W == 16, "8 or 16 warps");
     const float4 a0 = *reinterpret_cast<const float4*>(p);
     const float4 a1 = *reinterpret_cast<const float4*>(p + 4);
-    return ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
+    const float t = ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
+    if constexpr (W == 8) return t;
+    else return t + cta_total<8>(p + 8);
 }
 
 // gamma of the thread's columns (zero past nvec); the partial sums start at zero.
@@ -445,8 +450,11 @@ __device__ __forceinline__ void store_partials(float* pg, float* pb,
 // Columns per thread NV*E up to 16 fit two CTAs per SM; 32 need the full budget.
 // kRms: RMSNorm backward -- no mean subtraction (mean is not read), no sum of
 // dxhat, no beta: dX = rs*(dxhat - xhat*mean(dxhat*xhat)), partial rows of D.
-template <class Fmt, int NV, int R, bool kRms>
-__global__ void __launch_bounds__(kRowThreads, (NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
+// W: warps the CTA may have -- 8, or 16 for the wide variant (up to 512 threads,
+// one CTA per SM, 16 columns a thread: rows of 4097..8192 16-bit columns, which
+// would otherwise need 32 columns a thread and leave one 8-warp CTA per SM).
+template <class Fmt, int NV, int R, bool kRms, int W = kMaxWarps>
+__global__ void __launch_bounds__(W * 32, (W > kMaxWarps || NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
 ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
                         const float* __restrict__ mean, const float* __restrict__ inv_std,
                         const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
@@ -458,14 +466,14 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
     extern __shared__ __align__(128) unsigned char smem[];
     // Per-warp row sums: value 2i is sum(dxhat) of row i, 2i+1 is sum(dxhat*xhat).
     // Slots of warps the CTA does not have stay zero.
-    __shared__ __align__(16) float red[2][2 * R][kMaxWarps];
+    __shared__ __align__(16) float red[2][2 * R][W];
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int nthreads = blockDim.x;
     const int nvec = D / E;
     const uint32_t row_bytes = (uint32_t)D * (uint32_t)sizeof(T);
     const uint32_t grp_bytes = (uint32_t)R * row_bytes;
-    for (int i = tid; i < 2 * 2 * R * kMaxWarps; i += nthreads) (&red[0][0][0])[i] = 0.f;
+    for (int i = tid; i < 2 * 2 * R * W; i += nthreads) (&red[0][0][0])[i] = 0.f;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* ring = smem + kBarRegion;   // stage s at ring + s * 2 * grp_bytes
 
@@ -577,8 +585,8 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             if (i < nr) {
-                const float a = cta_total(&red[buf][2 * i][0]);
-                const float b = cta_total(&red[buf][2 * i + 1][0]);
+                const float a = cta_total<W>(&red[buf][2 * i][0]);
+                const float b = cta_total<W>(&red[buf][2 * i + 1][0]);
                 const float mean_a = kRms ? 0.f : a * inv_D, mean_b = b * inv_D;
                 row_dx<Fmt, NV, kRms>(st + (size_t)i * row_bytes,
                                       st + grp_bytes + (size_t)i * row_bytes, dX + (first + i) * D,
@@ -954,7 +962,7 @@ cudaError_t launch_colsum(const float* ws, int G, int64_t W, int64_t D, float* d
 }
 
 // ------------------------------------------------------------------ launch planning
-enum class Path { kRing, kSplit, kPlain };
+enum class Path { kRing, kRingWide, kSplit, kPlain };
 
 struct LnPlan {
     Path path;
@@ -1004,6 +1012,13 @@ struct RingOps {
         }
     };
 };
+
+// The wide variant: 16-bit rows of 513..1024 vectors, two vectors a thread, one row a stage.
+template <class Fmt>
+const void* wide_kernel_for(bool rms) {
+    return rms ? reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, 2, 1, true, kWideWarps>)
+               : reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, 2, 1, false, kWideWarps>);
+}
 
 template <class Fmt>
 const void* ring_kernel_for(int nv, int r, bool rms) {
@@ -1129,6 +1144,31 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
     if (aligned && row_bytes % 16 == 0 && row_bytes > kSplitFromRowBytes && rows > 0 &&
         make_split_plan(rows, D, dt, p, rms))
         return true;
+    // Wide ring: 16-bit rows of 513..1024 vectors, two a thread on up to 512 threads.
+    if (aligned && row_bytes % 16 == 0 && es == 2 && nvec > 2 * kRowThreads &&
+        nvec <= 2 * 32 * kWideWarps && rows > 0) {
+        const int threads = (int)((nvec + 1) / 2 + 31) / 32 * 32;
+        const int64_t budget = (int64_t)kRingBudget * (threads / 32) / kMaxWarps;
+        const int64_t stage_bytes = 2 * row_bytes;
+        const int stages =
+            (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, budget / stage_bytes));
+        const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
+        const void* k = dt == TB_BF16 ? wide_kernel_for<BF16>(rms) : wide_kernel_for<F16>(rms);
+        const int per_sm = (int64_t)smem <= info.max_smem_optin
+                               ? resident_ctas_per_sm(k, threads, smem) : 0;
+        if (per_sm > 0) {
+            p->path = Path::kRingWide;
+            p->threads = threads;
+            p->nv = 2;
+            p->r = 1;
+            p->stages = stages;
+            p->smem = smem;
+            p->grid = (int)std::min<int64_t>((int64_t)info.sm_count * per_sm, rows);
+            p->parts = p->grid;
+            p->rows_per_cta = (rows + p->grid - 1) / p->grid;
+            return true;
+        }
+    }
     // Ring path: at most kMaxElemsPerThread columns per thread (gamma and the two
     // partial sums live in registers), i.e. D <= 8192.
     if (aligned && row_bytes % 16 == 0 && D <= (int64_t)kMaxElemsPerThread * kRowThreads) {
@@ -1219,7 +1259,20 @@ void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* me
     const T* dy = static_cast<const T*>(dY);
     const T* xx = static_cast<const T*>(x);
     T* dx = static_cast<T*>(dX);
-    if (p.path == Path::kSplit) {
+    if (p.path == Path::kRingWide) {
+        if constexpr (sizeof(T) == 2) {
+            if (rms)
+                launch_pdl(ln_bwd_rows_ring_kernel<Fmt, 2, 1, true, kWideWarps>, dim3((unsigned)p.grid),
+                           dim3((unsigned)p.threads), p.smem, st, dy, xx, mean, inv_std, gamma, dx, ws,
+                           rows, (int)D, p.stages, p.rows_per_cta, err, p.wait_limit_ns,
+                           p.withhold_copies);
+            else
+                launch_pdl(ln_bwd_rows_ring_kernel<Fmt, 2, 1, false, kWideWarps>, dim3((unsigned)p.grid),
+                           dim3((unsigned)p.threads), p.smem, st, dy, xx, mean, inv_std, gamma, dx, ws,
+                           rows, (int)D, p.stages, p.rows_per_cta, err, p.wait_limit_ns,
+                           p.withhold_copies);
+        }
+    } else if (p.path == Path::kSplit) {
         if (rms)
             with_split_variant<Fmt, SplitLaunchOps<true>::template Launch>(
                 p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
