@@ -777,6 +777,72 @@ def run_layernorm_sweep(args):
         raise RuntimeError("a kernel's bounded wait gave up during the sweep")
 
 
+HIDDEN_SWEEP_SHAPES = ("bf16:256,bf16:512,bf16:768,bf16:1024,bf16:1536,bf16:2048,bf16:4096,"
+                       "bf16:5120,bf16:6144,bf16:8192,bf16:10240,bf16:12288,bf16:16384,"
+                       "bf16:20480,bf16:32768,f32:768,f32:1024,f32:4096,f32:5120,f32:8192,"
+                       "f32:12288,f32:16384")
+
+
+def run_hidden_sweep(args):
+    """LayerNorm and RMSNorm backward over hidden sizes D, each with as many rows as
+    make one input tensor args.sweep_mb MB: the short-row ring, the 512-thread ring
+    and the cluster-split path in turn.  One JSON line per op, dtype and D; not part
+    of the benchmark contract.  With --sweep-reps 0 each shape is called once,
+    untimed (for profiler captures)."""
+    import torch
+    import ln_backward_gb300 as tb
+    from ln_backward_gb300 import synth
+    dev = torch.device("cuda")
+    peak, peak_kind = measured_peak()
+    dtypes = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+    def best_ms(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(3):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(reps):
+                fn()
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e) / reps)
+        return best
+
+    for item in args.sweep_shapes.split(","):
+        name, d = item.split(":")
+        dt, D = dtypes[name], int(d)
+        es = torch.empty((), dtype=dt).element_size()
+        rows = max(1, (args.sweep_mb << 20) // (D * es))
+        x, dy, mu, rs, g = synth.layernorm_inputs(rows, D, dt, 3, dev, eps=1e-5, dy_std=1e-2)
+        dX = torch.empty_like(x)
+        dg, db = torch.empty(D, device=dev), torch.empty(D, device=dev)
+        ws = torch.empty(tb.tb_layernorm_bwd_workspace_size(rows, D, dt), dtype=torch.uint8,
+                         device=dev)
+        wr = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(rows, D, dt), dtype=torch.uint8,
+                         device=dev)
+        ops = (("layernorm_bwd", lambda: tb.tb_layernorm_bwd(dy, x, mu, rs, g, dX, dg, db, ws),
+                layernorm_bytes(rows, D, es)),
+               ("rmsnorm_bwd", lambda: tb.tb_rmsnorm_bwd(dy, x, rs, g, dX, dg, wr),
+                rmsnorm_bytes(rows, D, es)))
+        for op, fn, nbytes in ops:
+            if args.sweep_reps == 0:
+                fn()
+                torch.cuda.synchronize()
+                continue
+            ms = best_ms(fn, args.sweep_reps)
+            gbs = nbytes / ms / 1e6
+            print(json.dumps({"sweep": "hidden", "op": op, "dtype": name, "D": D, "rows": rows,
+                              "us": round(ms * 1e3, 1), "GB_s": round(gbs, 1),
+                              "frac": round(gbs / peak, 3), "peak": f"{peak:.1f} ({peak_kind})"}))
+        del x, dy, dX, ws, wr
+        torch.cuda.empty_cache()
+    if tb.tb_device_error(reset=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during the sweep")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -792,10 +858,21 @@ def main(argv=None):
     ap.add_argument("--sweep-layernorm", action="store_true",
                     help="time the LayerNorm/RMSNorm backward over row counts and fit "
                          "bytes/BW + fixed cost (one JSON line per op and dtype)")
+    ap.add_argument("--sweep-hidden", action="store_true",
+                    help="time the LayerNorm/RMSNorm backward over hidden sizes (one JSON "
+                         "line per op, dtype and D)")
+    ap.add_argument("--sweep-shapes", default=HIDDEN_SWEEP_SHAPES,
+                    help="dtype:D list for --sweep-hidden (dtype bf16, f16 or f32)")
+    ap.add_argument("--sweep-mb", type=int, default=256,
+                    help="MB per input tensor for --sweep-hidden")
+    ap.add_argument("--sweep-reps", type=int, default=20,
+                    help="timed calls per repetition for --sweep-hidden (0: one untimed call)")
     args = ap.parse_args(argv)
     if args.warmup < 1:
         ap.error("--warmup must be >= 1 (timed numbers use the default of 3)")
-    if args.sweep_layernorm:
+    if args.sweep_hidden:
+        run_hidden_sweep(args)
+    elif args.sweep_layernorm:
         run_layernorm_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
