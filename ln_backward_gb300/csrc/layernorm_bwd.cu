@@ -53,6 +53,7 @@ namespace {
 constexpr int kRowThreads = 256;               // max threads of the row kernels
 constexpr int kMaxWarps = kRowThreads / 32;
 constexpr int kWideWarps = 16;                 // warps of the wide ring variant (512 threads)
+constexpr int kWidePairThreads = 320;          // wide CTAs up to this size run two per SM
 constexpr int kMaxStages = 4;
 constexpr int kMaxElemsPerThread = 32;
 constexpr int kRingBudget = 96 * 1024;         // bytes of ring per CTA we aim for
@@ -453,8 +454,11 @@ __device__ __forceinline__ void store_partials(float* pg, float* pb,
 // W: warps the CTA may have -- 8, or 16 for the wide variant (up to 512 threads,
 // one CTA per SM, 16 columns a thread: rows of 4097..8192 16-bit columns, which
 // would otherwise need 32 columns a thread and leave one 8-warp CTA per SM).
-template <class Fmt, int NV, int R, bool kRms, int W = kMaxWarps>
-__global__ void __launch_bounds__(W * 32, (W > kMaxWarps || NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
+// kBound < W*32: an instance for CTAs of at most kBound threads, two per SM (the
+// register budget that leaves): the wide variant on rows of up to 640 vectors.
+template <class Fmt, int NV, int R, bool kRms, int W = kMaxWarps, int kBound = W * 32>
+__global__ void __launch_bounds__(kBound, (kBound < W * 32) ? 2
+                                          : (W > kMaxWarps || NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
 ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
                         const float* __restrict__ mean, const float* __restrict__ inv_std,
                         const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
@@ -978,6 +982,7 @@ struct LnPlan {
     int stages;      // ring stages
     size_t smem;     // dynamic shared memory (ring and split paths)
     int cluster = 1; // CTAs a row is split over (split path), else 1
+    bool pair = false;  // wide ring path: the two-CTAs-per-SM instance
     int grid;        // CTAs of the row kernel
     int parts;       // partial rows in the workspace: grid / cluster
     int64_t rows_per_cta;   // rows per CTA (per cluster on the split path)
@@ -1019,9 +1024,15 @@ struct RingOps {
     };
 };
 
-// The wide variant: 16-bit rows of 513..1024 vectors, two vectors a thread, one row a stage.
+// The wide variant: 16-bit rows of 513..1024 vectors, two vectors a thread, one row a stage;
+// `pair`: the instance bounded to kWidePairThreads threads, two CTAs per SM.
 template <class Fmt>
-const void* wide_kernel_for(bool rms) {
+const void* wide_kernel_for(bool rms, bool pair) {
+    if (pair)
+        return rms ? reinterpret_cast<const void*>(
+                         &ln_bwd_rows_ring_kernel<Fmt, 2, 1, true, kWideWarps, kWidePairThreads>)
+                   : reinterpret_cast<const void*>(
+                         &ln_bwd_rows_ring_kernel<Fmt, 2, 1, false, kWideWarps, kWidePairThreads>);
     return rms ? reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, 2, 1, true, kWideWarps>)
                : reinterpret_cast<const void*>(&ln_bwd_rows_ring_kernel<Fmt, 2, 1, false, kWideWarps>);
 }
@@ -1159,11 +1170,21 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
         const int stages =
             (int)std::min<int64_t>(kMaxStages, std::max<int64_t>(2, budget / stage_bytes));
         const size_t smem = kBarRegion + (size_t)stages * (size_t)stage_bytes;
-        const void* k = dt == TB_BF16 ? wide_kernel_for<BF16>(rms) : wide_kernel_for<F16>(rms);
-        const int per_sm = (int64_t)smem <= info.max_smem_optin
-                               ? resident_ctas_per_sm(k, threads, smem) : 0;
+        auto kernel = [&](bool pair) {
+            return dt == TB_BF16 ? wide_kernel_for<BF16>(rms, pair) : wide_kernel_for<F16>(rms, pair);
+        };
+        bool pair = false;
+        int per_sm = 0;
+        if ((int64_t)smem <= info.max_smem_optin) {
+            if (threads <= kWidePairThreads) {
+                per_sm = resident_ctas_per_sm(kernel(true), threads, smem);
+                pair = per_sm >= 2;
+            }
+            if (!pair) per_sm = resident_ctas_per_sm(kernel(false), threads, smem);
+        }
         if (per_sm > 0) {
             p->path = Path::kRingWide;
+            p->pair = pair;
             p->threads = threads;
             p->nv = 2;
             p->r = 1;
@@ -1265,7 +1286,20 @@ void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* me
     const T* dy = static_cast<const T*>(dY);
     const T* xx = static_cast<const T*>(x);
     T* dx = static_cast<T*>(dX);
-    if (p.path == Path::kRingWide) {
+    if (p.path == Path::kRingWide && p.pair) {
+        if constexpr (sizeof(T) == 2) {
+            if (rms)
+                launch_pdl(ln_bwd_rows_ring_kernel<Fmt, 2, 1, true, kWideWarps, kWidePairThreads>,
+                           dim3((unsigned)p.grid), dim3((unsigned)p.threads), p.smem, st, dy, xx,
+                           mean, inv_std, gamma, dx, ws, rows, (int)D, p.stages, p.rows_per_cta, err,
+                           p.wait_limit_ns, p.withhold_copies);
+            else
+                launch_pdl(ln_bwd_rows_ring_kernel<Fmt, 2, 1, false, kWideWarps, kWidePairThreads>,
+                           dim3((unsigned)p.grid), dim3((unsigned)p.threads), p.smem, st, dy, xx,
+                           mean, inv_std, gamma, dx, ws, rows, (int)D, p.stages, p.rows_per_cta, err,
+                           p.wait_limit_ns, p.withhold_copies);
+        }
+    } else if (p.path == Path::kRingWide) {
         if constexpr (sizeof(T) == 2) {
             if (rms)
                 launch_pdl(ln_bwd_rows_ring_kernel<Fmt, 2, 1, true, kWideWarps>, dim3((unsigned)p.grid),
