@@ -861,7 +861,137 @@ ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename 
     cluster_sync_all();
 }
 
+// ------------------------------------------------------------------ row kernel (registers, plain loads)
+// Rows the bulk-copy rings cannot take -- unaligned buffers, or rows whose byte
+// length is not a multiple of 16 -- of up to K*256 columns.  Thread t of T owns
+// the columns t, t+T, ..., t+(K-1)T: it keeps gamma and its dgamma/dbeta partial
+// sums for them in registers across all rows of the CTA.  One thread prefetches
+// the rows ahead into L2 in blocks of about 16 KB (bulk prefetches of the
+// 16-byte-aligned span covering them: rounding an address inside a row down or
+// up to 16 bytes stays in the same 16-byte block, so in mapped memory), so each
+// row's loads find their lines in L2.  Up to 8 columns a
+// thread it also holds a row's x and dY values in registers between the two
+// phases; with more, phase 2 reads the row again (it was just read, so from L1),
+// which keeps the registers of 16 and 32 columns a thread low enough for two or
+// three CTAs per SM.  Element loads and stores are scalar but coalesced (a warp
+// touches consecutive elements).  One block reduction (double-buffered by row
+// parity) per row.
+template <class Fmt, int K, bool kRms>
+__global__ void __launch_bounds__(kRowThreads, K > 8 ? 2 : 1)
+ln_bwd_rows_reg_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
+                       const float* __restrict__ mean, const float* __restrict__ inv_std,
+                       const float* __restrict__ gamma, typename Fmt::T* __restrict__ dX,
+                       float* __restrict__ partials, int64_t rows, int D, int64_t rows_per_cta) {
+    __shared__ float red[2][2][kMaxWarps];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    pdl_wait();   // the previous kernel has completed (programmatic launch)
+    float g[K], acc_g[K], acc_b[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int j = tid + k * nthreads;
+        g[k] = j < D ? gamma[j] : 0.f;
+        acc_g[k] = 0.f;
+        acc_b[k] = 0.f;
+    }
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = r0 + rows_per_cta < rows ? r0 + rows_per_cta : rows;
+    const float inv_D = 1.0f / (float)D;
+    constexpr bool kHold = K <= 8;   // keep the row in registers between the phases
+    // Rows per prefetch block: about 16 KB of each tensor.
+    const int64_t row_bytes = (int64_t)D * (int64_t)sizeof(typename Fmt::T);
+    const int64_t pf_rows = row_bytes >= 16384 ? 1 : 16384 / row_bytes;
+    auto prefetch_rows = [&](int64_t a, int64_t b) {   // rows [a, b) of x and dY into L2
+        if (b > r1) b = r1;
+        if (a >= b) return;
+        const uintptr_t lo_x = reinterpret_cast<uintptr_t>(x + a * D) & ~(uintptr_t)15;
+        const uintptr_t hi_x = (reinterpret_cast<uintptr_t>(x + b * D) + 15) & ~(uintptr_t)15;
+        const uintptr_t lo_d = reinterpret_cast<uintptr_t>(dY + a * D) & ~(uintptr_t)15;
+        const uintptr_t hi_d = (reinterpret_cast<uintptr_t>(dY + b * D) + 15) & ~(uintptr_t)15;
+        bulk_prefetch_l2(reinterpret_cast<const void*>(lo_x), (uint32_t)(hi_x - lo_x));
+        bulk_prefetch_l2(reinterpret_cast<const void*>(lo_d), (uint32_t)(hi_d - lo_d));
+    };
+    if (tid == 0) {   // the first two blocks
+        prefetch_rows(r0, r0 + pf_rows);
+        prefetch_rows(r0 + pf_rows, r0 + 2 * pf_rows);
+    }
+    int buf = 0;
+    for (int64_t r = r0; r < r1; ++r, buf ^= 1) {
+        // entering a block: fetch the block after next
+        if (tid == 0 && (r - r0) % pf_rows == 0) prefetch_rows(r + 2 * pf_rows, r + 3 * pf_rows);
+        const float mu = kRms ? 0.f : mean[r], rs = inv_std[r];
+        const typename Fmt::T* xr = x + r * D;
+        const typename Fmt::T* dyr = dY + r * D;
+        float xv[kHold ? K : 1], dv[kHold ? K : 1];
+        float sa = 0.f, sb = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int j = tid + k * nthreads;
+            const float xk = j < D ? Fmt::to_f32(xr[j]) : 0.f;
+            const float dk = j < D ? Fmt::to_f32(dyr[j]) : 0.f;
+            if constexpr (kHold) {
+                xv[k] = xk;
+                dv[k] = dk;
+            }
+            const float xh = (xk - mu) * rs;
+            const float dxh = __fmul_rn(dk, g[k]);
+            sa += dxh;
+            sb = fmaf(dxh, xh, sb);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, o);
+            sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        }
+        if (lane == 0) {
+            red[buf][0][wid] = sa;
+            red[buf][1][wid] = sb;
+        }
+        __syncthreads();
+        float a = 0.f, b = 0.f;
+        for (int w = 0; w < nwarps; ++w) {
+            a += red[buf][0][w];
+            b += red[buf][1][w];
+        }
+        const float mean_a = kRms ? 0.f : a * inv_D, mean_b = b * inv_D;
+        const float c0 = -(rs * mean_a), c1 = -(rs * mean_b);
+        typename Fmt::T* dxr = dX + r * D;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int j = tid + k * nthreads;
+            if (j < D) {
+                float xk, dk;
+                if constexpr (kHold) {
+                    xk = xv[k];
+                    dk = dv[k];
+                } else {
+                    // a load of its own (last use), not merged with phase 1's
+                    xk = Fmt::to_f32(__ldlu(xr + j));
+                    dk = Fmt::to_f32(__ldlu(dyr + j));
+                }
+                const float xh = (xk - mu) * rs;
+                const float dxh = __fmul_rn(dk, g[k]);
+                dxr[j] = Fmt::from_f32(fmaf(dxh, rs, fmaf(xh, c1, c0)));
+                acc_g[k] = fmaf(dk, xh, acc_g[k]);
+                if (!kRms) acc_b[k] += dk;
+            }
+        }
+    }
+    pdl_trigger();
+    float* pg = partials + (size_t)blockIdx.x * (kRms ? 1 : 2) * D;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int j = tid + k * nthreads;
+        if (j < D) {
+            pg[j] = acc_g[k];
+            if (!kRms) pg[D + j] = acc_b[k];
+        }
+    }
+}
+
 // ------------------------------------------------------------------ row kernel (plain loads)
+// The last resort: unaligned rows longer than 8192 columns.  Two global passes
+// per row, partials kept in the workspace.
 template <class Fmt, bool kRms>
 __global__ void __launch_bounds__(kRowThreads)
 ln_bwd_rows_plain_kernel(const typename Fmt::T* __restrict__ dY, const typename Fmt::T* __restrict__ x,
@@ -1087,6 +1217,55 @@ const void* split_kernel(tb_dtype dt, int nv, int r, bool rms) {
     }
 }
 
+// Op<Fmt, K>::run(args...) for the register row kernel's instantiated K.
+template <class Fmt, template <class, int> class Op, class... Args>
+auto with_reg_variant(int k, Args&&... args) {
+    switch (k) {
+        case 1: return Op<Fmt, 1>::run(args...);
+        case 2: return Op<Fmt, 2>::run(args...);
+        case 4: return Op<Fmt, 4>::run(args...);
+        case 8: return Op<Fmt, 8>::run(args...);
+        case 16: return Op<Fmt, 16>::run(args...);
+        default: return Op<Fmt, 32>::run(args...);
+    }
+}
+
+template <bool kRms>
+struct RegOps {
+    template <class Fmt, int K>
+    struct Ptr {
+        static const void* run() {
+            return reinterpret_cast<const void*>(&ln_bwd_rows_reg_kernel<Fmt, K, kRms>);
+        }
+    };
+    template <class Fmt, int K>
+    struct Launch {
+        using T = typename Fmt::T;
+        static int run(const LnPlan& p, const T* dy, const T* x, const float* mean,
+                       const float* inv_std, const float* gamma, T* dx, float* ws, int64_t rows,
+                       int D, cudaStream_t st) {
+            launch_pdl(ln_bwd_rows_reg_kernel<Fmt, K, kRms>, dim3((unsigned)p.grid),
+                       dim3((unsigned)p.threads), 0, st, dy, x, mean, inv_std, gamma, dx, ws, rows,
+                       D, p.rows_per_cta);
+            return 0;
+        }
+    };
+};
+
+template <class Fmt>
+const void* reg_kernel_for(int k, bool rms) {
+    return rms ? with_reg_variant<Fmt, RegOps<true>::template Ptr>(k)
+               : with_reg_variant<Fmt, RegOps<false>::template Ptr>(k);
+}
+
+const void* reg_kernel(tb_dtype dt, int k, bool rms) {
+    switch (dt) {
+        case TB_F32: return reg_kernel_for<F32>(k, rms);
+        case TB_BF16: return reg_kernel_for<BF16>(k, rms);
+        default: return reg_kernel_for<F16>(k, rms);
+    }
+}
+
 template <class Fmt>
 const void* plain_kernel_for(bool rms) {
     return rms ? reinterpret_cast<const void*>(&ln_bwd_rows_plain_kernel<Fmt, true>)
@@ -1226,14 +1405,22 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
         }
     }
     if (p->path == Path::kPlain) {
-        const int per_sm = resident_ctas_per_sm(plain_kernel(dt, rms), kRowThreads, 0);
+        // Register rows (nv = columns a thread) up to 32 columns a thread, else the
+        // last-resort kernel (nv = 0).
+        const int threads = (int)std::min<int64_t>(kRowThreads, (D + 31) / 32 * 32);
+        const int64_t per_thread = (D + threads - 1) / threads;
+        int k = 0;
+        if (per_thread <= 32) k = per_thread <= 1 ? 1 : per_thread <= 2 ? 2 : per_thread <= 4 ? 4
+                                 : per_thread <= 8 ? 8 : per_thread <= 16 ? 16 : 32;
+        const int per_sm = resident_ctas_per_sm(k ? reg_kernel(dt, k, rms) : plain_kernel(dt, rms),
+                                                k ? threads : kRowThreads, 0);
         if (per_sm == 0) return false;
-        p->threads = kRowThreads;
-        p->nv = 0;
+        p->threads = k ? threads : kRowThreads;
+        p->nv = k;
         p->r = 0;
         p->stages = 0;
         p->smem = 0;
-        p->grid = info.sm_count * std::min(per_sm, 2);
+        p->grid = info.sm_count * (k ? per_sm : std::min(per_sm, 2));
     }
     p->grid = (int)std::min<int64_t>(p->grid, rows);
     p->parts = p->grid;
@@ -1326,6 +1513,13 @@ void launch_rows(const LnPlan& p, const void* dY, const void* x, const float* me
         else
             with_ring_variant<Fmt, RingLaunchOps<false>::template Launch>(
                 p.nv, p.r, p, dy, xx, mean, inv_std, gamma, dx, ws, rows, (int)D, err, st);
+    } else if (p.nv > 0) {
+        if (rms)
+            with_reg_variant<Fmt, RegOps<true>::template Launch>(p.nv, p, dy, xx, mean, inv_std,
+                                                                 gamma, dx, ws, rows, (int)D, st);
+        else
+            with_reg_variant<Fmt, RegOps<false>::template Launch>(p.nv, p, dy, xx, mean, inv_std,
+                                                                  gamma, dx, ws, rows, (int)D, st);
     } else if (rms) {
         launch_pdl(ln_bwd_rows_plain_kernel<Fmt, true>, dim3((unsigned)p.grid), dim3((unsigned)p.threads),
                    0, st, dy, xx, mean, inv_std, gamma, dx, ws, rows, D, p.rows_per_cta);

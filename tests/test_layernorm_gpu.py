@@ -111,6 +111,31 @@ def test_unaligned_buffers_take_plain_path(tb, synth, dtype):
     check(tb, x, dY, mean, rstd, gamma, *run(tb, x, dY, mean, rstd, gamma))
 
 
+# Rows the bulk-copy rings cannot take: byte lengths that are not a multiple of
+# 16 (odd D) or buffers one element off 16-byte alignment.  1..32 columns a thread
+# on the register row kernel (D up to 8,192), then the last-resort kernel (8,196).
+PLAIN_D = [5, 100, 1004, 2052, 4100, 6150, 8191, 8196]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
+                         ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", PLAIN_D)
+def test_plain_path_shapes(tb, synth, D, dtype):
+    for rows, shift in ((1, 0), (7, 1), (300, 0), (129, 1)):
+        x0, dY0, mean, rstd, gamma = synth.layernorm_inputs(rows, D, dtype, seed=5 * D + rows,
+                                                           device="cuda")
+        if shift:
+            bx = torch.empty(rows * D + shift, dtype=dtype, device="cuda")
+            by = torch.empty(rows * D + shift, dtype=dtype, device="cuda")
+            x = bx[shift:].view(rows, D)
+            dY = by[shift:].view(rows, D)
+            x.copy_(x0)
+            dY.copy_(dY0)
+        else:
+            x, dY = x0, dY0
+        check(tb, x, dY, mean, rstd, gamma, *run(tb, x, dY, mean, rstd, gamma))
+
+
 def test_zero_rows_write_zero_parameter_gradients(tb):
     D = 96
     x = torch.empty(0, D, device="cuda")

@@ -98,6 +98,23 @@ def test_feature_dim_sweep(tb, synth, D, dtype):
         check(*args, *run(tb, *args))
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("D", [100, 1004, 4100, 8191, 8196])
+def test_plain_path_shapes(tb, synth, D, dtype):
+    """Odd row lengths and buffers one element off alignment: the register row
+    kernel up to 8,192 columns, the last-resort kernel beyond."""
+    for rows, shift in ((7, 1), (300, 0)):
+        x0, dY0, rs, gamma = synth.rmsnorm_inputs(rows, D, dtype, seed=7 * D + rows, device="cuda")
+        if shift:
+            x = torch.empty(rows * D + shift, dtype=dtype, device="cuda")[shift:].view(rows, D)
+            dY = torch.empty(rows * D + shift, dtype=dtype, device="cuda")[shift:].view(rows, D)
+            x.copy_(x0)
+            dY.copy_(dY0)
+        else:
+            x, dY = x0, dY0
+        check(x, dY, rs, gamma, *run(tb, x, dY, rs, gamma))
+
+
 def test_zero_rows_write_zero_dgamma(tb):
     D = 64
     x = torch.empty(0, D, device="cuda")

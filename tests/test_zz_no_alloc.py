@@ -68,9 +68,9 @@ def _close(a, b):
     (16384, 4096, torch.bfloat16),   # partials fit with the usual grid: bitwise equal
     (4096, 8192, torch.float32),     # rows split over a two-CTA cluster
     (1024, 12288, torch.bfloat16),   # rows split over a three-CTA cluster: bitwise equal
-    (300, 1000, torch.float16),      # row length not a multiple of 16 bytes: plain-load path
+    (300, 1004, torch.float16),      # 2,008-byte rows, not a multiple of 16 bytes: plain-load path
     (512, 12300, torch.bfloat16),    # plain path; partials of 2 CTAs/SM exceed 16 MiB: fewer CTAs
-], ids=["16384x4096-bf16", "4096x8192-f32", "1024x12288-bf16", "300x1000-f16", "512x12300-bf16"])
+], ids=["16384x4096-bf16", "4096x8192-f32", "1024x12288-bf16", "300x1004-f16", "512x12300-bf16"])
 def test_matches_workspace_entry_point_twice(tb, synth, rows, D, dtype):
     args = synth.layernorm_inputs(rows, D, dtype, seed=rows + D, device="cuda", dy_std=1e-2)
     ref = _with_workspace(tb, *args)
