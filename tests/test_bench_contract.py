@@ -79,3 +79,28 @@ def test_gpu_arm_line_has_every_contract_key():
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+
+
+@pytest.mark.gpu
+def test_hidden_size_sweep_lines():
+    """bench.py --sweep-hidden: one JSON line per op and shape with a consistent
+    bandwidth figure; with --sweep-reps 0 it only calls each shape once."""
+    args = [sys.executable, os.path.join(ROOT, "bench.py"), "--sweep-hidden", "--sweep-shapes",
+            "bf16:1004,bf16:4096,f32:6144", "--sweep-mb", "16"]
+    p = subprocess.run(args + ["--sweep-reps", "2"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert p.returncode == 0, p.stdout + p.stderr
+    lines = [json.loads(ln) for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert [(d["op"], d["dtype"], d["D"]) for d in lines] == [
+        (op, dt, D) for dt, D in (("bf16", 1004), ("bf16", 4096), ("f32", 6144))
+        for op in ("layernorm_bwd", "rmsnorm_bwd")]
+    for d in lines:
+        es = 4 if d["dtype"] == "f32" else 2
+        assert d["rows"] == (16 << 20) // (d["D"] * es)
+        assert d["us"] > 0 and 0 < d["frac"] < 1.5
+        peak = float(d["peak"].split()[0])
+        assert abs(d["frac"] * peak - d["GB_s"]) <= 0.0006 * peak + 0.1   # frac has 3 decimals
+    p = subprocess.run(args + ["--sweep-reps", "0"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert p.returncode == 0, p.stdout + p.stderr
+    assert not [ln for ln in p.stdout.splitlines() if ln.startswith("{")]

@@ -102,6 +102,49 @@ def test_cuda_graph_capture_and_replay(tb, synth):
     assert tb.tb_device_error() == 0
 
 
+@pytest.mark.parametrize("D, dtype", [(1004, torch.bfloat16), (2048, torch.bfloat16),
+                                      (8192, torch.bfloat16), (16384, torch.bfloat16),
+                                      (12288, torch.float32)],
+                         ids=["fallback-bf16", "ring-bf16", "wide-ring-bf16", "split-bf16",
+                              "split-f32"])
+def test_norm_row_paths_replay_from_a_graph(tb, synth, D, dtype):
+    """LayerNorm and RMSNorm backward on each row path (the register fallback, the
+    ring, the 512-thread ring, the cluster-split kernel) captured in a CUDA graph,
+    replayed on new data, bitwise equal to eager calls."""
+    rows = 300
+    x, ldY, mu, rs, g = synth.layernorm_inputs(rows, D, dtype, seed=70 + D, device="cuda")
+    ldx, ldg, ldb, lws = _ln_bufs(tb, rows, D, dtype)
+    rdx = torch.empty_like(x)
+    rdg = torch.empty(D, device="cuda")
+    rws = torch.empty(tb.tb_rmsnorm_bwd_workspace_size(rows, D, dtype), dtype=torch.uint8,
+                      device="cuda")
+
+    def calls():
+        tb.tb_layernorm_bwd(ldY, x, mu, rs, g, ldx, ldg, ldb, lws)
+        tb.tb_rmsnorm_bwd(ldY, x, rs, g, rdx, rdg, rws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls()                      # warm-up outside capture (per-device queries are cached)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        calls()
+    x2, ldY2, mu2, rs2, _ = synth.layernorm_inputs(rows, D, dtype, seed=80 + D, device="cuda")
+    for dst, src in ((x, x2), (ldY, ldY2), (mu, mu2), (rs, rs2)):
+        dst.copy_(src)
+    graph.replay()
+    torch.cuda.synchronize()
+    got = [t.clone() for t in (ldx, ldg, ldb, rdx, rdg)]
+    calls()
+    torch.cuda.synchronize()
+    for a, b in zip(got, (ldx, ldg, ldb, rdx, rdg)):
+        assert torch.equal(a, b)
+    assert tb.tb_device_error() == 0
+
+
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 
 
