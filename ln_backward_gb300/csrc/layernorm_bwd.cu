@@ -9,20 +9,23 @@
 //
 // Design (GB300):
 //  * Kernel 1 (rows): persistent CTAs, each owning a contiguous block of rows.
-//    One elected thread streams the x and dY rows into a ring of shared-memory
-//    stages with 1-D bulk async copies (cp.async.bulk, completion counted on an
-//    mbarrier), several rows ahead, so HBM stays busy without holding the rows
-//    in registers.  It is launched as a programmatic dependent: its CTAs set up
-//    their barriers and prefetch their first stage into L2 while the previous
-//    kernel drains, and copy nothing before that kernel has completed.  Each
-//    thread owns a fixed set of 16-byte column vectors: it keeps gamma and its
-//    dgamma/dbeta partial sums for those columns in registers across all rows
-//    of the CTA.  Phase 1 reads the staged row and
-//    forms the two row sums (dxhat, dxhat*xhat) with a warp butterfly plus one
-//    shared-memory exchange and one barrier per row; phase 2 re-reads the
-//    staged row (shared memory, not HBM), writes dX and accumulates the column
-//    partials.  A stage is refilled one row later, once every thread is past
-//    it.  At the end each CTA stores its column partials to the workspace.
+//    One elected thread streams groups of x and dY rows into a ring of
+//    shared-memory stages with 1-D bulk async copies (cp.async.bulk, completion
+//    counted on an mbarrier), several groups ahead, so HBM stays busy without
+//    holding the rows in registers.  It is launched as a programmatic
+//    dependent: its CTAs set up their barriers and prefetch their first stage
+//    into L2 while the previous kernel drains, and copy nothing before that
+//    kernel has completed.  Each thread owns a fixed set of 16-byte column
+//    vectors: it keeps gamma and its dgamma/dbeta partial sums for those
+//    columns in registers across all rows of the CTA.  Phase 1 reads the staged
+//    rows and forms the two row sums (dxhat, dxhat*xhat) with a warp butterfly
+//    plus one shared-memory exchange and one barrier per group; phase 2
+//    re-reads the staged rows (shared memory, not HBM), writes dX and
+//    accumulates the column partials.  A stage is refilled one group later,
+//    once every thread is past it.  At the end each CTA stores its column
+//    partials to the workspace.  CTAs have 1..8 warps (ring bytes in proportion
+//    to the warps, so short rows fit several CTAs per SM), or up to 16 for
+//    16-bit rows of 4097..8192 columns (16 columns a thread instead of 32).
 //  * Kernel 1' (rows longer than 16 KB): the same ring, with each row
 //    split by columns over the 2..8 CTAs of a thread-block cluster.  Every CTA
 //    keeps the gamma and partials of its column slice in registers (so two CTAs
@@ -31,9 +34,11 @@
 //    slots, counted on an mbarrier there) -- one exchange per row group.
 //  * Kernel 2 (columns): adds the per-CTA (per-cluster) partials in a fixed
 //    order -> dgamma, dbeta, bitwise reproducible run to run.
-//  * Rows whose byte length is not a multiple of 16, unaligned buffers, or D
-//    that neither ring covers use a plain-load fallback of the same structure
-//    (two passes over the row, partials kept in the workspace).
+//  * Rows the bulk copies cannot take (unaligned buffers, byte lengths not a
+//    multiple of 16) run a register-row kernel of the same structure with
+//    scalar coalesced loads and an L2 prefetch of the rows ahead, up to 8192
+//    columns; beyond that a last-resort kernel makes two global passes per row
+//    and keeps the partials in the workspace.
 //
 // RMSNorm backward (tb_rmsnorm_bwd) runs the same kernels with kRms set:
 //   xhat = x * inv_rms, dX = inv_rms * (dxhat - xhat * mean_D(dxhat * xhat)),
@@ -452,10 +457,11 @@ __device__ __forceinline__ void store_partials(float* pg, float* pb,
 // kRms: RMSNorm backward -- no mean subtraction (mean is not read), no sum of
 // dxhat, no beta: dX = rs*(dxhat - xhat*mean(dxhat*xhat)), partial rows of D.
 // W: warps the CTA may have -- 8, or 16 for the wide variant (up to 512 threads,
-// one CTA per SM, 16 columns a thread: rows of 4097..8192 16-bit columns, which
-// would otherwise need 32 columns a thread and leave one 8-warp CTA per SM).
-// kBound < W*32: an instance for CTAs of at most kBound threads, two per SM (the
-// register budget that leaves): the wide variant on rows of up to 640 vectors.
+// 16 columns a thread: rows of 4097..8192 16-bit columns, which would otherwise
+// need 32 columns a thread and leave one 8-warp CTA per SM).  kBound < W*32: an
+// instance for CTAs of at most kBound threads, two per SM (the register budget
+// that leaves): the wide variant on rows of up to 640 vectors; otherwise a wide
+// CTA has its SM to itself.
 template <class Fmt, int NV, int R, bool kRms, int W = kMaxWarps, int kBound = W * 32>
 __global__ void __launch_bounds__(kBound, (kBound < W * 32) ? 2
                                           : (W > kMaxWarps || NV * Vec<Fmt>::kElems >= 32) ? 1 : 2)
