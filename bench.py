@@ -369,6 +369,12 @@ def run_ours(args):
     if e2e is not None:
         e2e_ms = reduce_over_ranks([e2e.pop("ms")], "max")[0]
         e2e["value"] = round(job_gbs(world, step_bytes, K, e2e_ms), 1)
+        # a pipelined step can be no shorter than its copies in both directions at
+        # once, nor than its kernels: the floor, and how close the loop came to it
+        floor_ms = max(e2e["link"]["both_ms"], total_ms / K)
+        e2e["step_ms"] = round(e2e_ms / K, 2)
+        e2e["floor_ms"] = round(floor_ms, 2)
+        e2e["frac_of_floor"] = round(floor_ms / (e2e_ms / K), 3)
 
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline and args.workload == "full":
@@ -546,8 +552,42 @@ def run_e2e(hp_path, K):
     torch.cuda.synchronize()
     barrier()
     plans[1].close()
+
+    # The host link on its own, with the same buffers: one step's uploads, its
+    # downloads, and both at once (best of three each, after the timed region).
+    def link_ms(up, down):
+        best = float("inf")
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(cur)
+            for q in (s_in, s_out):
+                q.wait_event(a)
+            if up:
+                with torch.cuda.stream(s_in):
+                    grads[0].copy_(h_grad, non_blocking=True)
+                    for d, h in zip(ins[0], h_ins):
+                        d.copy_(h, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s_out):
+                    h_copy.copy_(copies[0], non_blocking=True)
+                    for h, d in zip(h_outs, outs[0]):
+                        h.copy_(d, non_blocking=True)
+            cur.wait_stream(s_in)
+            cur.wait_stream(s_out)
+            b.record(cur)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    up_ms, down_ms, both_ms = link_ms(True, False), link_ms(False, True), link_ms(True, True)
     return {"ms": s.elapsed_time(e), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+            "link": {"h2d_ms": round(up_ms, 2), "d2h_ms": round(down_ms, 2),
+                     "both_ms": round(both_ms, 2),
+                     "h2d_GB_s": round(h2d / up_ms / 1e6, 1),
+                     "d2h_GB_s": round(d2h / down_ms / 1e6, 1),
+                     "both_GB_s": round((h2d + d2h) / both_ms / 1e6, 1)},
             "note": "algorithmic HBM bytes per step / step time of a pipelined loop whose every "
                     "step copies its gradients and activations up from pinned host memory and "
                     "its bf16 working copy and backward outputs back down (three streams, "

@@ -79,6 +79,15 @@ def test_gpu_arm_line_has_every_contract_key():
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    link = e2e["link"]
+    assert link["h2d_ms"] > 0 and link["d2h_ms"] > 0 and link["both_ms"] > 0
+    # (the rate was computed before the milliseconds were rounded to 0.01)
+    assert abs(link["h2d_GB_s"] - e2e["h2d_bytes_per_step"] / link["h2d_ms"] / 1e6) \
+        <= 0.005 * link["h2d_GB_s"] + 0.1
+    # the floor is the slower of the two-way copies and the device step; no loop beats it
+    assert e2e["floor_ms"] >= link["both_ms"] - 0.01 and e2e["floor_ms"] >= line["ms_per_step"] - 0.01
+    assert 0 < e2e["frac_of_floor"] <= 1.05
+    assert abs(e2e["frac_of_floor"] - e2e["floor_ms"] / e2e["step_ms"]) <= 2e-3
 
 
 @pytest.mark.gpu
