@@ -454,31 +454,38 @@ def time_extras(hp_path, reps, peak):
     return out
 
 
+E2E_BUFFER_SETS = 2
+
+
 def run_e2e(hp_path, K):
     """Same step through the public API, starting from pinned host buffers: every step
     copies its gradients and activations host->device, runs the kernels and copies the
     working copy and every backward output device->host.  Steps are pipelined the way a
     training loop would overlap them: the inputs of step k+1 go up on one stream while
     step k computes on a second and the results of step k-1 come down on a third, with
-    two device buffers for every copied tensor (two AdamW plans over the same
-    theta/m/v).  The timed region spans all K steps, copies included."""
+    E2E_BUFFER_SETS device buffers for every copied tensor (as many AdamW plans over the
+    same theta/m/v).  (Three sets, which let uploads start a step earlier, measured
+    slower than two on the same box: e2e 1,744 and 1,370 against 1,884 and 1,628 GB/s.)
+    The timed region spans all K steps, copies included."""
     import torch
     tb, st = hp_path.tb, hp_path.st
     k_t = len(st.sizes)
     pin = dict(pin_memory=True)
-    # device side: buffer set 0 is the step's own tensors, set 1 a second copy
-    grads = [st.grad, torch.empty_like(st.grad)]
-    copies = [st.copy, torch.empty_like(st.copy)]
+    nb = E2E_BUFFER_SETS
+    # device side: buffer set 0 is the step's own tensors, the others copies of them
+    grads = [st.grad] + [torch.empty_like(st.grad) for _ in range(nb - 1)]
+    copies = [st.copy] + [torch.empty_like(st.copy) for _ in range(nb - 1)]
     ins0 = [hp_path.P32, hp_path.dY32, hp_path.P16, hp_path.dY16, hp_path.x, hp_path.ldY,
             hp_path.mean, hp_path.rstd]
     outs0 = [hp_path.dX32, hp_path.dX16, hp_path.ldX, hp_path.dg, hp_path.db]
-    ins = [ins0, [torch.empty_like(t) for t in ins0]]
-    outs = [outs0, [torch.empty_like(t) for t in outs0]]
-    plans = [hp_path.plan, tb.tb_adamw_plan_create(
+    ins = [ins0] + [[torch.empty_like(t) for t in ins0] for _ in range(nb - 1)]
+    outs = [outs0] + [[torch.empty_like(t) for t in outs0] for _ in range(nb - 1)]
+    plans = [hp_path.plan] + [tb.tb_adamw_plan_create(
         *[[st.tensor(a, i) for i in range(k_t)] for a in ("theta", "m", "v")],
-        [grads[1].narrow(0, st.offsets[i], st.sizes[i]) for i in range(k_t)],
-        [copies[1].narrow(0, st.offsets[i], st.sizes[i]) for i in range(k_t)])]
-    ws = [hp_path.ws, torch.empty_like(hp_path.ws)]
+        [grads[b].narrow(0, st.offsets[i], st.sizes[i]) for i in range(k_t)],
+        [copies[b].narrow(0, st.offsets[i], st.sizes[i]) for i in range(k_t)])
+        for b in range(1, nb)]
+    ws = [hp_path.ws] + [torch.empty_like(hp_path.ws) for _ in range(nb - 1)]
     # host side
     h_grad = torch.empty_like(st.grad, device="cpu", **pin)
     h_grad.copy_(st.grad)
@@ -497,10 +504,10 @@ def run_e2e(hp_path, K):
         in_done, cmp_done, out_done = {}, {}, {}
 
         def upload(k):
-            b = k % 2
+            b = k % nb
             with torch.cuda.stream(s_in):
-                if k - 2 in cmp_done:        # step k-2 has finished reading set b
-                    s_in.wait_event(cmp_done[k - 2])
+                if k - nb in cmp_done:       # step k-nb has finished reading set b
+                    s_in.wait_event(cmp_done[k - nb])
                 grads[b].copy_(h_grad, non_blocking=True)
                 for d, h in zip(ins[b], h_ins):
                     d.copy_(h, non_blocking=True)
@@ -509,13 +516,13 @@ def run_e2e(hp_path, K):
 
         upload(0)
         for k in range(n_steps):
-            b = k % 2
+            b = k % nb
             if k + 1 < n_steps:
                 upload(k + 1)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(in_done[k])
-                if k - 2 in out_done:        # the results of step k-2 (set b) are down
-                    s_cmp.wait_event(out_done[k - 2])
+                if k - nb in out_done:       # the results of step k-nb (set b) are down
+                    s_cmp.wait_event(out_done[k - nb])
                 tb.tb_adamw_step(plans[b], t0 + k, inv_loss_scale=1.0 / LOSS_SCALE, **HP)
                 tb.tb_softmax_bwd(ins[b][1], ins[b][0], outs[b][0])
                 tb.tb_softmax_bwd(ins[b][3], ins[b][2], outs[b][1])
@@ -534,8 +541,8 @@ def run_e2e(hp_path, K):
 
     cur = torch.cuda.current_stream()
     torch.cuda.synchronize()
-    run(2, hp_path.t + 1)                    # warm-up: both buffer sets, all streams
-    hp_path.t += 2
+    run(nb, hp_path.t + 1)                   # warm-up: every buffer set, all streams
+    hp_path.t += nb
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -551,7 +558,8 @@ def run_e2e(hp_path, K):
     e.record(cur)
     torch.cuda.synchronize()
     barrier()
-    plans[1].close()
+    for pl in plans[1:]:
+        pl.close()
 
     # The host link on its own, with the same buffers: one step's uploads, its
     # downloads, and both at once (best of three each, after the timed region).
@@ -591,7 +599,7 @@ def run_e2e(hp_path, K):
             "note": "algorithmic HBM bytes per step / step time of a pipelined loop whose every "
                     "step copies its gradients and activations up from pinned host memory and "
                     "its bf16 working copy and backward outputs back down (three streams, "
-                    "double-buffered device tensors)"}
+                    f"{nb} device buffer sets)"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
