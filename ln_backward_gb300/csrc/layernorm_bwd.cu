@@ -1387,11 +1387,18 @@ bool make_plan(int64_t rows, int64_t D, tb_dtype dt, bool aligned, const DeviceI
         const int threads = (int)std::min<int64_t>(kRowThreads, (nvec + 31) / 32 * 32);
         int nv = (int)((nvec + threads - 1) / threads);
         nv = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : 8;
-        // Ring bytes in proportion to the CTA's warps (12 KB a warp, 96 KB for 8), so
-        // that CTAs of short rows -- one to seven warps -- fit more per SM; a stage
-        // holds about a third of the ring (at most 16 KB of x and as much dY).
-        const int64_t budget = (int64_t)kRingBudget * (threads / 32) / kMaxWarps;
-        const int64_t stage_target = std::min<int64_t>(kStageTargetBytes, budget / 3);
+        // Ring bytes in proportion to the CTA's warps, so that CTAs of short rows -- one
+        // to seven warps -- fit more per SM: 12 KB a warp in three stages for 16-bit
+        // LayerNorm rows, 24 KB for 16-bit RMSNorm rows (fewer, larger groups), 8 KB in
+        // two stages for fp32 rows -- each the best measured of 8..24 KB a warp and 2..4
+        // stages at D = 512..1024.  A stage holds at most 16 KB of x and as much dY; eight
+        // warps get 96 KB in every case.
+        const bool short_row = threads < kRowThreads;
+        const int64_t per_warp = !short_row ? kRingBudget / kMaxWarps
+                                 : es == 4 ? 8 * 1024 : rms ? 24 * 1024 : 12 * 1024;
+        const int nst = short_row && es == 4 ? 2 : 3;
+        const int64_t budget = std::min<int64_t>(kRingBudget, per_warp * (threads / 32));
+        const int64_t stage_target = std::min<int64_t>(kStageTargetBytes, budget / nst);
         int r = 1;
         while (r < max_r_for(nv) && (int64_t)(2 * r) * row_bytes <= stage_target / 2) r *= 2;
         const int64_t stage_bytes = 2 * (int64_t)r * row_bytes;
