@@ -57,6 +57,42 @@ def test_concurrent_streams_match_serial(tb, synth):
     assert tb.tb_device_error() == 0
 
 
+def test_concurrent_cluster_split_calls_match_serial(tb, synth):
+    """Two cluster-split LayerNorm calls (16,384 bf16 columns: four-CTA clusters) and
+    an RMSNorm call on split fp32 rows, each on its own stream and overlapping on the
+    GPU: the clusters of different calls share the SMs, and every result is bitwise
+    equal to the serial call's."""
+    D, rows = 16384, 1024
+    a = synth.layernorm_inputs(rows, D, torch.bfloat16, seed=90, device="cuda", dy_std=1e-2)
+    b = synth.layernorm_inputs(rows, D, torch.bfloat16, seed=91, device="cuda", dy_std=1e-2)
+    rx, rdY, rinv, rg = synth.rmsnorm_inputs(rows, 12288, torch.float32, seed=92, device="cuda")
+    rws_size = tb.tb_rmsnorm_bwd_workspace_size(rows, 12288, torch.float32)
+
+    def rms_bufs():
+        return (torch.empty_like(rx), torch.empty(12288, device="cuda"),
+                torch.empty(rws_size, dtype=torch.uint8, device="cuda"))
+
+    ref_a, ref_b = _ln_bufs(tb, rows, D, torch.bfloat16), _ln_bufs(tb, rows, D, torch.bfloat16)
+    ref_r = rms_bufs()
+    tb.tb_layernorm_bwd(a[1], a[0], a[2], a[3], a[4], *ref_a)
+    tb.tb_layernorm_bwd(b[1], b[0], b[2], b[3], b[4], *ref_b)
+    tb.tb_rmsnorm_bwd(rdY, rx, rinv, rg, *ref_r)
+    torch.cuda.synchronize()
+    out_a, out_b = _ln_bufs(tb, rows, D, torch.bfloat16), _ln_bufs(tb, rows, D, torch.bfloat16)
+    out_r = rms_bufs()
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        tb.tb_layernorm_bwd(a[1], a[0], a[2], a[3], a[4], *out_a, stream=streams[0])
+        tb.tb_layernorm_bwd(b[1], b[0], b[2], b[3], b[4], *out_b, stream=streams[1])
+        tb.tb_rmsnorm_bwd(rdY, rx, rinv, rg, *out_r, stream=streams[2])
+    torch.cuda.synchronize()
+    for got, want in ((out_a, ref_a), (out_b, ref_b), (out_r, ref_r)):
+        for u, w in zip(got[:-1], want[:-1]):     # outputs, not the workspaces
+            assert torch.equal(u, w)
+    assert tb.tb_device_error() == 0
+
+
 def test_cuda_graph_capture_and_replay(tb, synth):
     rows_sm, rows_ln, D = 4096, 2048, 4096
     P, dY = synth.softmax_inputs(rows_sm, 1024, torch.float32, seed=43, device="cuda")
