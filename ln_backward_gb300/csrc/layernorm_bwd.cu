@@ -48,6 +48,7 @@
 // the CTA sets the device error word, waits (bounded) for the copies it issued
 // and returns.
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "tb_common.cuh"
@@ -323,14 +324,35 @@ __device__ __forceinline__ void stg_pairs<F16>(void* p, const float2 (&f)[4]) {
     st_stream_u4(p, make_uint4(w[0], w[1], w[2], w[3]));
 }
 
+// (x - mu) for the two 16-bit values packed in w, each widened inside the
+// subtraction (sub.f32.bf16 / sub.f32.f16, mixed-precision forms of sm_100-class
+// targets): the same values as widening first, one instruction fewer per element.
+template <class Fmt> __device__ __forceinline__ float2 sub_mu_pair(uint32_t w, float mu);
+template <> __device__ __forceinline__ float2 sub_mu_pair<BF16>(uint32_t w, float mu) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(w), "f"(mu));
+    return make_float2(lo, hi);
+}
+template <> __device__ __forceinline__ float2 sub_mu_pair<F16>(uint32_t w, float mu) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "sub.rn.f32.f16 %0, l, %3;\n\tsub.rn.f32.f16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(w), "f"(mu));
+    return make_float2(lo, hi);
+}
+
 // ------------------------------------------------------------------ per-row math (both ring kernels)
 // A thread owns the 16-byte column vectors vi = tid + k*nthreads (k < NV, vi <
 // nvec) of the columns a CTA covers; g holds gamma for them, acc_g / acc_b the
 // CTA's dgamma / dbeta partial sums.  xr and dyr point at the staged row (the
 // CTA's columns of it) in shared memory.
 
+// kMix (16-bit LayerNorm rows): x - mean by sub_mu_pair, from the raw staged words.
+
 // Phase 1: this thread's shares of sum(dxhat) (sa) and sum(dxhat*xhat) (sb).
-template <class Fmt, int NV, bool kRms>
+template <class Fmt, int NV, bool kRms, bool kMix = false>
 __device__ __forceinline__ void row_shares(const unsigned char* xr, const unsigned char* dyr,
                                            const float2 (&g)[NV][Pairs<Fmt>::kN], float mu,
                                            float rs, int tid, int nthreads, int nvec, float& sa,
@@ -341,7 +363,21 @@ __device__ __forceinline__ void row_shares(const unsigned char* xr, const unsign
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         const int vi = tid + k * nthreads;
-        if (vi < nvec) {
+        if constexpr (kMix) {
+            if (vi < nvec) {
+                const uint4 u = *reinterpret_cast<const uint4*>(xr + (size_t)vi * 16);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                float2 dy[NP];
+                lds_pairs<Fmt>(dyr + (size_t)vi * 16, dy);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const float2 xh = __fmul2_rn(sub_mu_pair<Fmt>(w[q], mu), rs2);
+                    const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
+                    sa2 = __fadd2_rn(sa2, dxh);
+                    sb2 = __ffma2_rn(dxh, xh, sb2);
+                }
+            }
+        } else if (vi < nvec) {
             float2 xv[NP], dy[NP];
             lds_pairs<Fmt>(xr + (size_t)vi * 16, xv);
             lds_pairs<Fmt>(dyr + (size_t)vi * 16, dy);
@@ -363,7 +399,7 @@ __device__ __forceinline__ void row_shares(const unsigned char* xr, const unsign
 // and the column partials, from the row means mean_a = mean(dxhat) and
 // mean_b = mean(dxhat*xhat):
 //   dX = rs*dxhat - rs*mean_a - rs*mean_b*xhat  (two packed FMAs per pair)
-template <class Fmt, int NV, bool kRms>
+template <class Fmt, int NV, bool kRms, bool kMix = false>
 __device__ __forceinline__ void row_dx(const unsigned char* xr, const unsigned char* dyr,
                                        typename Fmt::T* dxr, const float2 (&g)[NV][Pairs<Fmt>::kN],
                                        float2 (&acc_g)[NV][Pairs<Fmt>::kN],
@@ -378,7 +414,23 @@ __device__ __forceinline__ void row_dx(const unsigned char* xr, const unsigned c
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
         const int vi = tid + k * nthreads;
-        if (vi < nvec) {
+        if constexpr (kMix) {
+            if (vi < nvec) {
+                const uint4 u = *reinterpret_cast<const uint4*>(xr + (size_t)vi * 16);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                float2 dy[NP], out[NP];
+                lds_pairs<Fmt>(dyr + (size_t)vi * 16, dy);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const float2 xh = __fmul2_rn(sub_mu_pair<Fmt>(w[q], mu), rs2);
+                    const float2 dxh = __fmul2_rn(dy[q], g[k][q]);
+                    out[q] = __ffma2_rn(dxh, rs2, __ffma2_rn(xh, nc1, nc0));
+                    acc_g[k][q] = __ffma2_rn(dy[q], xh, acc_g[k][q]);
+                    acc_b[k][q] = __fadd2_rn(acc_b[k][q], dy[q]);
+                }
+                stg_pairs<Fmt>(dxr + (size_t)vi * E, out);
+            }
+        } else if (vi < nvec) {
             float2 xv[NP], dy[NP], out[NP];
             lds_pairs<Fmt>(xr + (size_t)vi * 16, xv);
             lds_pairs<Fmt>(dyr + (size_t)vi * 16, dy);
@@ -473,6 +525,10 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
                         int withhold_copies) {
     using T = typename Fmt::T;
     constexpr int E = Vec<Fmt>::kElems;
+    // x - mean by mixed-precision subtraction: fp16 rows, and bf16 rows on 16 warps
+    // (on the 8-warp bf16 instances it measured up to 1% slower)
+    constexpr bool kMix = !kRms && (std::is_same<Fmt, F16>::value ||
+                                    (std::is_same<Fmt, BF16>::value && W > kMaxWarps));
     extern __shared__ __align__(128) unsigned char smem[];
     // Per-warp row sums: value 2i is sum(dxhat) of row i, 2i+1 is sum(dxhat*xhat).
     // Slots of warps the CTA does not have stay zero.
@@ -570,7 +626,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
             sa[i] = 0.f;
             sb[i] = 0.f;
             if (ok && i < nr)
-                row_shares<Fmt, NV, kRms>(st + (size_t)i * row_bytes,
+                row_shares<Fmt, NV, kRms, kMix>(st + (size_t)i * row_bytes,
                                           st + grp_bytes + (size_t)i * row_bytes, g, mu[i], rs[i],
                                           tid, nthreads, nvec, sa[i], sb[i]);
         }
@@ -602,7 +658,7 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
                 const float a = cta_total<W>(&red[buf][2 * i][0]);
                 const float b = cta_total<W>(&red[buf][2 * i + 1][0]);
                 const float mean_a = kRms ? 0.f : a * inv_D, mean_b = b * inv_D;
-                row_dx<Fmt, NV, kRms>(st + (size_t)i * row_bytes,
+                row_dx<Fmt, NV, kRms, kMix>(st + (size_t)i * row_bytes,
                                       st + grp_bytes + (size_t)i * row_bytes, dX + (first + i) * D,
                                       g, acc_g, acc_b, mu[i], rs[i], mean_a, mean_b, tid, nthreads,
                                       nvec);
@@ -682,6 +738,7 @@ ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename 
     using T = typename Fmt::T;
     constexpr int E = Vec<Fmt>::kElems;
     constexpr int kWords = 2 * R + 1;   // shares: 2R row sums, then the failure flag
+    constexpr bool kMix = !kRms && sizeof(T) == 2;   // x - mean by mixed-precision subtraction
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(16) float red[2][2 * R][kMaxWarps];
     __shared__ float xs[2][kMaxCluster][kWords];
@@ -790,7 +847,7 @@ ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename 
             sums[2 * i] = 0.f;
             sums[2 * i + 1] = 0.f;
             if (ok && i < nr)
-                row_shares<Fmt, NV, kRms>(st + (size_t)i * slice_bytes,
+                row_shares<Fmt, NV, kRms, kMix>(st + (size_t)i * slice_bytes,
                                           st + half_bytes + (size_t)i * slice_bytes, g, mu[i],
                                           rs[i], tid, nthreads, nvec, sums[2 * i], sums[2 * i + 1]);
         }
@@ -832,7 +889,7 @@ ln_bwd_rows_split_kernel(const typename Fmt::T* __restrict__ dY, const typename 
         for (int i = 0; i < R; ++i) {
             if (i < nr) {
                 const float mean_a = kRms ? 0.f : rsum[2 * i] * inv_D, mean_b = rsum[2 * i + 1] * inv_D;
-                row_dx<Fmt, NV, kRms>(st + (size_t)i * slice_bytes,
+                row_dx<Fmt, NV, kRms, kMix>(st + (size_t)i * slice_bytes,
                                       st + half_bytes + (size_t)i * slice_bytes,
                                       dX + (first + i) * D + col0, g, acc_g, acc_b, mu[i], rs[i],
                                       mean_a, mean_b, tid, nthreads, nvec);
