@@ -525,10 +525,12 @@ ln_bwd_rows_ring_kernel(const typename Fmt::T* __restrict__ dY, const typename F
                         int withhold_copies) {
     using T = typename Fmt::T;
     constexpr int E = Vec<Fmt>::kElems;
-    // x - mean by mixed-precision subtraction: fp16 rows, and bf16 rows on 16 warps
-    // (on the 8-warp bf16 instances it measured up to 1% slower)
+    // x - mean by mixed-precision subtraction: fp16 rows, and bf16 rows on the
+    // 16-warp instance that has its SM to itself (on the 8-warp bf16 instances it
+    // measured up to 1% slower, on the two-per-SM wide instance 3% slower)
     constexpr bool kMix = !kRms && (std::is_same<Fmt, F16>::value ||
-                                    (std::is_same<Fmt, BF16>::value && W > kMaxWarps));
+                                    (std::is_same<Fmt, BF16>::value && W > kMaxWarps &&
+                                     kBound == W * 32));
     extern __shared__ __align__(128) unsigned char smem[];
     // Per-warp row sums: value 2i is sum(dxhat) of row i, 2i+1 is sum(dxhat*xhat).
     // Slots of warps the CTA does not have stay zero.
