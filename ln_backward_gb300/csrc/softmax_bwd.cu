@@ -12,6 +12,8 @@
 //
 // Paths, chosen on the host:
 //   group : rows of <= 256 vectors (1024 fp32 / 2048 16-bit), G lanes per row
+//   pairs : causal 16-bit rows of 65..128 vectors (520..1024 columns) whose causal
+//           block fits in the rows: rows q and period-1-q of a block on one warp
 //   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
 // The group and CTA paths launch one CTA per row group when a CTA carries enough
@@ -76,26 +78,46 @@ template <> __device__ __forceinline__ uint32_t narrow2<F16>(float2 r) {
 // Mixed-precision forms of sm_100-class targets: a 16-bit element of a packed word
 // used directly as an operand, widened exactly inside the instruction, so the
 // results equal those of widening first.  half: 0 the low element, 1 the high one.
-__device__ __forceinline__ float fma_bf16(uint32_t a, uint32_t b, int half, float c) {
+#define TB_FMA_MIX(TY)                                                                          \
+    if (half)                                                                                   \
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t" \
+            "fma.rn.f32." TY " %0, a1, b1, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));         \
+    else                                                                                        \
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t" \
+            "fma.rn.f32." TY " %0, a0, b0, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+#define TB_SUB_MIX(TY)                                                                          \
+    if (half)                                                                                   \
+        asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %1;\n\tsub.rn.f32." TY " %0, a1, %2;\n\t}" \
+            : "=f"(d) : "r"(a), "f"(c));                                                        \
+    else                                                                                        \
+        asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %1;\n\tsub.rn.f32." TY " %0, a0, %2;\n\t}" \
+            : "=f"(d) : "r"(a), "f"(c));
+
+// a*b + c and a - c for 16-bit a, b taken from a packed word
+template <class Fmt> __device__ __forceinline__ float fma_mix(uint32_t a, uint32_t b, int half, float c);
+template <class Fmt> __device__ __forceinline__ float sub_mix(uint32_t a, int half, float c);
+template <> __device__ __forceinline__ float fma_mix<BF16>(uint32_t a, uint32_t b, int half, float c) {
     float d;
-    if (half)
-        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, a1, b1, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
-    else
-        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-            "fma.rn.f32.bf16 %0, a0, b0, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    TB_FMA_MIX("bf16")
     return d;
 }
-__device__ __forceinline__ float sub_bf16(uint32_t a, int half, float c) {
+template <> __device__ __forceinline__ float fma_mix<F16>(uint32_t a, uint32_t b, int half, float c) {
     float d;
-    if (half)
-        asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %1;\n\tsub.rn.f32.bf16 %0, a1, %2;\n\t}"
-            : "=f"(d) : "r"(a), "f"(c));
-    else
-        asm("{\n\t.reg .b16 a0, a1;\n\tmov.b32 {a0, a1}, %1;\n\tsub.rn.f32.bf16 %0, a0, %2;\n\t}"
-            : "=f"(d) : "r"(a), "f"(c));
+    TB_FMA_MIX("f16")
     return d;
 }
+template <> __device__ __forceinline__ float sub_mix<BF16>(uint32_t a, int half, float c) {
+    float d;
+    TB_SUB_MIX("bf16")
+    return d;
+}
+template <> __device__ __forceinline__ float sub_mix<F16>(uint32_t a, int half, float c) {
+    float d;
+    TB_SUB_MIX("f16")
+    return d;
+}
+#undef TB_FMA_MIX
+#undef TB_SUB_MIX
 
 // ------------------------------------------------------------------ group path
 // G lanes per row (G divides 32), VPL vectors per lane; 256 threads per CTA.
@@ -168,7 +190,7 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
                 const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
                 const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
-                for (int e = 0; e < E; ++e) dot = fma_bf16(pw[e / 2], dw[e / 2], e & 1, dot);
+                for (int e = 0; e < E; ++e) dot = fma_mix<Fmt>(pw[e / 2], dw[e / 2], e & 1, dot);
             }
         } else {
 #pragma unroll
@@ -201,7 +223,7 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
                         const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
                         for (int e = 0; e < E; ++e)
-                            out[e] = vec_elem<Fmt>(p[k], e) * sub_bf16(dw[e / 2], e & 1, dot);
+                            out[e] = vec_elem<Fmt>(p[k], e) * sub_mix<Fmt>(dw[e / 2], e & 1, dot);
                     } else {
 #pragma unroll
                         for (int e = 0; e < E; ++e)
@@ -211,6 +233,135 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
                 }
             } else if (live && vi < nv) {
                 __stcs(dX + off + vi, make_uint4(0u, 0u, 0u, 0u));   // masked: dX = +0
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ folded causal pairs
+// 16-bit causal rows of 65..128 vectors.  Inside one causal block of `period` rows,
+// row q opens min(cols, q + 1 + offset) columns and row period-1-q opens
+// min(cols, period - q + offset): the two together open about period + 1 + 2 offset
+// columns wherever q lies.  A warp takes such a pair, so every warp keeps about the
+// same number of loads in flight; with one row per warp, the warps on the short rows
+// of a block issue a load or two each and wait.  Lane l holds vectors l, l + 32, ...
+// of the first row in its first slots and the same vectors of the second row in the
+// slots after them: each row is summed in the order of the one-row-per-warp kernel
+// (and of the dense kernel, whose extra terms are exact zeros), so the results are
+// the same bit for bit.  The masked vectors of both rows are written as +0 right after
+// the loads are issued, while they are in flight (here that measured faster than
+// writing them after the dot products; in the one-row kernel it measured slower).
+// An odd period leaves the middle row without a partner; rows past `rows` in a last,
+// partial block are skipped.  VPL >= ceil(na / 32) + ceil(nb / 32) for every pair
+// (checked on the host); a larger pair would lose vectors, never touch other memory.
+// kEvenOdd: a lane sums even and odd elements apart and adds the two at the end, the
+// order of the one-row kernel's packed pairs (fp16 rows); otherwise one running sum.
+template <class Fmt, int VPL, bool kEvenOdd>
+__global__ void __launch_bounds__(256, 3)
+softmax_bwd_causal_pair_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
+                               uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
+                               int64_t offset, int64_t npairs) {
+    constexpr int E = Vec<Fmt>::kElems;
+    static_assert(E == 8, "16-bit rows only");
+    pdl_wait();      // the previous kernel has completed (programmatic launch)
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t per_block = (period + 1) / 2;
+    const int64_t cols = (int64_t)nv * E;
+    for (int64_t pi = warp; pi < npairs; pi += nwarps) {
+        const int64_t blk = pi / per_block;
+        const int64_t q = pi - blk * per_block;
+        const int64_t ra = blk * period + q;
+        const int64_t rb = blk * period + (period - 1 - q);
+        const bool live_a = ra < rows;
+        const bool live_b = rb != ra && rb < rows;
+        const int64_t ca = q + 1 + offset, cb = period - q + offset;
+        const int na = live_a ? (int)(((ca < cols ? ca : cols) + E - 1) / E) : 0;
+        const int nb = live_b ? (int)(((cb < cols ? cb : cols) + E - 1) / E) : 0;
+        const int ka = (na + 31) >> 5;                  // slots of row a (warp-uniform)
+        const int64_t offa = ra * (int64_t)nv;
+        const int64_t offb = rb * (int64_t)nv;
+        uint4 p[VPL], d[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const bool in_a = k < ka;
+            const int v = lane + 32 * (in_a ? k : k - ka);
+            if (v < (in_a ? na : nb)) {
+                const int64_t o = (in_a ? offa : offb) + v;
+                p[k] = __ldcs(P + o);
+                d[k] = __ldcs(dY + o);
+            } else {
+                p[k] = make_uint4(0u, 0u, 0u, 0u);
+                d[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        // masked vectors, row a's [na, nv) then row b's [nb, nv), written as +0 while
+        // the loads are in flight (they depend on none of them)
+        {
+            const int ma = live_a ? nv - na : 0;
+            const int mb = live_b ? nv - nb : 0;
+            uint4* const za = live_a ? dX + offa + na : dX;
+            uint4* const zb = live_b ? dX + offb + nb - ma : dX;   // index j >= ma: zb + j
+#pragma unroll 2
+            for (int j = lane; j < ma + mb; j += 32)
+                __stcs((j < ma ? za : zb) + j, make_uint4(0u, 0u, 0u, 0u));
+        }
+        float da = 0.f, db = 0.f;
+        // the mixed-precision forms: 16-bit operands, fp32 sums (the packed pairs'
+        // order is two such sums, even and odd elements, with the same values as
+        // packed fp32 math on the widened elements)
+        if constexpr (kEvenOdd) {
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const bool in_a = k < ka;
+                float s0 = in_a ? a0 : b0, s1 = in_a ? a1 : b1;
+                const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
+                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    s0 = fma_mix<Fmt>(pw[w], dw[w], 0, s0);
+                    s1 = fma_mix<Fmt>(pw[w], dw[w], 1, s1);
+                }
+                if (in_a) { a0 = s0; a1 = s1; } else { b0 = s0; b1 = s1; }
+            }
+            da = a0 + a1;
+            db = b0 + b1;
+        } else {
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const bool in_a = k < ka;
+                float acc = in_a ? da : db;
+                const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
+                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc = fma_mix<Fmt>(pw[e / 2], dw[e / 2], e & 1, acc);
+                if (in_a) da = acc; else db = acc;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            da += __shfl_xor_sync(0xffffffffu, da, o);
+            db += __shfl_xor_sync(0xffffffffu, db, o);
+        }
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const bool in_a = k < ka;
+            const int v = lane + 32 * (in_a ? k : k - ka);
+            if (v < (in_a ? na : nb)) {
+                const float dot = in_a ? da : db;
+                const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
+                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float2 pf = widen_a<Fmt>(pw[w]);
+                    o4[w] = narrow2<Fmt>(make_float2(pf.x * sub_mix<Fmt>(dw[w], 0, dot),
+                                                     pf.y * sub_mix<Fmt>(dw[w], 1, dot)));
+                }
+                __stcs(dX + (in_a ? offa : offb) + v, make_uint4(o4[0], o4[1], o4[2], o4[3]));
             }
         }
     }
@@ -365,6 +516,33 @@ tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, in
     return launch_status();
 }
 
+// Slots a lane needs for one folded pair, at most: with na + nb <= period + 1 +
+// 2 offset open vectors (ceil(a/E) + ceil(b/E) <= ceil((a+b)/E) + 1),
+// ceil(na/32) + ceil(nb/32) <= ceil((na+nb)/32) + 1; and never more than two whole
+// rows' worth.  (Called with period <= rows and offset <= cols: nothing overflows.)
+int64_t pair_slots(int64_t nv, int E, int64_t period, int64_t offset) {
+    const int64_t vec = (period + 1 + 2 * offset + E - 1) / E + 1;
+    return std::min<int64_t>(2 * ((nv + 31) / 32), (vec + 31) / 32 + 1);
+}
+
+template <class Fmt, int VPL, bool kEvenOdd>
+tb_status launch_pair(const void* dY, const void* P, void* dX, int64_t rows, int nv,
+                      int64_t period, int64_t offset, int sms, cudaStream_t st) {
+    constexpr int kPairsPerCta = 8;                 // one pair per warp
+    const int per_sm = resident_ctas_per_sm(
+        reinterpret_cast<const void*>(&softmax_bwd_causal_pair_kernel<Fmt, VPL, kEvenOdd>), 256, 0);
+    if (per_sm == 0) return TB_ERR_CUDA;
+    const int64_t npairs = ((rows + period - 1) / period) * ((period + 1) / 2);
+    const int64_t want = (npairs + kPairsPerCta - 1) / kPairsPerCta;
+    const int64_t grid = grid_for(want, 2 * kPairsPerCta, (int64_t)nv * Vec<Fmt>::kElems, period,
+                                  offset, sizeof(typename Fmt::T), sms, per_sm);
+    if (launch_pdl(softmax_bwd_causal_pair_kernel<Fmt, VPL, kEvenOdd>, dim3((unsigned)grid), dim3(256), 0, st,
+                   static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
+                   static_cast<uint4*>(dX), rows, nv, period, offset, npairs) != cudaSuccess)
+        return TB_ERR_CUDA;
+    return launch_status();
+}
+
 template <class Fmt, int VPL>
 tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int nv,
                      int64_t period, int64_t offset, int sms, cudaStream_t st) {
@@ -386,6 +564,21 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
     constexpr int E = Vec<Fmt>::kElems;
     if (aligned && cols % E == 0 && cols / E <= 2048) {
         const int nv = (int)(cols / E);
+        if constexpr (sizeof(typename Fmt::T) == 2) {
+            // causal blocks that fit in the rows, rows of 65..128 vectors: folded pairs,
+            // one per warp, at the same three CTAs per SM as the one-row kernel there
+            // (shorter rows run the one-row kernel at up to five CTAs per SM, longer
+            // ones need more slots than fit in its registers; both measured slower
+            // as pairs)
+            if (period > 0 && period <= rows && nv > 64 && nv <= 128) {
+                // the sum order of the one-row kernel: one running sum for bf16, even
+                // and odd elements apart for fp16
+                constexpr bool kEvenOdd = std::is_same<Fmt, F16>::value;
+                const int64_t k = pair_slots(nv, E, period, offset);
+                if (k <= 4) return launch_pair<Fmt, 4, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
+                if (k <= 6) return launch_pair<Fmt, 6, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
+            }
+        }
         if (nv <= 4) return launch_group<Fmt, 4, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 8) return launch_group<Fmt, 8, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 16) return launch_group<Fmt, 16, 1>(dY, P, dX, rows, nv, period, offset, sms, st);

@@ -85,7 +85,7 @@ def test_row_length_sweep(tb, synth, cols, dtype):
 @pytest.mark.parametrize("rows, cols, dtype, period", [
     (4000, 1024, torch.float32, 0),        # warp per row, 96 KB per CTA: one CTA per group
     (4000, 128, torch.float32, 0),         # warp per row, 12 KB per CTA: persistent
-    (4000, 1024, torch.bfloat16, 1024),    # causal, about 33 KB per CTA: persistent
+    (4000, 512, torch.bfloat16, 512),      # causal, about 16 KB per CTA: persistent
     (4000, 1024, torch.float32, 1024),     # causal, about 66 KB per CTA: one CTA per group
     (2000, 4096, torch.float32, 0),        # CTA per row, 48 KB: one CTA per row
     (2000, 2048, torch.float32, 0),        # CTA per row, 24 KB: persistent
@@ -184,6 +184,38 @@ def test_causal_variant_shapes(tb, synth, rows, cols, period, offset, dtype):
     dX = torch.full_like(P, float("nan"))
     tb.tb_softmax_bwd_causal(dY, P, dX, period=period, offset=offset)
     check(dX, P, dY)
+
+
+# Folded pairs (16-bit causal rows of 65..128 vectors with period <= rows: rows q and
+# period-1-q of a block on one warp).  Odd periods (a middle row without a partner),
+# partial last blocks, period 1, period == rows, offsets, both grid regimes, more pairs
+# than a persistent grid holds, both slot counts (4 and 6 vectors a lane); and shapes
+# beside the band (shorter and longer rows, pairs that would need more slots) that
+# stay on the one-row kernel.
+PAIRS = [(2500, 1024, 1024, 0), (2049, 1024, 1023, 3), (1000, 768, 333, 0), (640, 1024, 640, 0),
+         (600, 520, 1, 7), (20000, 1024, 256, 0), (20000, 528, 528, 0), (1100, 1016, 1016, 5),
+         (777, 256, 256, 0), (1000, 512, 333, 0), (2100, 2048, 2048, 0), (1500, 1024, 1500, 0),
+         (300, 1024, 256, 768)]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("rows, cols, period, offset", PAIRS)
+def test_causal_folded_pairs(tb, synth, rows, cols, period, offset, dtype):
+    P, dY = synth.softmax_inputs(rows, cols, dtype, seed=7 * rows + period, device="cuda",
+                                 causal_period=period, causal_offset=offset)
+    dX = torch.full_like(P, float("nan"))
+    tb.tb_softmax_bwd_causal(dY, P, dX, period=period, offset=offset)
+    # vectors of 8 columns that hold no open column are written as +0
+    r = torch.arange(rows, device="cuda")[:, None] % period
+    c = torch.arange(cols, device="cuda")[None, :]
+    closed = (c // 8) * 8 >= r + 1 + offset
+    assert torch.all(dX.view(torch.int16)[closed] == 0)
+    check(dX, P, dY)
+    # each row summed in the dense kernel's order (its extra terms are exact zeros)
+    dense = torch.empty_like(P)
+    tb.tb_softmax_bwd(dY, P, dense)
+    torch.cuda.synchronize()
+    assert torch.equal(dX, dense)
 
 
 def test_causal_variant_rejects_bad_period(tb, synth):
