@@ -12,7 +12,7 @@
 //
 // Paths, chosen on the host:
 //   group : rows of <= 256 vectors (1024 fp32 / 2048 16-bit), G lanes per row
-//   pairs : causal 16-bit rows of 65..128 vectors (520..1024 columns) whose causal
+//   pairs : causal 16-bit rows of 65..256 vectors (520..2048 columns) whose causal
 //           block fits in the rows: rows q and period-1-q of a block on one warp
 //   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
@@ -239,7 +239,7 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
 }
 
 // ------------------------------------------------------------------ folded causal pairs
-// 16-bit causal rows of 65..128 vectors.  Inside one causal block of `period` rows,
+// 16-bit causal rows of 65..256 vectors.  Inside one causal block of `period` rows,
 // row q opens min(cols, q + 1 + offset) columns and row period-1-q opens
 // min(cols, period - q + offset): the two together open about period + 1 + 2 offset
 // columns wherever q lies.  A warp takes such a pair, so every warp keeps about the
@@ -255,9 +255,10 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
 // partial block are skipped.  VPL >= ceil(na / 32) + ceil(nb / 32) for every pair
 // (checked on the host); a larger pair would lose vectors, never touch other memory.
 // kEvenOdd: a lane sums even and odd elements apart and adds the two at the end, the
-// order of the one-row kernel's packed pairs (fp16 rows); otherwise one running sum.
+// order of the one-row kernel's packed pairs (bf16 rows of more than 128 vectors, fp16
+// rows of up to 128); otherwise one running sum.
 template <class Fmt, int VPL, bool kEvenOdd>
-__global__ void __launch_bounds__(256, 3)
+__global__ void __launch_bounds__(256, VPL <= 6 ? 3 : 2)
 softmax_bwd_causal_pair_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
                                uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
                                int64_t offset, int64_t npairs) {
@@ -526,7 +527,7 @@ int64_t pair_slots(int64_t nv, int E, int64_t period, int64_t offset) {
 }
 
 template <class Fmt, int VPL, bool kEvenOdd>
-tb_status launch_pair(const void* dY, const void* P, void* dX, int64_t rows, int nv,
+tb_status launch_pair_vpl(const void* dY, const void* P, void* dX, int64_t rows, int nv,
                       int64_t period, int64_t offset, int sms, cudaStream_t st) {
     constexpr int kPairsPerCta = 8;                 // one pair per warp
     const int per_sm = resident_ctas_per_sm(
@@ -541,6 +542,15 @@ tb_status launch_pair(const void* dY, const void* P, void* dX, int64_t rows, int
                    static_cast<uint4*>(dX), rows, nv, period, offset, npairs) != cudaSuccess)
         return TB_ERR_CUDA;
     return launch_status();
+}
+
+// The smallest instance with at least k slots a lane (k <= 10).
+template <class Fmt, bool kEvenOdd>
+tb_status launch_pair(int64_t k, const void* dY, const void* P, void* dX, int64_t rows, int nv,
+                      int64_t period, int64_t offset, int sms, cudaStream_t st) {
+    if (k <= 4) return launch_pair_vpl<Fmt, 4, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
+    if (k <= 6) return launch_pair_vpl<Fmt, 6, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
+    return launch_pair_vpl<Fmt, 10, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
 }
 
 template <class Fmt, int VPL>
@@ -565,18 +575,19 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
     if (aligned && cols % E == 0 && cols / E <= 2048) {
         const int nv = (int)(cols / E);
         if constexpr (sizeof(typename Fmt::T) == 2) {
-            // causal blocks that fit in the rows, rows of 65..128 vectors: folded pairs,
-            // one per warp, at the same three CTAs per SM as the one-row kernel there
-            // (shorter rows run the one-row kernel at up to five CTAs per SM, longer
-            // ones need more slots than fit in its registers; both measured slower
-            // as pairs)
-            if (period > 0 && period <= rows && nv > 64 && nv <= 128) {
-                // the sum order of the one-row kernel: one running sum for bf16, even
-                // and odd elements apart for fp16
-                constexpr bool kEvenOdd = std::is_same<Fmt, F16>::value;
+            // causal blocks that fit in the rows, rows of 65..256 vectors: folded pairs,
+            // one per warp, at the occupancy of the one-row kernel there (3 CTAs per SM
+            // up to 6 slots a lane, 2 beyond).  Shorter rows run the one-row kernel at
+            // up to five CTAs per SM, which measured faster than pairs.
+            if (period > 0 && period <= rows && nv > 64 && nv <= 256) {
                 const int64_t k = pair_slots(nv, E, period, offset);
-                if (k <= 4) return launch_pair<Fmt, 4, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
-                if (k <= 6) return launch_pair<Fmt, 6, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
+                // the one-row kernel's sum order: even and odd elements apart where it
+                // takes packed pairs (bf16 rows of more than 128 vectors, fp16 rows of
+                // up to 128), else one running sum
+                const bool eo = std::is_same<Fmt, BF16>::value ? nv > 128 : nv <= 128;
+                if (k <= 6 || (nv > 128 && k <= 10))
+                    return eo ? launch_pair<Fmt, true>(k, dY, P, dX, rows, nv, period, offset, sms, st)
+                              : launch_pair<Fmt, false>(k, dY, P, dX, rows, nv, period, offset, sms, st);
             }
         }
         if (nv <= 4) return launch_group<Fmt, 4, 1>(dY, P, dX, rows, nv, period, offset, sms, st);

@@ -186,16 +186,18 @@ def test_causal_variant_shapes(tb, synth, rows, cols, period, offset, dtype):
     check(dX, P, dY)
 
 
-# Folded pairs (16-bit causal rows of 65..128 vectors with period <= rows: rows q and
+# Folded pairs (16-bit causal rows of 65..256 vectors with period <= rows: rows q and
 # period-1-q of a block on one warp).  Odd periods (a middle row without a partner),
-# partial last blocks, period 1, period == rows, offsets, both grid regimes, more pairs
-# than a persistent grid holds, both slot counts (4 and 6 vectors a lane); and shapes
-# beside the band (shorter and longer rows, pairs that would need more slots) that
-# stay on the one-row kernel.
+# partial last blocks, period 1, period == rows, periods longer than the row, offsets,
+# both grid regimes, more pairs than a persistent grid holds, every slot count (4, 6
+# and 10 vectors a lane) and both sum orders; and shapes beside them (shorter rows,
+# pairs that would need more slots) that stay on the one-row kernel.
 PAIRS = [(2500, 1024, 1024, 0), (2049, 1024, 1023, 3), (1000, 768, 333, 0), (640, 1024, 640, 0),
          (600, 520, 1, 7), (20000, 1024, 256, 0), (20000, 528, 528, 0), (1100, 1016, 1016, 5),
-         (777, 256, 256, 0), (1000, 512, 333, 0), (2100, 2048, 2048, 0), (1500, 1024, 1500, 0),
-         (300, 1024, 256, 768)]
+         (2100, 2048, 2048, 0), (3000, 2048, 1024, 0), (1500, 2048, 1500, 0), (2100, 1040, 1040, 0),
+         (4100, 2048, 2048, 9), (3000, 1536, 1536, 0),
+         (777, 256, 256, 0), (1000, 512, 333, 0), (1500, 1024, 1500, 0), (300, 1024, 256, 768),
+         (300, 2048, 256, 1800)]
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
