@@ -14,7 +14,8 @@
 //   group : rows of <= 256 vectors (1024 fp32 / 2048 16-bit), G lanes per row
 //   pairs : causal 16-bit rows of 65..256 vectors (520..2048 columns) whose causal
 //           block fits in the rows: rows q and period-1-q of a block on one warp
-//   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row
+//   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row;
+//           causal 16-bit rows: rows q and period-1-q on one CTA of 128..512 threads
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
 // The group and CTA paths launch one CTA per row group when a CTA carries enough
 // traffic (the hardware scheduler then balances the SMs), else a persistent grid.
@@ -426,6 +427,119 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
     }
 }
 
+// Folded pairs on the CTA path: 16-bit causal rows of 257..2048 vectors whose causal
+// block fits in the rows.  One CTA of T threads (128, 256 or 512: the smallest that
+// needs at most six slots a thread) takes rows q and period-1-q of a block, as the warp
+// version above does, so every CTA streams about one row's worth per pair.  (T = 256
+// also takes up to ten slots, at two CTAs per SM.)  With one
+// row per 512-thread CTA, most of a CTA's threads load nothing on a block's short rows
+// and wait at the barrier; smaller CTAs let several pairs per SM overlap one another's
+// barrier and loads.  Thread t holds vectors t, t + T, ... of the first row in its
+// first slots and the same vectors of the second row after them, sums them in order,
+// then each warp's butterfly and the warp sums in warp order.  (At T = 512 that is the
+// one-row CTA kernel's order, so the results equal it bit for bit; smaller T sums the
+// same terms in another grouping.)  Masked vectors are written as +0 while the loads
+// are in flight; one barrier per pair.  Launch bounds hold 2, 4, 6 and 8..10 slots to
+// 32, 64, 85 and 128 registers a thread.
+constexpr int cta_pair_regs(int VPL) { return VPL <= 2 ? 32 : VPL <= 4 ? 64 : VPL <= 6 ? 85 : 128; }
+constexpr int cta_pair_min_blocks(int T, int VPL) {
+    return 65536 / (T * cta_pair_regs(VPL)) > 0 ? 65536 / (T * cta_pair_regs(VPL)) : 1;
+}
+
+template <class Fmt, int T, int VPL>
+__global__ void __launch_bounds__(T, cta_pair_min_blocks(T, VPL))
+softmax_bwd_causal_cta_pair_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
+                                   uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
+                                   int64_t offset, int64_t npairs) {
+    constexpr int E = Vec<Fmt>::kElems;
+    static_assert(E == 8, "16-bit rows only");
+    constexpr int kWarps = T / 32;
+    __shared__ float red[2][2][kWarps];
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int64_t per_block = (period + 1) / 2;
+    const int64_t cols = (int64_t)nv * E;
+    int parity = 0;
+    for (int64_t pi = blockIdx.x; pi < npairs; pi += gridDim.x, parity ^= 1) {
+        const int64_t blk = pi / per_block;
+        const int64_t q = pi - blk * per_block;
+        const int64_t ra = blk * period + q;
+        const int64_t rb = blk * period + (period - 1 - q);
+        const bool live_a = ra < rows;
+        const bool live_b = rb != ra && rb < rows;
+        const int64_t ca = q + 1 + offset, cb = period - q + offset;
+        const int na = live_a ? (int)(((ca < cols ? ca : cols) + E - 1) / E) : 0;
+        const int nb = live_b ? (int)(((cb < cols ? cb : cols) + E - 1) / E) : 0;
+        const int ka = (na + T - 1) / T;   // slots of row a (CTA-uniform)
+        const int64_t offa = ra * (int64_t)nv;
+        const int64_t offb = rb * (int64_t)nv;
+        uint4 p[VPL], d[VPL];
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const bool in_a = k < ka;
+            const int v = tid + T * (in_a ? k : k - ka);
+            if (v < (in_a ? na : nb)) {
+                const int64_t o = (in_a ? offa : offb) + v;
+                p[k] = __ldcs(P + o);
+                d[k] = __ldcs(dY + o);
+            } else {
+                p[k] = make_uint4(0u, 0u, 0u, 0u);
+                d[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        {   // masked vectors, row a's [na, nv) then row b's [nb, nv)
+            const int ma = live_a ? nv - na : 0;
+            const int mb = live_b ? nv - nb : 0;
+            uint4* const za = live_a ? dX + offa + na : dX;
+            uint4* const zb = live_b ? dX + offb + nb - ma : dX;   // index j >= ma: zb + j
+            for (int j = tid; j < ma + mb; j += T)
+                __stcs((j < ma ? za : zb) + j, make_uint4(0u, 0u, 0u, 0u));
+        }
+        float da = 0.f, db = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const bool in_a = k < ka;
+            float acc = in_a ? da : db;
+            const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
+            const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc = fma_mix<Fmt>(pw[e / 2], dw[e / 2], e & 1, acc);
+            if (in_a) da = acc; else db = acc;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            da += __shfl_xor_sync(0xffffffffu, da, o);
+            db += __shfl_xor_sync(0xffffffffu, db, o);
+        }
+        if (lane == 0) {
+            red[parity][0][wid] = da;
+            red[parity][1][wid] = db;
+        }
+        __syncthreads();   // one barrier per pair: the other buffer is reused two pairs later
+        da = 0.f;
+        db = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            da += red[parity][0][w];
+            db += red[parity][1][w];
+        }
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const bool in_a = k < ka;
+            const int v = tid + T * (in_a ? k : k - ka);
+            if (v < (in_a ? na : nb)) {
+                const float dot = in_a ? da : db;
+                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+                float out[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) out[e] = vec_elem<Fmt>(p[k], e) * sub_mix<Fmt>(dw[e / 2], e & 1, dot);
+                __stcs(dX + (in_a ? offa : offb) + v, vec_from<Fmt>(out));
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ two-pass path
 constexpr int kTwoPassThreads = 256;
 
@@ -517,13 +631,14 @@ tb_status launch_group(const void* dY, const void* P, void* dX, int64_t rows, in
     return launch_status();
 }
 
-// Slots a lane needs for one folded pair, at most: with na + nb <= period + 1 +
-// 2 offset open vectors (ceil(a/E) + ceil(b/E) <= ceil((a+b)/E) + 1),
-// ceil(na/32) + ceil(nb/32) <= ceil((na+nb)/32) + 1; and never more than two whole
-// rows' worth.  (Called with period <= rows and offset <= cols: nothing overflows.)
-int64_t pair_slots(int64_t nv, int E, int64_t period, int64_t offset) {
+// Slots a thread needs for one folded pair whose vectors are dealt over `lanes`
+// threads, at most: with na + nb <= period + 1 + 2 offset open vectors
+// (ceil(a/E) + ceil(b/E) <= ceil((a+b)/E) + 1), ceil(na/lanes) + ceil(nb/lanes) <=
+// ceil((na+nb)/lanes) + 1; and never more than two whole rows' worth.  (Called with
+// period <= rows and offset <= cols: nothing overflows.)
+int64_t pair_slots(int64_t nv, int E, int64_t period, int64_t offset, int64_t lanes = 32) {
     const int64_t vec = (period + 1 + 2 * offset + E - 1) / E + 1;
-    return std::min<int64_t>(2 * ((nv + 31) / 32), (vec + 31) / 32 + 1);
+    return std::min<int64_t>(2 * ((nv + lanes - 1) / lanes), (vec + lanes - 1) / lanes + 1);
 }
 
 template <class Fmt, int VPL, bool kEvenOdd>
@@ -551,6 +666,42 @@ tb_status launch_pair(int64_t k, const void* dY, const void* P, void* dX, int64_
     if (k <= 4) return launch_pair_vpl<Fmt, 4, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
     if (k <= 6) return launch_pair_vpl<Fmt, 6, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
     return launch_pair_vpl<Fmt, 10, kEvenOdd>(dY, P, dX, rows, nv, period, offset, sms, st);
+}
+
+template <class Fmt, int T, int VPL>
+tb_status launch_cta_pair_vpl(const void* dY, const void* P, void* dX, int64_t rows, int nv,
+                              int64_t period, int64_t offset, int sms, cudaStream_t st) {
+    const int per_sm = resident_ctas_per_sm(
+        reinterpret_cast<const void*>(&softmax_bwd_causal_cta_pair_kernel<Fmt, T, VPL>), T, 0);
+    if (per_sm == 0) return TB_ERR_CUDA;
+    const int64_t npairs = ((rows + period - 1) / period) * ((period + 1) / 2);
+    const int64_t grid = grid_for(npairs, 2, (int64_t)nv * Vec<Fmt>::kElems, period, offset,
+                                  sizeof(typename Fmt::T), sms, per_sm);
+    if (launch_pdl(softmax_bwd_causal_cta_pair_kernel<Fmt, T, VPL>, dim3((unsigned)grid), dim3(T),
+                   0, st, static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
+                   static_cast<uint4*>(dX), rows, nv, period, offset, npairs) != cudaSuccess)
+        return TB_ERR_CUDA;
+    return launch_status();
+}
+
+// The instance of T threads with the fewest slots a thread, at least k: 2..6 slots at
+// T = 128, 4..10 at T = 256, 6 at T = 512 (a pair that fits fewer slots of a larger CTA
+// fits a smaller CTA, which the host prefers).
+template <class Fmt, int T>
+tb_status launch_cta_pair_t(int64_t k, const void* dY, const void* P, void* dX, int64_t rows, int nv,
+                            int64_t period, int64_t offset, int sms, cudaStream_t st) {
+    if constexpr (T == 128) {
+        if (k <= 2) return launch_cta_pair_vpl<Fmt, T, 2>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (k <= 4) return launch_cta_pair_vpl<Fmt, T, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
+        return launch_cta_pair_vpl<Fmt, T, 6>(dY, P, dX, rows, nv, period, offset, sms, st);
+    } else if constexpr (T == 256) {
+        if (k <= 4) return launch_cta_pair_vpl<Fmt, T, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (k <= 6) return launch_cta_pair_vpl<Fmt, T, 6>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (k <= 8) return launch_cta_pair_vpl<Fmt, T, 8>(dY, P, dX, rows, nv, period, offset, sms, st);
+        return launch_cta_pair_vpl<Fmt, T, 10>(dY, P, dX, rows, nv, period, offset, sms, st);
+    } else {
+        return launch_cta_pair_vpl<Fmt, T, 6>(dY, P, dX, rows, nv, period, offset, sms, st);
+    }
 }
 
 template <class Fmt, int VPL>
@@ -597,6 +748,18 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
         if (nv <= 64) return launch_group<Fmt, 32, 2>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 128) return launch_group<Fmt, 32, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 256) return launch_group<Fmt, 32, 8>(dY, P, dX, rows, nv, period, offset, sms, st);
+        // 16-bit causal rows whose causal blocks fit in the rows: folded pairs, one per
+        // CTA of the fewest threads that need at most six slots each (128) or ten (256)
+        if constexpr (sizeof(typename Fmt::T) == 2) {
+            if (period > 0 && period <= rows) {
+                int64_t k = pair_slots(nv, E, period, offset, 128);
+                if (k <= 6) return launch_cta_pair_t<Fmt, 128>(k, dY, P, dX, rows, nv, period, offset, sms, st);
+                k = pair_slots(nv, E, period, offset, 256);
+                if (k <= 10) return launch_cta_pair_t<Fmt, 256>(k, dY, P, dX, rows, nv, period, offset, sms, st);
+                k = pair_slots(nv, E, period, offset, 512);
+                if (k <= 6) return launch_cta_pair_t<Fmt, 512>(k, dY, P, dX, rows, nv, period, offset, sms, st);
+            }
+        }
         if (nv <= 512) return launch_cta<Fmt, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 1024) return launch_cta<Fmt, 2>(dY, P, dX, rows, nv, period, offset, sms, st);
         return launch_cta<Fmt, 4>(dY, P, dX, rows, nv, period, offset, sms, st);

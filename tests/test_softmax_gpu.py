@@ -220,6 +220,45 @@ def test_causal_folded_pairs(tb, synth, rows, cols, period, offset, dtype):
     assert torch.equal(dX, dense)
 
 
+# Folded pairs on the CTA path (16-bit causal rows of 257..2048 vectors, 2,056..16,384
+# columns: rows q and period-1-q of a block on one CTA of 128, 256 or 512 threads).  Every
+# instance that can be chosen (128 threads with 2, 4 or 6 slots a thread, 256 with 4, 6, 8
+# or 10, 512 with 6), full blocks plus partial ones, odd periods with offsets, periods
+# shorter than the row, row lengths that are not a multiple of the CTA, and period 1.  fp32 rows of the same
+# shapes stay on the one-row CTA kernel.  CTAs of fewer than 512 threads group each row's
+# sum differently from the dense kernel, so the check is the oracle's, plus bitwise
+# repeatability.
+CTA_PAIRS = [(4500, 4096, 4096, 0), (4500, 6144, 4095, 3), (3000, 8192, 2048, 0),
+             (2100, 4104, 2000, 7), (600, 4112, 1, 0), (3000, 2560, 2560, 0),
+             (5700, 6144, 5600, 0), (2053, 8192, 2048, 3100), (1030, 12288, 1024, 5000),
+             (1027, 16384, 1024, 7700), (1027, 16384, 1024, 9000)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
+                         ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("rows, cols, period, offset", CTA_PAIRS)
+def test_causal_folded_pairs_cta(tb, synth, rows, cols, period, offset, dtype):
+    if cols * torch.tensor([], dtype=dtype).element_size() > 2048 * 16:
+        pytest.skip("rows of more than 2048 vectors take the two-pass kernel")
+    P, dY = synth.softmax_inputs(rows, cols, dtype, seed=3 * rows + period, device="cuda",
+                                 causal_period=period, causal_offset=offset)
+    dX = torch.full_like(P, float("nan"))
+    tb.tb_softmax_bwd_causal(dY, P, dX, period=period, offset=offset)
+    E = 16 // P.element_size()
+    r = torch.arange(rows, device="cuda")[:, None] % period
+    c = torch.arange(cols, device="cuda")[None, :]
+    closed = (c // E) * E >= r + 1 + offset
+    itype = torch.int32 if dtype == torch.float32 else torch.int16
+    assert torch.all(dX.view(itype)[closed] == 0)
+    again = torch.full_like(P, float("nan"))
+    tb.tb_softmax_bwd_causal(dY, P, again, period=period, offset=offset)
+    torch.cuda.synchronize()
+    assert torch.equal(dX.view(itype), again.view(itype))
+    step = max(1, (1 << 23) // cols)
+    for r0 in range(0, rows, step):
+        check(dX[r0:r0 + step], P[r0:r0 + step], dY[r0:r0 + step])
+
+
 def test_causal_variant_rejects_bad_period(tb, synth):
     P, dY = synth.softmax_inputs(8, 64, torch.float32, seed=3, device="cuda")
     with pytest.raises(tb.TbError):
