@@ -831,6 +831,25 @@ HIDDEN_SWEEP_SHAPES = ("bf16:256,bf16:512,bf16:768,bf16:1024,bf16:1536,bf16:2048
                        "f32:12288,f32:16384")
 
 
+def sweep_best_ms(fn, reps):
+    """Best of three CUDA-event timings of `reps` back-to-back calls, after three warm-up
+    calls, in ms per call (the hidden-size and causal sweeps)."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(3):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        best = min(best, s.elapsed_time(e) / reps)
+    return best
+
+
 def run_hidden_sweep(args):
     """LayerNorm and RMSNorm backward over hidden sizes D, each with as many rows as
     make one input tensor args.sweep_mb MB: the short-row ring, the 512-thread ring
@@ -844,22 +863,7 @@ def run_hidden_sweep(args):
     peak, peak_kind = measured_peak()
     dtypes = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 
-    def best_ms(fn, reps):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        best = float("inf")
-        for _ in range(3):
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record()
-            for _ in range(reps):
-                fn()
-            e.record()
-            torch.cuda.synchronize()
-            best = min(best, s.elapsed_time(e) / reps)
-        return best
-
-    for item in args.sweep_shapes.split(","):
+    for item in (args.sweep_shapes or HIDDEN_SWEEP_SHAPES).split(","):
         name, d = item.split(":")
         dt, D = dtypes[name], int(d)
         es = torch.empty((), dtype=dt).element_size()
@@ -880,12 +884,59 @@ def run_hidden_sweep(args):
                 fn()
                 torch.cuda.synchronize()
                 continue
-            ms = best_ms(fn, args.sweep_reps)
+            ms = sweep_best_ms(fn, args.sweep_reps)
             gbs = nbytes / ms / 1e6
             print(json.dumps({"sweep": "hidden", "op": op, "dtype": name, "D": D, "rows": rows,
                               "us": round(ms * 1e3, 1), "GB_s": round(gbs, 1),
                               "frac": round(gbs / peak, 3), "peak": f"{peak:.1f} ({peak_kind})"}))
         del x, dy, dX, ws, wr
+        torch.cuda.empty_cache()
+    if tb.tb_device_error(reset=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during the sweep")
+
+
+CAUSAL_SWEEP_SHAPES = ("bf16:256,bf16:512,bf16:768,bf16:1024,bf16:2048,bf16:3072,bf16:4096,"
+                       "bf16:8192,bf16:12288,bf16:16384,f16:1024,f16:4096,f32:512,f32:1024,"
+                       "f32:2048,f32:4096,f32:8192")
+
+
+def run_causal_sweep(args):
+    """Causal softmax backward over sequence lengths S: rows of S columns in whole S x S
+    causal blocks (period S; as many blocks as make one input tensor args.sweep_mb MB, at
+    least one), with the dense call on the same tensors beside it.  One JSON line per
+    dtype and S; not part of the benchmark contract.  With --sweep-reps 0 each shape is
+    called once, untimed (for profiler captures)."""
+    import torch
+    import ln_backward_gb300 as tb
+    from ln_backward_gb300 import synth
+    dev = torch.device("cuda")
+    peak, peak_kind = measured_peak()
+    dtypes = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+    for item in (args.sweep_shapes or CAUSAL_SWEEP_SHAPES).split(","):
+        name, s = item.split(":")
+        dt, S = dtypes[name], int(s)
+        es = torch.empty((), dtype=dt).element_size()
+        rows = S * max(1, (args.sweep_mb << 20) // (S * S * es))
+        P, dY = synth.softmax_inputs(rows, S, dt, seed=S, device=dev, causal_period=S)
+        dX = torch.empty_like(P)
+        causal = lambda: tb.tb_softmax_bwd_causal(dY, P, dX, period=S)
+        dense = lambda: tb.tb_softmax_bwd(dY, P, dX)
+        if args.sweep_reps == 0:
+            causal()
+            dense()
+            torch.cuda.synchronize()
+        else:
+            cb = causal_softmax_bytes(rows, S, S, 0, es)
+            db = softmax_bytes(rows, S, es)
+            cms = sweep_best_ms(causal, args.sweep_reps)
+            dms = sweep_best_ms(dense, args.sweep_reps)
+            print(json.dumps({"sweep": "causal_softmax", "dtype": name, "S": S, "rows": rows,
+                              "us": round(cms * 1e3, 1), "GB_s": round(cb / cms / 1e6, 1),
+                              "frac": round(cb / cms / 1e6 / peak, 3),
+                              "dense_us": round(dms * 1e3, 1),
+                              "dense_frac": round(db / dms / 1e6 / peak, 3),
+                              "peak": f"{peak:.1f} ({peak_kind})"}))
+        del P, dY, dX
         torch.cuda.empty_cache()
     if tb.tb_device_error(reset=True) != 0:
         raise RuntimeError("a kernel's bounded wait gave up during the sweep")
@@ -909,17 +960,23 @@ def main(argv=None):
     ap.add_argument("--sweep-hidden", action="store_true",
                     help="time the LayerNorm/RMSNorm backward over hidden sizes (one JSON "
                          "line per op, dtype and D)")
-    ap.add_argument("--sweep-shapes", default=HIDDEN_SWEEP_SHAPES,
-                    help="dtype:D list for --sweep-hidden (dtype bf16, f16 or f32)")
+    ap.add_argument("--sweep-causal", action="store_true",
+                    help="time the causal softmax backward over sequence lengths S (whole "
+                         "S x S causal blocks; one JSON line per dtype and S)")
+    ap.add_argument("--sweep-shapes", default=None,
+                    help="dtype:D (or dtype:S) list for --sweep-hidden and --sweep-causal "
+                         "(dtype bf16, f16 or f32)")
     ap.add_argument("--sweep-mb", type=int, default=256,
-                    help="MB per input tensor for --sweep-hidden")
+                    help="MB per input tensor for --sweep-hidden and --sweep-causal")
     ap.add_argument("--sweep-reps", type=int, default=20,
-                    help="timed calls per repetition for --sweep-hidden (0: one untimed call)")
+                    help="timed calls per repetition for the sweeps (0: one untimed call)")
     args = ap.parse_args(argv)
     if args.warmup < 1:
         ap.error("--warmup must be >= 1 (timed numbers use the default of 3)")
     if args.sweep_hidden:
         run_hidden_sweep(args)
+    elif args.sweep_causal:
+        run_causal_sweep(args)
     elif args.sweep_layernorm:
         run_layernorm_sweep(args)
     elif args.impl == "reference":

@@ -15,7 +15,7 @@
 //   pairs : causal 16-bit rows of 65..256 vectors (520..2048 columns) whose causal
 //           block fits in the rows: rows q and period-1-q of a block on one warp
 //   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row;
-//           causal 16-bit rows: rows q and period-1-q on one CTA of 128..512 threads
+//           causal rows: rows q and period-1-q on one CTA of 128..512 threads
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
 // The group and CTA paths launch one CTA per row group when a CTA carries enough
 // traffic (the hardware scheduler then balances the SMs), else a persistent grid.
@@ -427,8 +427,8 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
     }
 }
 
-// Folded pairs on the CTA path: 16-bit causal rows of 257..2048 vectors whose causal
-// block fits in the rows.  One CTA of T threads (128, 256 or 512: the smallest that
+// Folded pairs on the CTA path: causal rows of 257..2048 vectors (16-bit rows of
+// 2,056..16,384 columns, fp32 rows of 1,028..8,192) whose causal block fits in the rows.  One CTA of T threads (128, 256 or 512: the smallest that
 // needs at most six slots a thread) takes rows q and period-1-q of a block, as the warp
 // version above does, so every CTA streams about one row's worth per pair.  (T = 256
 // also takes up to ten slots, at two CTAs per SM.)  With one
@@ -452,7 +452,7 @@ softmax_bwd_causal_cta_pair_kernel(const uint4* __restrict__ dY, const uint4* __
                                    uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
                                    int64_t offset, int64_t npairs) {
     constexpr int E = Vec<Fmt>::kElems;
-    static_assert(E == 8, "16-bit rows only");
+    constexpr bool k16 = E == 8;     // 16-bit rows: the mixed-precision forms
     constexpr int kWarps = T / 32;
     __shared__ float red[2][2][kWarps];
     pdl_wait();
@@ -501,10 +501,15 @@ softmax_bwd_causal_cta_pair_kernel(const uint4* __restrict__ dY, const uint4* __
         for (int k = 0; k < VPL; ++k) {
             const bool in_a = k < ka;
             float acc = in_a ? da : db;
-            const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
-            const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+            if constexpr (k16) {
+                const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
+                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
-            for (int e = 0; e < E; ++e) acc = fma_mix<Fmt>(pw[e / 2], dw[e / 2], e & 1, acc);
+                for (int e = 0; e < E; ++e) acc = fma_mix<Fmt>(pw[e / 2], dw[e / 2], e & 1, acc);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc = fmaf(vec_elem<Fmt>(p[k], e), vec_elem<Fmt>(d[k], e), acc);
+            }
             if (in_a) da = acc; else db = acc;
         }
 #pragma unroll
@@ -530,10 +535,15 @@ softmax_bwd_causal_cta_pair_kernel(const uint4* __restrict__ dY, const uint4* __
             const int v = tid + T * (in_a ? k : k - ka);
             if (v < (in_a ? na : nb)) {
                 const float dot = in_a ? da : db;
-                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
                 float out[E];
+                if constexpr (k16) {
+                    const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
-                for (int e = 0; e < E; ++e) out[e] = vec_elem<Fmt>(p[k], e) * sub_mix<Fmt>(dw[e / 2], e & 1, dot);
+                    for (int e = 0; e < E; ++e) out[e] = vec_elem<Fmt>(p[k], e) * sub_mix<Fmt>(dw[e / 2], e & 1, dot);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) out[e] = vec_elem<Fmt>(p[k], e) * (vec_elem<Fmt>(d[k], e) - dot);
+                }
                 __stcs(dX + (in_a ? offa : offb) + v, vec_from<Fmt>(out));
             }
         }
@@ -748,17 +758,15 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
         if (nv <= 64) return launch_group<Fmt, 32, 2>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 128) return launch_group<Fmt, 32, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 256) return launch_group<Fmt, 32, 8>(dY, P, dX, rows, nv, period, offset, sms, st);
-        // 16-bit causal rows whose causal blocks fit in the rows: folded pairs, one per
-        // CTA of the fewest threads that need at most six slots each (128) or ten (256)
-        if constexpr (sizeof(typename Fmt::T) == 2) {
-            if (period > 0 && period <= rows) {
-                int64_t k = pair_slots(nv, E, period, offset, 128);
-                if (k <= 6) return launch_cta_pair_t<Fmt, 128>(k, dY, P, dX, rows, nv, period, offset, sms, st);
-                k = pair_slots(nv, E, period, offset, 256);
-                if (k <= 10) return launch_cta_pair_t<Fmt, 256>(k, dY, P, dX, rows, nv, period, offset, sms, st);
-                k = pair_slots(nv, E, period, offset, 512);
-                if (k <= 6) return launch_cta_pair_t<Fmt, 512>(k, dY, P, dX, rows, nv, period, offset, sms, st);
-            }
+        // causal rows whose causal blocks fit in the rows: folded pairs, one per CTA of
+        // the fewest threads that need at most six slots each (128) or ten (256)
+        if (period > 0 && period <= rows) {
+            int64_t k = pair_slots(nv, E, period, offset, 128);
+            if (k <= 6) return launch_cta_pair_t<Fmt, 128>(k, dY, P, dX, rows, nv, period, offset, sms, st);
+            k = pair_slots(nv, E, period, offset, 256);
+            if (k <= 10) return launch_cta_pair_t<Fmt, 256>(k, dY, P, dX, rows, nv, period, offset, sms, st);
+            k = pair_slots(nv, E, period, offset, 512);
+            if (k <= 6) return launch_cta_pair_t<Fmt, 512>(k, dY, P, dX, rows, nv, period, offset, sms, st);
         }
         if (nv <= 512) return launch_cta<Fmt, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
         if (nv <= 1024) return launch_cta<Fmt, 2>(dY, P, dX, rows, nv, period, offset, sms, st);

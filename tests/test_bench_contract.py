@@ -113,3 +113,27 @@ def test_hidden_size_sweep_lines():
                        timeout=600)
     assert p.returncode == 0, p.stdout + p.stderr
     assert not [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+
+
+@pytest.mark.gpu
+def test_causal_sweep_lines():
+    """bench.py --sweep-causal: one JSON line per dtype and S, rows in whole S x S blocks,
+    consistent bandwidth figures; with --sweep-reps 0 it only calls each shape once."""
+    args = [sys.executable, os.path.join(ROOT, "bench.py"), "--sweep-causal", "--sweep-shapes",
+            "bf16:1024,f32:512,bf16:4096", "--sweep-mb", "8"]
+    p = subprocess.run(args + ["--sweep-reps", "2"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert p.returncode == 0, p.stdout + p.stderr
+    lines = [json.loads(ln) for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert [(d["dtype"], d["S"]) for d in lines] == [("bf16", 1024), ("f32", 512), ("bf16", 4096)]
+    for d in lines:
+        es = 4 if d["dtype"] == "f32" else 2
+        S = d["S"]
+        assert d["rows"] == S * max(1, (8 << 20) // (S * S * es))
+        assert d["us"] > 0 and 0 < d["frac"] < 1.5 and 0 < d["dense_frac"] < 1.5
+        peak = float(d["peak"].split()[0])
+        assert abs(d["frac"] * peak - d["GB_s"]) <= 0.0006 * peak + 0.1
+    p = subprocess.run(args + ["--sweep-reps", "0"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert p.returncode == 0, p.stdout + p.stderr
+    assert not [ln for ln in p.stdout.splitlines() if ln.startswith("{")]

@@ -220,14 +220,13 @@ def test_causal_folded_pairs(tb, synth, rows, cols, period, offset, dtype):
     assert torch.equal(dX, dense)
 
 
-# Folded pairs on the CTA path (16-bit causal rows of 257..2048 vectors, 2,056..16,384
-# columns: rows q and period-1-q of a block on one CTA of 128, 256 or 512 threads).  Every
-# instance that can be chosen (128 threads with 2, 4 or 6 slots a thread, 256 with 4, 6, 8
-# or 10, 512 with 6), full blocks plus partial ones, odd periods with offsets, periods
-# shorter than the row, row lengths that are not a multiple of the CTA, and period 1.  fp32 rows of the same
-# shapes stay on the one-row CTA kernel.  CTAs of fewer than 512 threads group each row's
-# sum differently from the dense kernel, so the check is the oracle's, plus bitwise
-# repeatability.
+# Folded pairs on the CTA path (causal rows of 257..2048 vectors: 16-bit rows of 2,056..16,384
+# columns, fp32 of 1,028..8,192; rows q and period-1-q of a block on one CTA of 128, 256 or
+# 512 threads).  Every instance that can be chosen (128 threads with 2, 4 or 6 slots a
+# thread, 256 with 4, 6, 8 or 10, 512 with 6), full blocks plus partial ones, odd periods
+# with offsets, periods shorter than the row, row lengths that are not a multiple of the CTA,
+# and period 1.  CTAs of fewer than 512 threads group each row's sum differently from the
+# dense kernel, so the check is the oracle's, plus bitwise repeatability.
 CTA_PAIRS = [(4500, 4096, 4096, 0), (4500, 6144, 4095, 3), (3000, 8192, 2048, 0),
              (2100, 4104, 2000, 7), (600, 4112, 1, 0), (3000, 2560, 2560, 0),
              (5700, 6144, 5600, 0), (2053, 8192, 2048, 3100), (1030, 12288, 1024, 5000),
