@@ -372,8 +372,12 @@ softmax_bwd_causal_pair_kernel(const uint4* __restrict__ dY, const uint4* __rest
 // ------------------------------------------------------------------ CTA path
 constexpr int kCtaThreads = 512;
 
+// 16-bit rows take the mixed-precision forms (fewer registers than widening first, the
+// same values); launch bounds keep four CTAs per SM at one vector a thread, three for
+// fp32 at two, two otherwise.
 template <class Fmt, int VPL>
-__global__ void __launch_bounds__(kCtaThreads)
+__global__ void __launch_bounds__(kCtaThreads,
+                                  VPL <= 1 ? 4 : (VPL <= 2 && sizeof(typename Fmt::T) == 4) ? 3 : 2)
 softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
                        uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
                        int64_t offset) {
@@ -401,9 +405,17 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
         }
         float dot = 0.f;
 #pragma unroll
-        for (int k = 0; k < VPL; ++k)
+        for (int k = 0; k < VPL; ++k) {
+            if constexpr (E == 8) {
+                const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
+                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
-            for (int e = 0; e < E; ++e) dot += vec_elem<Fmt>(p[k], e) * vec_elem<Fmt>(d[k], e);
+                for (int e = 0; e < E; ++e) dot = fma_mix<Fmt>(pw[e / 2], dw[e / 2], e & 1, dot);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) dot += vec_elem<Fmt>(p[k], e) * vec_elem<Fmt>(d[k], e);
+            }
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
         if (lane == 0) red[parity][wid] = dot;
@@ -416,9 +428,15 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
             const int vi = tid + k * kCtaThreads;
             if (vi < nvv) {
                 float out[E];
+                if constexpr (E == 8) {
+                    const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
-                for (int e = 0; e < E; ++e)
-                    out[e] = vec_elem<Fmt>(p[k], e) * (vec_elem<Fmt>(d[k], e) - dot);
+                    for (int e = 0; e < E; ++e) out[e] = vec_elem<Fmt>(p[k], e) * sub_mix<Fmt>(dw[e / 2], e & 1, dot);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e)
+                        out[e] = vec_elem<Fmt>(p[k], e) * (vec_elem<Fmt>(d[k], e) - dot);
+                }
                 __stcs(dX + off + vi, vec_from<Fmt>(out));
             } else if (vi < nv) {
                 __stcs(dX + off + vi, make_uint4(0u, 0u, 0u, 0u));
