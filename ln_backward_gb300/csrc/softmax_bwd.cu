@@ -703,8 +703,11 @@ tb_status launch_cta_pair_vpl(const void* dY, const void* P, void* dX, int64_t r
         reinterpret_cast<const void*>(&softmax_bwd_causal_cta_pair_kernel<Fmt, T, VPL>), T, 0);
     if (per_sm == 0) return TB_ERR_CUDA;
     const int64_t npairs = ((rows + period - 1) / period) * ((period + 1) / 2);
-    const int64_t grid = grid_for(npairs, 2, (int64_t)nv * Vec<Fmt>::kElems, period, offset,
-                                  sizeof(typename Fmt::T), sms, per_sm);
+    // one CTA per pair, whatever its traffic: against the persistent grid the 40 KB rule
+    // would pick, bf16 4,096-column causal rows went from 0.90 to 0.99 of the copy peak,
+    // 2,560 columns from 0.91 to 0.98, fp32 2,048 from 0.91 to 0.99
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(npairs, INT32_MAX));
+    (void)sms;
     if (launch_pdl(softmax_bwd_causal_cta_pair_kernel<Fmt, T, VPL>, dim3((unsigned)grid), dim3(T),
                    0, st, static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
                    static_cast<uint4*>(dX), rows, nv, period, offset, npairs) != cudaSuccess)
