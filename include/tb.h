@@ -307,8 +307,13 @@ tb_status tb_softmax_bwd(const void* dY, const void* P, void* dX,
  * columns: `period` is the query length S_q of one (batch, head) block whose
  * rows are stacked, `offset` = S_k - S_q (0 for square self-attention).  P must
  * be exactly 0 on every other column, as a masked forward softmax leaves it; the
- * kernel never reads those columns of P or dY and writes +0 to dX there.  The
- * result equals tb_softmax_bwd's on such inputs (masked entries are +-0 there).
+ * kernel never reads those columns of P or dY and writes +0 to dX there.  On
+ * such inputs the result equals tb_softmax_bwd's (masked entries are +-0 there)
+ * bit for bit for rows of up to 2,048 16-bit / 1,024 fp32 columns; longer rows
+ * sum the same dot-product terms in another grouping and agree within its fp32
+ * rounding.  Every call on the same inputs returns the same bits.  When a
+ * causal block fits in `rows` (period <= rows), rows q and period-1-q of a block
+ * are processed together, so the work per warp or CTA does not depend on q.
  * HBM traffic per row: reads of the valid columns (rounded up to 16-byte
  * vectors) plus the full row of dX written.
  *   period >= 1, offset >= 0; other arguments and errors as tb_softmax_bwd.
