@@ -14,8 +14,8 @@
 //   group : rows of <= 256 vectors (1024 fp32 / 2048 16-bit), G lanes per row
 //   pairs : causal 16-bit rows of 65..256 vectors (520..2048 columns) whose causal
 //           block fits in the rows: rows q and period-1-q of a block on one warp
-//   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA per row;
-//           causal rows: rows q and period-1-q on one CTA of 128..512 threads
+//   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA of 128..512
+//           threads per row; causal rows: rows q and period-1-q on one such CTA
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
 // The group and CTA paths launch one CTA per row group when a CTA carries enough
 // traffic (the hardware scheduler then balances the SMs), else a persistent grid.
@@ -370,19 +370,20 @@ softmax_bwd_causal_pair_kernel(const uint4* __restrict__ dY, const uint4* __rest
 }
 
 // ------------------------------------------------------------------ CTA path
-constexpr int kCtaThreads = 512;
-
-// 16-bit rows take the mixed-precision forms (fewer registers than widening first, the
-// same values); launch bounds keep four CTAs per SM at one vector a thread, three for
-// fp32 at two, two otherwise.
-template <class Fmt, int VPL>
-__global__ void __launch_bounds__(kCtaThreads,
-                                  VPL <= 1 ? 4 : (VPL <= 2 && sizeof(typename Fmt::T) == 4) ? 3 : 2)
+// One CTA of T threads per row, T the smallest of 128, 256 and 512 that holds the row
+// in at most four vectors a thread: with 512 threads on every row, rows of 257..384
+// vectors left a quarter or more of the threads idle and rows of 513..1024 vectors ran
+// at one or two vectors a thread (bf16 2,056 columns 0.73 of the copy peak, 6,144 0.87;
+// with CTAs sized to the row 0.99 and 1.00).  16-bit rows take the mixed-precision
+// forms (fewer registers than widening first, the same values); launch bounds hold
+// 64 registers a thread, so 2..8 CTAs fit per SM.
+template <class Fmt, int T, int VPL>
+__global__ void __launch_bounds__(T, 65536 / (T * 64))
 softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P,
                        uint4* __restrict__ dX, int64_t rows, int nv, int64_t period,
                        int64_t offset) {
     constexpr int E = Vec<Fmt>::kElems;
-    constexpr int kWarps = kCtaThreads / 32;
+    constexpr int kWarps = T / 32;
     __shared__ float red[2][kWarps];
     pdl_wait();
     pdl_trigger();
@@ -394,7 +395,7 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
         uint4 p[VPL], d[VPL];
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
-            const int vi = tid + k * kCtaThreads;
+            const int vi = tid + k * T;
             if (vi < nvv) {
                 p[k] = __ldcs(P + off + vi);
                 d[k] = __ldcs(dY + off + vi);
@@ -425,7 +426,7 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
         for (int w = 0; w < kWarps; ++w) dot += red[parity][w];
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
-            const int vi = tid + k * kCtaThreads;
+            const int vi = tid + k * T;
             if (vi < nvv) {
                 float out[E];
                 if constexpr (E == 8) {
@@ -735,15 +736,15 @@ tb_status launch_cta_pair_t(int64_t k, const void* dY, const void* P, void* dX, 
     }
 }
 
-template <class Fmt, int VPL>
+template <class Fmt, int T, int VPL>
 tb_status launch_cta(const void* dY, const void* P, void* dX, int64_t rows, int nv,
                      int64_t period, int64_t offset, int sms, cudaStream_t st) {
     const int per_sm = resident_ctas_per_sm(
-        reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, VPL>), kCtaThreads, 0);
+        reinterpret_cast<const void*>(&softmax_bwd_cta_kernel<Fmt, T, VPL>), T, 0);
     if (per_sm == 0) return TB_ERR_CUDA;
     const int64_t grid = grid_for(rows, 1, (int64_t)nv * Vec<Fmt>::kElems, period, offset,
                                   sizeof(typename Fmt::T), sms, per_sm);
-    if (launch_pdl(softmax_bwd_cta_kernel<Fmt, VPL>, dim3((unsigned)grid), dim3(kCtaThreads), 0, st,
+    if (launch_pdl(softmax_bwd_cta_kernel<Fmt, T, VPL>, dim3((unsigned)grid), dim3(T), 0, st,
                    static_cast<const uint4*>(dY), static_cast<const uint4*>(P),
                    static_cast<uint4*>(dX), rows, nv, period, offset) != cudaSuccess)
         return TB_ERR_CUDA;
@@ -789,9 +790,12 @@ tb_status dispatch(const void* dY, const void* P, void* dX, int64_t rows, int64_
             k = pair_slots(nv, E, period, offset, 512);
             if (k <= 6) return launch_cta_pair_t<Fmt, 512>(k, dY, P, dX, rows, nv, period, offset, sms, st);
         }
-        if (nv <= 512) return launch_cta<Fmt, 1>(dY, P, dX, rows, nv, period, offset, sms, st);
-        if (nv <= 1024) return launch_cta<Fmt, 2>(dY, P, dX, rows, nv, period, offset, sms, st);
-        return launch_cta<Fmt, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 384) return launch_cta<Fmt, 128, 3>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 512) return launch_cta<Fmt, 128, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 768) return launch_cta<Fmt, 256, 3>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 1024) return launch_cta<Fmt, 256, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
+        if (nv <= 1536) return launch_cta<Fmt, 512, 3>(dY, P, dX, rows, nv, period, offset, sms, st);
+        return launch_cta<Fmt, 512, 4>(dY, P, dX, rows, nv, period, offset, sms, st);
     }
     using T = typename Fmt::T;
     const int per_sm = resident_ctas_per_sm(

@@ -66,7 +66,7 @@ def test_tiny_config_fp32(tb, synth):
 
 
 COLS = [1, 2, 3, 4, 5, 8, 16, 31, 33, 64, 127, 128, 255, 256, 1000, 1023, 1024, 1025, 2048,
-        2049, 4096, 8192, 8200, 16384, 16392, 20000]
+        2049, 2056, 3072, 4096, 6144, 8192, 8200, 16384, 16392, 20000]
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16],
