@@ -15,10 +15,12 @@
 //   pairs : causal 16-bit rows of 65..256 vectors (520..2048 columns) whose causal
 //           block fits in the rows: rows q and period-1-q of a block on one warp
 //   cta   : rows of <= 2048 vectors (8192 fp32 / 16384 16-bit), one CTA of 128..512
-//           threads per row; causal rows: rows q and period-1-q on one such CTA
+//           threads per row; causal rows whose causal block fits in the rows: rows q
+//           and period-1-q of a block on one CTA of 128..512 threads
 //   twopass: anything longer or not 16-byte aligned; reads the row twice
-// The group and CTA paths launch one CTA per row group when a CTA carries enough
-// traffic (the hardware scheduler then balances the SMs), else a persistent grid.
+// The group, warp-pair and one-row CTA paths launch one CTA per row group when a CTA
+// carries enough traffic (the hardware scheduler then balances the SMs), else a
+// persistent grid; the CTA pairs always launch one CTA per pair.
 //
 // Causal variant (tb_softmax_bwd_causal): row r of an attention block can only be
 // nonzero on its first min(cols, r mod period + 1 + offset) columns (the forward
