@@ -449,19 +449,20 @@ softmax_bwd_cta_kernel(const uint4* __restrict__ dY, const uint4* __restrict__ P
 }
 
 // Folded pairs on the CTA path: causal rows of 257..2048 vectors (16-bit rows of
-// 2,056..16,384 columns, fp32 rows of 1,028..8,192) whose causal block fits in the rows.  One CTA of T threads (128, 256 or 512: the smallest that
-// needs at most six slots a thread) takes rows q and period-1-q of a block, as the warp
-// version above does, so every CTA streams about one row's worth per pair.  (T = 256
-// also takes up to ten slots, at two CTAs per SM.)  With one
-// row per 512-thread CTA, most of a CTA's threads load nothing on a block's short rows
-// and wait at the barrier; smaller CTAs let several pairs per SM overlap one another's
-// barrier and loads.  Thread t holds vectors t, t + T, ... of the first row in its
-// first slots and the same vectors of the second row after them, sums them in order,
-// then each warp's butterfly and the warp sums in warp order.  (At T = 512 that is the
-// one-row CTA kernel's order, so the results equal it bit for bit; smaller T sums the
-// same terms in another grouping.)  Masked vectors are written as +0 while the loads
-// are in flight; one barrier per pair.  Launch bounds hold 2, 4, 6 and 8..10 slots to
-// 32, 64, 85 and 128 registers a thread.
+// 2,056..16,384 columns, fp32 rows of 1,028..8,192) whose causal block fits in the
+// rows.  One CTA of T threads (128 or 256 with up to six slots a thread, 256 with up
+// to ten at two CTAs per SM, else 512 with six) takes rows q and period-1-q of a
+// block, as the warp version above does, so every CTA streams about one row's worth
+// per pair.  With one row per 512-thread CTA, most of a CTA's threads load nothing on
+// a block's short rows and wait at the barrier; smaller CTAs let several pairs per SM
+// overlap one another's barrier and loads.  Thread t holds vectors t, t + T, ... of
+// the first row in its first slots and the same vectors of the second row after them,
+// sums them in order, then each warp's butterfly and the warp sums in warp order: the
+// one-row CTA kernel's order at the same T, so where both pick the same CTA size the
+// results equal the dense kernel's bit for bit, and elsewhere the same terms are
+// grouped differently.  Masked vectors are written as +0 while the loads are in
+// flight; one barrier per pair.  Launch bounds hold 2, 4, 6 and 8..10 slots to 32,
+// 64, 85 and 128 registers a thread.
 constexpr int cta_pair_regs(int VPL) { return VPL <= 2 ? 32 : VPL <= 4 ? 64 : VPL <= 6 ? 85 : 128; }
 constexpr int cta_pair_min_blocks(int T, int VPL) {
     return 65536 / (T * cta_pair_regs(VPL)) > 0 ? 65536 / (T * cta_pair_regs(VPL)) : 1;
