@@ -8,7 +8,10 @@ fp32, every element), the attention config (98,304 x 1,024 causal, fp32 and
 bf16, every element), a sweep of row lengths across every kernel path with a
 ragged row count, unaligned buffers (two-pass path) and empty inputs, and the
 causal variant (reads only the open columns) on the attention config and on
-shapes that exercise every path with row offsets and wrap-around periods.
+shapes that exercise every path with row offsets and wrap-around periods,
+including the folded pairs (rows q and period-1-q of a causal block on one warp
+or one CTA) on every instance the host can pick, with odd periods, partial last
+blocks and large offsets.
 """
 import numpy as np
 import pytest
