@@ -144,8 +144,11 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
     // Packed f32x2 math on 16-bit rows where it measured faster and kept the
     // staged row in registers without spilling (bf16 at 8 vectors per lane,
     // fp16 at up to 4); the scalar form elsewhere.
+    // fp16 rows of up to two vectors a lane: the packed form's sums (even and odd
+    // elements apart) by the mixed-precision forms instead, the same values
+    constexpr bool kMixEO = std::is_same<Fmt, F16>::value && VPL <= 2;
     constexpr bool kPacked = std::is_same<Fmt, BF16>::value ? VPL >= 8
-                           : std::is_same<Fmt, F16>::value ? VPL <= 4 : false;
+                           : std::is_same<Fmt, F16>::value ? VPL <= 4 && !kMixEO : false;
     // bf16 rows of up to two vectors a lane: the dot product and dY - dot by the
     // mixed-precision forms (causal 512-column rows 0.829 -> 0.891 of the copy peak,
     // 256-column rows 0.706 -> 0.798; at four vectors a lane they measured slower)
@@ -195,6 +198,19 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
 #pragma unroll
                 for (int e = 0; e < E; ++e) dot = fma_mix<Fmt>(pw[e / 2], dw[e / 2], e & 1, dot);
             }
+        } else if constexpr (kMixEO) {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const uint32_t pw[4] = {p[k].x, p[k].y, p[k].z, p[k].w};
+                const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    s0 = fma_mix<Fmt>(pw[w], dw[w], 0, s0);
+                    s1 = fma_mix<Fmt>(pw[w], dw[w], 1, s1);
+                }
+            }
+            dot = s0 + s1;
         } else {
 #pragma unroll
             for (int k = 0; k < VPL; ++k)
@@ -222,7 +238,7 @@ softmax_bwd_group_kernel(const uint4* __restrict__ dY, const uint4* __restrict__
                     __stcs(dX + off + vi, make_uint4(o[0], o[1], o[2], o[3]));
                 } else {
                     float out[E];
-                    if constexpr (kMix) {
+                    if constexpr (kMix || kMixEO) {
                         const uint32_t dw[4] = {d[k].x, d[k].y, d[k].z, d[k].w};
 #pragma unroll
                         for (int e = 0; e < E; ++e)
